@@ -1,0 +1,473 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantized decode-time linear layer on one GB300 (or N
+independent replicas, one per GPU, under torchrun).
+
+One step = one full decode projection call on one batch of synthetic input:
+activation quantisation (optionally SiLU-fused) plus the GEMV over all
+segments, for W8A8 workloads; the fused INT4 QKV GEMV for the AWQ workload.
+Steps are replayed from CUDA graphs; the weights rotate over enough copies
+that the working set is several times the L2 cache, so every step streams its
+weights from HBM.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "quantized decode GEMV µs/call & weight-stream GB/s (% of GB300 HBM roofline)"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM traffic per launch of the dominant kernel from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and rows;
+# valid only while the kernel source hash matches.  Source: profiles/.
+TRAFFIC = {}
+
+
+def _rank_world():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _src_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "quantized_decode_linear_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------- workloads
+
+class W8A8Case:
+    """Device buffers for one W8A8 workload at `rows` token rows."""
+
+    def __init__(self, wl, rows, torch, qdl, syn, l2_bytes):
+        self.wl, self.rows = wl, rows
+        segs = syn.w8a8_weights(wl)
+        self.weight_bytes = sum(c.nbytes + s.nbytes for c, s in segs)
+        self.copies = max(1, math.ceil(4 * l2_bytes / self.weight_bytes))
+        base = [(torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda()) for c, s in segs]
+        self.weights = [qdl.w8a8_weight_init(base, wl.fmt)]
+        for _ in range(self.copies - 1):
+            self.weights.append(qdl.w8a8_weight_init([(c.clone(), s.clone()) for c, s in base], wl.fmt))
+        xb = syn.w8a8_activations(wl, rows)
+        self.x_host = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
+        self.x = self.x_host.cuda()
+        k = wl.k
+        self.q = torch.empty((rows, k), dtype=torch.uint8, device="cuda")
+        spr = 1 if wl.fmt == qdl.PER_ROW else k // 128
+        self.s = torch.empty((rows, spr), dtype=torch.float32, device="cuda")
+        self.out = torch.empty((rows, wl.n), dtype=torch.float32, device="cuda")
+        self.out_host = torch.empty((rows, wl.n), dtype=torch.float32).pin_memory()
+        self.qdl = qdl
+        n, K = wl.n, k
+        w_scales = sum(s.nbytes for _, s in segs)
+        x_bytes = rows * (2 * K if wl.silu else K) * 2
+        # algorithmic bytes of one fused call: weights + weight scales + bf16 input + f32 output
+        self.step_bytes = n * K + w_scales + x_bytes + rows * n * 4
+        # of one GEMV launch: weights + scales + e4m3 activations + act scales + output
+        self.gemv_bytes = n * K + w_scales + rows * K + self.s.numel() * 4 + rows * n * 4
+        self.gemv_launches = math.ceil(rows / 16)
+        self.launches_per_step = 1 + self.gemv_launches
+
+    def step(self, i):
+        w = self.weights[i % self.copies]
+        wl, k, qdl = self.wl, self.wl.k, self.qdl
+        if wl.silu:
+            qdl.w8a8_proj_silu(w, self.x[:, :k], self.x[:, k:], self.rows, self.out, self.q, self.s,
+                               ld_gate=2 * k, ld_up=2 * k)
+        else:
+            qdl.w8a8_proj(w, self.x, self.rows, self.out, self.q, self.s)
+
+    def dominant(self, i):
+        self.qdl.w8a8_gemv(self.weights[i % self.copies], self.q, self.s, self.rows, self.out)
+
+    def e2e_step(self, i):
+        self.x.copy_(self.x_host, non_blocking=True)
+        self.step(i)
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def e2e_bytes(self):
+        return self.x_host.numel() * 2, self.out_host.numel() * 4
+
+    def describe(self):
+        wl = self.wl
+        return {"workload": wl.name, "rows": self.rows, "k": wl.k, "n_segments": list(wl.segments),
+                "scale_format": "per_row" if wl.fmt == 0 else "block128", "silu_fused": wl.silu,
+                "out_dtype": "f32", "weight_copies": self.copies,
+                "l2": f"inputs larger than L2: weights rotate over {self.copies} copies "
+                      f"({self.copies * self.weight_bytes / 1e6:.0f} MB)"}
+
+
+class Int4Case:
+    def __init__(self, wl, rows, torch, qdl, syn, l2_bytes):
+        self.wl, self.rows = wl, rows
+        ws = syn.int4_weights(wl)
+        self.weight_bytes = sum(a.nbytes for w in ws for a in w)
+        self.copies = max(1, math.ceil(4 * l2_bytes / self.weight_bytes))
+        base = [[torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else a).cuda() for a in w]
+                for w in ws]
+        self.sets = [base] + [[[a.clone() for a in w] for w in base] for _ in range(self.copies - 1)]
+        x = syn.int4_activations(wl, rows)
+        self.x_host = torch.from_numpy(x).pin_memory()
+        self.x = self.x_host.cuda()
+        self.outs = [torch.empty((rows, n), device="cuda") for n in (wl.nq, wl.nkv, wl.nkv)]
+        self.out_hosts = [torch.empty((rows, n)).pin_memory() for n in (wl.nq, wl.nkv, wl.nkv)]
+        self.qdl = qdl
+        n_tot = wl.nq + 2 * wl.nkv
+        self.step_bytes = self.weight_bytes + x.nbytes + rows * n_tot * 4
+        self.gemv_bytes = self.step_bytes
+        self.gemv_launches = math.ceil(rows / 16)
+        self.launches_per_step = self.gemv_launches
+
+    def step(self, i):
+        s = self.sets[i % self.copies]
+        wl = self.wl
+        self.qdl.int4_qkv_gemv(self.x, self.rows, wl.k, wl.nq, wl.nkv, wl.group, [w[0] for w in s],
+                               [w[1] for w in s], [w[2] for w in s], self.outs)
+
+    dominant = step
+
+    def e2e_step(self, i):
+        self.x.copy_(self.x_host, non_blocking=True)
+        self.step(i)
+        for h, d in zip(self.out_hosts, self.outs):
+            h.copy_(d, non_blocking=True)
+
+    def e2e_bytes(self):
+        return self.x_host.numel() * 4, sum(h.numel() * 4 for h in self.out_hosts)
+
+    def describe(self):
+        wl = self.wl
+        return {"workload": wl.name, "rows": self.rows, "k": wl.k, "nq": wl.nq, "nkv": wl.nkv,
+                "group": wl.group, "weight_copies": self.copies,
+                "l2": f"inputs larger than L2: weights rotate over {self.copies} copies "
+                      f"({self.copies * self.weight_bytes / 1e6:.0f} MB)"}
+
+
+# ---------------------------------------------------------------- timing helpers
+
+def _graph(torch, fn, start, count):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(start, start + count):
+            fn(i)
+    return g
+
+
+def _time_graphs(torch, fn, total, chunk=250):
+    """capture `fn` over `total` consecutive step indices into graphs of
+    `chunk` calls each (kept alive by the returned list)"""
+    graphs = []
+    for start in range(0, total, chunk):
+        graphs.append(_graph(torch, fn, start, chunk))
+    return graphs
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle timing
+
+def _oracle_step_fn(wl, rows, syn, fraction):
+    """returns (fn, bytes_equiv, sample description) for one oracle step on a
+    fraction of the workload's output columns"""
+    import oracle
+    if hasattr(wl, "fmt"):
+        segs = syn.w8a8_weights(wl)
+        xb = syn.w8a8_activations(wl, rows)
+        n = wl.n
+        cols = max(1, int(round(n * fraction)))
+        rng = np.random.default_rng(0)
+        ci = np.sort(rng.choice(n, cols, replace=False)).astype(np.int32)
+        r_idx = np.repeat(np.arange(rows, dtype=np.int32), cols)
+        c_idx = np.tile(ci, rows)
+        step_bytes = W8A8Bytes(wl, rows, segs)
+
+        def fn():
+            if wl.silu:
+                q, s = oracle.act_quant_silu(wl.fmt, xb[:, :wl.k], xb[:, wl.k:], wl.k)
+            else:
+                q, s = oracle.act_quant(wl.fmt, xb, wl.k)
+            oracle.w8a8_gemv_sampled(wl.fmt, q, s, segs, r_idx, c_idx)
+        return fn, step_bytes * cols / n, f"act quant of all {rows} rows + GEMV of {cols} of {n} output columns"
+    ws = syn.int4_weights(wl)
+    x = syn.int4_activations(wl, rows)
+    # oracle INT4 on a column slice of each projection
+    ns = (wl.nq, wl.nkv, wl.nkv)
+    take = [max(8, int(round(n * fraction / 8)) * 8) for n in ns]
+    sl = [(w[0][:, :t // 8].copy(), w[1][:, :t].copy(), w[2][:, :t].copy()) for w, t in zip(ws, take)]
+    total_bytes = sum(a.nbytes for w in ws for a in w) + x.nbytes + rows * sum(ns) * 4
+
+    def fn():
+        oracle.int4_qkv(x, take[0], take[1], wl.group, [s[0] for s in sl], [s[1] for s in sl],
+                        [s[2] for s in sl])
+    frac = sum(take) / sum(ns)
+    return fn, total_bytes * frac, f"all {rows} rows x {sum(take)} of {sum(ns)} output columns"
+
+
+def W8A8Bytes(wl, rows, segs):
+    w_scales = sum(s.nbytes for _, s in segs)
+    return wl.n * wl.k + w_scales + rows * (2 * wl.k if wl.silu else wl.k) * 2 + rows * wl.n * 4
+
+
+def _cpu_baseline(wl, rows, syn, budget_s=12.0):
+    import oracle
+    fn, b, desc = _oracle_step_fn(wl, rows, syn, 1.0 / 256)
+    t0 = time.perf_counter()
+    fn()
+    t_probe = time.perf_counter() - t0
+    frac = min(1.0, (1.0 / 256) * max(1.0, budget_s / max(t_probe, 1e-3)))
+    fn, b, desc = _oracle_step_fn(wl, rows, syn, frac)
+    t0 = time.perf_counter()
+    fn()
+    dt = time.perf_counter() - t0
+    return {"value": b / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": desc, "seconds": dt}
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from quantized_decode_linear_gb300 import synthetic as syn
+    import oracle
+    wl = syn.WORKLOADS[args.workload]
+    rows = args.rows or wl.rows[0]
+    # size one step so that the whole run takes about two minutes of CPU time
+    fn, b, desc = _oracle_step_fn(wl, rows, syn, 1.0 / 512)
+    t0 = time.perf_counter()
+    fn()
+    t_probe = max(time.perf_counter() - t0, 1e-4)
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    frac = min(1.0, max(1.0 / 4096, (1.0 / 512) * per_step / t_probe))
+    fn, b, desc = _oracle_step_fn(wl, rows, syn, frac)
+    for _ in range(args.warmup):
+        fn()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        fn()
+    dt = time.perf_counter() - t0
+    value = b * args.steps / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "rows": rows, "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import quantized_decode_linear_gb300 as qdl
+    from quantized_decode_linear_gb300 import build as qbuild
+    from quantized_decode_linear_gb300 import synthetic as syn
+
+    qbuild.build()
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    props = torch.cuda.get_device_properties(local_rank)
+    l2 = getattr(props, "L2_cache_size", 0) or 126 * 2**20
+
+    wl = syn.WORKLOADS[args.workload]
+    rows = args.rows or wl.rows[0]
+    Case = W8A8Case if hasattr(wl, "fmt") else Int4Case
+    case = Case(wl, rows, torch, qdl, syn, l2)
+
+    # graphs covering exactly K steps: up to four distinct graphs of c calls
+    # replayed in turn, plus one remainder graph
+    K, W = args.steps, args.warmup
+    c = min(250, K)
+    full, rem = divmod(K, c)
+
+    def graphs_for(fn):
+        main = [_graph(torch, fn, j * c, c) for j in range(min(full, 4))]
+        tail = _graph(torch, fn, full * c, rem) if rem else None
+        return main, tail
+
+    def replay(gs):
+        main, tail = gs
+        for r in range(full):
+            main[r % len(main)].replay()
+        if tail is not None:
+            tail.replay()
+
+    for i in range(W):  # untimed warm-up steps (eager calls; also loads every kernel)
+        case.step(i)
+    torch.cuda.synchronize()
+    timed = graphs_for(case.step)
+    dom = graphs_for(case.dominant)
+    for gs in (timed, dom):  # first replay uploads the graph
+        for g in gs[0] + ([gs[1]] if gs[1] is not None else []):
+            g.replay()
+    torch.cuda.synchronize()
+    steps, warm = K, W
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    replay(timed)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    # dominant kernel alone, same graphs-of-launches method
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    replay(dom)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dom_ms = d0.elapsed_time(d1)
+    clk = clocks.stop()
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        if dist:
+            dist.barrier()
+
+    # end to end through the public API with host buffers (no graphs)
+    e2e_steps = min(steps, 2000)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        case.e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    h2d, d2h = case.e2e_bytes()
+
+    peak, peak_kind = _peaks()
+    value = case.step_bytes * steps * world / (ms / 1e3) / 1e9
+    dom_launch_s = dom_ms / 1e3 / (steps * case.gemv_launches)
+    achieved = case.gemv_bytes / case.gemv_launches / dom_launch_s / 1e9
+    key = f"{wl.name}@{rows}"
+    src = ["w8a8_gemv_mma.cu"] if Case is W8A8Case else ["int4_qkv.cu"]
+    tr = TRAFFIC.get(key)
+    traffic = tr["bytes"] if tr and tr.get("src") == _src_hash(src) else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": warm, "ms_per_step": ms / steps, "us_per_call": ms / steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if Case is W8A8Case else "f16", "data": "synthetic",
+        "config": dict(case.describe(), parallelism="replicas" if world > 1 else "single"),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "w8a8_gemv_mma_kernel" if Case is W8A8Case else "int4_qkv_kernel",
+                     "peak_source": f"{peak_kind} hbm_gbs", "kernel_us": dom_launch_s * 1e6},
+        "hbm_frac_step": value / world / peak,
+        "e2e": {"value": case.step_bytes * e2e_steps / e2e_s / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "us_per_call": e2e_s / e2e_steps * 1e6},
+        "gpu_launches": steps * case.launches_per_step,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = _cpu_baseline(wl, rows, syn)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="qdl", choices=["qdl", "reference"])
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--rows", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.steps < 1 or args.warmup < 3:
+        ap.error("need --steps >= 1 and --warmup >= 3")
+    from quantized_decode_linear_gb300 import synthetic as syn
+    args.workload = args.workload or syn.HEADLINE
+    if args.workload not in syn.WORKLOADS:
+        ap.error(f"unknown workload; choose from {sorted(syn.WORKLOADS)}")
+    rank, world, local_rank = _rank_world()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+/*
+ * libqdl -- quantized decode-time linear layer for NVIDIA GB300 (sm_103a).
+ *
+ * Two variants of the decode-time projection y = x W^T:
+ *
+ *   W8A8   FP8 E4M3 activations (quantised here, per token row or per
+ *          128-wide K group, optionally with SiLU(gate)*up fused in) times an
+ *          FP8 E4M3 weight with per-row or 128x128-block f32 scales, made of
+ *          1..3 segments concatenated along the output dimension.
+ *          Defined by w8a8_decode.rs (metrale_model_layers, layers::ops).
+ *   W4A16  AWQ INT4 fused Q/K/V projection with per-group scales and zeros.
+ *          Defined by fused_int4_qkv.rs (boostr, quant::wgpu::shaders).
+ *
+ * Conventions for every entry point:
+ *   - All tensor arguments are device pointers owned by the caller; the
+ *     library never allocates, frees or retains them.  Layouts are row-major
+ *     with the strides given.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously; nothing synchronises.
+ *   - Every call validates all arguments on the host before it touches the
+ *     device.  On any error nothing is launched, the call returns a non-zero
+ *     qdl_status and qdl_last_error() returns a message for the calling
+ *     thread.  Kernel launch failures return QDL_ERR_CUDA.
+ *   - FP8 E4M3 is the OCP "E4M3" format (bias 7, max finite 448, no inf,
+ *     NaN = S.1111.111).  Activation codes are produced by
+ *     round-to-nearest-even with saturation to +-448.
+ */
+#ifndef QDL_H
+#define QDL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QDL_API __attribute__((visibility("default")))
+#else
+#define QDL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QDL_OK = 0,
+    QDL_ERR_INVALID_ARG = 1,       /* a shape, stride, pointer or enum is invalid */
+    QDL_ERR_SCRATCH_TOO_SMALL = 2, /* activation buffers cannot hold rows x K   */
+    QDL_ERR_UNSUPPORTED = 3,       /* valid per the definition, beyond a limit  */
+    QDL_ERR_CUDA = 4,              /* the CUDA runtime reported an error        */
+    QDL_ERR_DEVICE_TIMEOUT = 5     /* a bounded device-side wait gave up        */
+} qdl_status;
+
+/* Scale layouts, w8a8_decode.rs enum W8a8Scale.
+ *   PER_ROW : one f32 weight scale per output row; one activation scale per
+ *             token row.
+ *   BLOCK128: one f32 weight scale per 128x128 block of each segment, stored
+ *             [ceil(n_s/128), K/128] row-major; one activation scale per
+ *             token row and 128-wide K group, stored [rows, K/128]. */
+typedef enum { QDL_SCALE_PER_ROW = 0, QDL_SCALE_BLOCK128 = 1 } qdl_scale;
+
+/* Output element type of the W8A8 GEMV. */
+typedef enum { QDL_OUT_F32 = 0, QDL_OUT_BF16 = 1 } qdl_dtype;
+
+#define QDL_MAX_ROWS 256  /* w8a8_decode.rs W8A8_MAX_ROWS */
+#define QDL_K_UNIT 128    /* w8a8_decode.rs W8A8_K_UNIT   */
+#define QDL_MAX_K 65536   /* library limit on K for the activation quantiser */
+
+/* One FP8 weight segment (the fields w8a8_decode.rs reads from Fp8Weight).
+ *   weight : device, e4m3 codes [n, k], row-major (K contiguous), 16-byte
+ *            aligned.
+ *   scale  : device, f32, [n] (PER_ROW) or [ceil(n/128), k/128] (BLOCK128).
+ *   format : qdl_scale of this segment; all segments must agree. */
+typedef struct {
+    const uint8_t *weight;
+    const float *scale;
+    uint32_t n;
+    uint32_t k;
+    int32_t format;
+} qdl_fp8_segment;
+
+/* A validated W8A8 weight: 1..3 segments concatenated along N (w8a8_decode.rs
+ * struct W8a8Weight).  Fill only through qdl_w8a8_weight_init. */
+typedef struct {
+    qdl_fp8_segment segs[3];
+    uint32_t count;
+    uint32_t n;  /* total output width, sum of segment n */
+    uint32_t k;
+    int32_t format;
+    uint32_t n1, n2; /* split points, W8a8Weight::boundaries */
+    uint32_t magic;  /* set by qdl_w8a8_weight_init */
+} qdl_w8a8_weight;
+
+/* W8a8Weight::new.  Checks: 1 <= count <= 3; every segment has the same k
+ * and format; k > 0 and k % 128 == 0; format is PER_ROW or BLOCK128; every
+ * n > 0 with non-NULL weight and scale; every segment but the last has n a
+ * multiple of 16 (PER_ROW) or 128 (BLOCK128) (W8a8Scale::segment_align);
+ * weight pointers 16-byte aligned and scale pointers 4-byte aligned; the
+ * total n fits in 2^31.  Output column j maps to segment 0 for j < n1, to
+ * segment 1 (row j - n1) for n1 <= j < n2, to segment 2 (row j - n2) after;
+ * (n1, n2) = (N, N), (n0, N) or (n0, n0 + n1) for 1, 2 or 3 segments.
+ * Reads host memory only. */
+QDL_API qdl_status qdl_w8a8_weight_init(qdl_w8a8_weight *out, const qdl_fp8_segment *segs,
+                                uint32_t count);
+
+/* Activation buffer sizes for up to QDL_MAX_ROWS rows of K <= max_k
+ * (W8a8Scratch::alloc): q_bytes = 256 * max_k, scale_bytes =
+ * 256 * max(ceil(max_k / 128), 1) * 4.  Either output pointer may be NULL. */
+QDL_API qdl_status qdl_scratch_bytes(uint32_t max_k, size_t *q_bytes, size_t *scale_bytes);
+
+/* Activation quantisation (w8a8_decode.rs fn w8a8_act_quant).
+ *   x       : device bf16 [rows, ldx]; columns 0..k-1 of each row are read.
+ *   q       : device e4m3 codes [rows, k] (row stride k), q_bytes capacity.
+ *   q_scale : device f32 [rows] (PER_ROW) or [rows, k/128] (BLOCK128),
+ *             scale_bytes capacity.
+ * s = absmax / 448 (binary32 division); q = e4m3_rne_sat(x / s); a group
+ * whose absmax is 0 gets s = 0 and the codes of its signed zeros.
+ * Checks: 1 <= rows <= 256; q_bytes >= rows*k and scale_bytes >= rows *
+ * scales_per_row * 4 (else QDL_ERR_SCRATCH_TOO_SMALL); k % 128 == 0,
+ * k <= QDL_MAX_K, ldx >= k, ldx % 8 == 0, x 16-byte aligned, q 16-byte
+ * aligned, q_scale 4-byte aligned. */
+QDL_API qdl_status qdl_act_quant(int32_t format, const void *x, uint32_t ldx, uint32_t rows,
+                         uint32_t k, uint8_t *q, float *q_scale, size_t q_bytes,
+                         size_t scale_bytes, void *stream);
+
+/* Activation quantisation of act = SiLU(gate) * up (w8a8_decode.rs fn
+ * w8a8_act_quant_silu), silu(g) = g / (1 + e^-g).  Each step is one binary32
+ * operation (e = exp(-g), d = 1 + e, s = g / d, act = s * up) with the
+ * library's own exp (Cody and Waite reduction, degree-7 Taylor polynomial;
+ * specified in the source), so the codes are reproducible bit for bit.
+ * gate, up: device bf16 [rows, ld_gate] / [rows, ld_up]; they may be two
+ * column ranges of one buffer.  Same checks as qdl_act_quant, per stride. */
+QDL_API qdl_status qdl_act_quant_silu(int32_t format, const void *gate, const void *up,
+                              uint32_t ld_gate, uint32_t ld_up, uint32_t rows, uint32_t k,
+                              uint8_t *q, float *q_scale, size_t q_bytes, size_t scale_bytes,
+                              void *stream);
+
+/* W8A8 GEMV / skinny GEMM (w8a8_decode.rs fn w8a8_gemv):
+ *   y[m, j] = sum_k dec(q[m,k]) sa(m,k) dec(W[j,k]) sw(j,k)
+ * with the scale layouts of qdl_scale, over all rows (one pass over the
+ * weights for any rows <= 256).
+ *   q, q_scale : device, as written by qdl_act_quant (capacities q_bytes,
+ *                scale_bytes are checked like the activation scratch).
+ *   out        : device [rows, ldc] of out_dtype (f32, or bf16 rounded to
+ *                nearest even); columns N..ldc-1 are not written.
+ * Checks: weight initialised; 1 <= rows <= 256; capacities; ldc >= N;
+ * out aligned to its element size; out_dtype valid. */
+QDL_API qdl_status qdl_w8a8_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *q_scale,
+                         size_t q_bytes, size_t scale_bytes, uint32_t rows, void *out,
+                         int32_t out_dtype, uint32_t ldc, void *stream);
+
+/* Decode projection (w8a8_decode.rs fn w8a8_proj): qdl_act_quant with the
+ * weight's format and K, then qdl_w8a8_gemv, on one stream.  q and q_scale
+ * are the caller's activation scratch (sizes from qdl_scratch_bytes). */
+QDL_API qdl_status qdl_w8a8_proj(const qdl_w8a8_weight *w, const void *x, uint32_t ldx, uint32_t rows,
+                         void *out, int32_t out_dtype, uint32_t ldc, uint8_t *q, float *q_scale,
+                         size_t q_bytes, size_t scale_bytes, void *stream);
+
+/* MLP down projection: qdl_act_quant_silu with the weight's format and K,
+ * then qdl_w8a8_gemv (the composition w8a8_decode.rs uses for gate/up
+ * inputs). */
+QDL_API qdl_status qdl_w8a8_proj_silu(const qdl_w8a8_weight *w, const void *gate, const void *up,
+                              uint32_t ld_gate, uint32_t ld_up, uint32_t rows, void *out,
+                              int32_t out_dtype, uint32_t ldc, uint8_t *q, float *q_scale,
+                              size_t q_bytes, size_t scale_bytes, void *stream);
+
+/* AWQ INT4 fused Q/K/V projection (fused_int4_qkv.rs: fused_int4_qkv_q,
+ * fused_int4_qkv_k, fused_int4_qkv_v, unpack_awq_qkv).  For projection p
+ * (0 = q with width nq, 1 = k and 2 = v with width nkv), column c, row i:
+ *   nib = (qw[p][kk * (n/8) + c/8] >> SHIFT[c % 8]) & 0xF,
+ *         SHIFT = {0, 16, 4, 20, 8, 24, 12, 28}
+ *   w   = (nib - zr[p][(kk/group) * n + c]) * sc[p][(kk/group) * n + c]
+ *   out[p][i * n + c] = sum_kk x[i * k + kk] * w
+ *   x      : device f32 [m, k], 16-byte aligned, |x| < 65504.
+ *   qw[p]  : device u32 [k, n/8], 4-byte aligned (8-byte aligned with
+ *            nq, nkv multiples of 16 enables 8-byte weight loads).
+ *   sc[p], zr[p] : device f32 [k/group, n], 16-byte aligned.
+ *   out[p] : device f32 [m, n], 4-byte aligned.
+ * The kernel multiplies x rounded to f16 with exact nibbles on tensor cores
+ * and applies zeros and scales per group in f32 (error within 2^-11 of
+ * sum |x w|).  Checks: m >= 1; k >= 1; group > 0, group % 16 == 0,
+ * k % group == 0; nq, nkv > 0 and multiples of 8; no NULL pointer;
+ * alignments above.  Rows are processed 16 at a time (one weight pass per
+ * 16 rows). */
+QDL_API qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq, uint32_t nkv,
+                             uint32_t group, const uint32_t *const *qw, const float *const *sc,
+                             const float *const *zr, float *const *out, void *stream);
+
+/* Reads and clears the device-side fault word that bounded waits in the
+ * kernels set when they give up (synchronises `stream`).  Returns QDL_OK or
+ * QDL_ERR_DEVICE_TIMEOUT. */
+QDL_API qdl_status qdl_check_device_fault(void *stream);
+
+/* Message for the last error on the calling thread ("" if none). */
+QDL_API const char *qdl_last_error(void);
+
+/* Static name of a status code. */
+QDL_API const char *qdl_status_string(qdl_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

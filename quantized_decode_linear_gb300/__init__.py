@@ -1,0 +1,215 @@
+"""Python binding of libqdl, the quantized decode-time linear layer for GB300.
+
+Thin argument marshalling over the C ABI declared in ``include/qdl.h``: every
+function here has the C entry point's name without the ``qdl_`` prefix, takes
+torch CUDA tensors (or raw device pointers) and the current CUDA stream, and
+calls the library through ctypes.  All computation happens in the library's
+CUDA kernels; there is no host fallback.  If the library cannot be loaded the
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PER_ROW = 0
+BLOCK128 = 1
+OUT_F32 = 0
+OUT_BF16 = 1
+MAX_ROWS = 256
+K_UNIT = 128
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libqdl.so")
+
+STATUS_NAMES = {0: "QDL_OK", 1: "QDL_ERR_INVALID_ARG", 2: "QDL_ERR_SCRATCH_TOO_SMALL",
+                3: "QDL_ERR_UNSUPPORTED", 4: "QDL_ERR_CUDA", 5: "QDL_ERR_DEVICE_TIMEOUT"}
+
+# every symbol include/qdl.h declares
+EXPORTS = ("qdl_w8a8_weight_init", "qdl_scratch_bytes", "qdl_act_quant", "qdl_act_quant_silu",
+           "qdl_w8a8_gemv", "qdl_w8a8_proj", "qdl_w8a8_proj_silu", "qdl_int4_qkv_gemv",
+           "qdl_check_device_fault", "qdl_last_error", "qdl_status_string")
+
+
+class QdlError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+class Fp8Segment(ctypes.Structure):
+    _fields_ = [("weight", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("n", ctypes.c_uint32),
+                ("k", ctypes.c_uint32), ("format", ctypes.c_int32)]
+
+
+class W8A8WeightDesc(ctypes.Structure):
+    _fields_ = [("segs", Fp8Segment * 3), ("count", ctypes.c_uint32), ("n", ctypes.c_uint32),
+                ("k", ctypes.c_uint32), ("format", ctypes.c_int32), ("n1", ctypes.c_uint32),
+                ("n2", ctypes.c_uint32), ("magic", ctypes.c_uint32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libqdl.so (built by ``quantized_decode_linear_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libqdl.so is not built ({p}); run quantized_decode_linear_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        P, U32, I32, SZ = ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int32, ctypes.c_size_t
+        sig = {
+            "qdl_w8a8_weight_init": [P, P, U32],
+            "qdl_scratch_bytes": [U32, P, P],
+            "qdl_act_quant": [I32, P, U32, U32, U32, P, P, SZ, SZ, P],
+            "qdl_act_quant_silu": [I32, P, P, U32, U32, U32, U32, P, P, SZ, SZ, P],
+            "qdl_w8a8_gemv": [P, P, P, SZ, SZ, U32, P, I32, U32, P],
+            "qdl_w8a8_proj": [P, P, U32, U32, P, I32, U32, P, P, SZ, SZ, P],
+            "qdl_w8a8_proj_silu": [P, P, P, U32, U32, U32, P, I32, U32, P, P, SZ, SZ, P],
+            "qdl_int4_qkv_gemv": [P, U32, U32, U32, U32, U32, P, P, P, P, P],
+            "qdl_check_device_fault": [P],
+            "qdl_last_error": [],
+            "qdl_status_string": [ctypes.c_int],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_char_p if name in ("qdl_last_error", "qdl_status_string") else ctypes.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def last_error() -> str:
+    return load().qdl_last_error().decode()
+
+
+def _check(status: int):
+    if status != 0:
+        raise QdlError(status, last_error())
+
+
+def _ptr(t) -> int | None:
+    """device address of a tensor or an int; None -> NULL"""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ---------------------------------------------------------------- W8A8
+
+
+class W8A8Weight:
+    """A validated W8A8 weight (C struct qdl_w8a8_weight) plus references to
+    the tensors it points at, so they outlive the descriptor."""
+
+    def __init__(self, desc: W8A8WeightDesc, tensors):
+        self.desc = desc
+        self._tensors = tensors
+
+    @property
+    def n(self) -> int:
+        return self.desc.n
+
+    @property
+    def k(self) -> int:
+        return self.desc.k
+
+    @property
+    def format(self) -> int:
+        return self.desc.format
+
+
+def w8a8_weight_init(segments, fmt: int) -> W8A8Weight:
+    """segments: list of (codes uint8 [n, k] CUDA tensor, f32 scales)."""
+    segs = (Fp8Segment * max(1, len(segments)))()
+    keep = []
+    for i, (w, s) in enumerate(segments):
+        segs[i] = Fp8Segment(_ptr(w), _ptr(s), w.shape[0], w.shape[1], fmt)
+        keep += [w, s]
+    desc = W8A8WeightDesc()
+    _check(load().qdl_w8a8_weight_init(ctypes.byref(desc), segs, len(segments)))
+    return W8A8Weight(desc, keep)
+
+
+def scratch_bytes(max_k: int):
+    q = ctypes.c_size_t()
+    s = ctypes.c_size_t()
+    _check(load().qdl_scratch_bytes(max_k, ctypes.byref(q), ctypes.byref(s)))
+    return q.value, s.value
+
+
+def act_quant(fmt: int, x, rows: int, k: int, q, q_scale, ldx: int | None = None, stream=None):
+    ldx = x.stride(0) if ldx is None else ldx
+    _check(load().qdl_act_quant(fmt, _ptr(x), ldx, rows, k, _ptr(q), _ptr(q_scale), _nbytes(q),
+                                _nbytes(q_scale), _stream(stream)))
+
+
+def act_quant_silu(fmt: int, gate, up, rows: int, k: int, q, q_scale, ld_gate: int | None = None,
+                   ld_up: int | None = None, stream=None):
+    ld_gate = gate.stride(0) if ld_gate is None else ld_gate
+    ld_up = up.stride(0) if ld_up is None else ld_up
+    _check(load().qdl_act_quant_silu(fmt, _ptr(gate), _ptr(up), ld_gate, ld_up, rows, k, _ptr(q),
+                                     _ptr(q_scale), _nbytes(q), _nbytes(q_scale), _stream(stream)))
+
+
+def w8a8_gemv(w: W8A8Weight, q, q_scale, rows: int, out, out_dtype: int = OUT_F32,
+              ldc: int | None = None, stream=None):
+    ldc = out.stride(0) if ldc is None else ldc
+    _check(load().qdl_w8a8_gemv(ctypes.byref(w.desc), _ptr(q), _ptr(q_scale), _nbytes(q),
+                                _nbytes(q_scale), rows, _ptr(out), out_dtype, ldc, _stream(stream)))
+
+
+def w8a8_proj(w: W8A8Weight, x, rows: int, out, q, q_scale, out_dtype: int = OUT_F32,
+              ldx: int | None = None, ldc: int | None = None, stream=None):
+    ldx = x.stride(0) if ldx is None else ldx
+    ldc = out.stride(0) if ldc is None else ldc
+    _check(load().qdl_w8a8_proj(ctypes.byref(w.desc), _ptr(x), ldx, rows, _ptr(out), out_dtype, ldc,
+                                _ptr(q), _ptr(q_scale), _nbytes(q), _nbytes(q_scale), _stream(stream)))
+
+
+def w8a8_proj_silu(w: W8A8Weight, gate, up, rows: int, out, q, q_scale, out_dtype: int = OUT_F32,
+                   ld_gate: int | None = None, ld_up: int | None = None, ldc: int | None = None,
+                   stream=None):
+    ld_gate = gate.stride(0) if ld_gate is None else ld_gate
+    ld_up = up.stride(0) if ld_up is None else ld_up
+    ldc = out.stride(0) if ldc is None else ldc
+    _check(load().qdl_w8a8_proj_silu(ctypes.byref(w.desc), _ptr(gate), _ptr(up), ld_gate, ld_up, rows,
+                                     _ptr(out), out_dtype, ldc, _ptr(q), _ptr(q_scale), _nbytes(q),
+                                     _nbytes(q_scale), _stream(stream)))
+
+
+# ---------------------------------------------------------------- INT4
+
+
+def int4_qkv_gemv(x, m: int, k: int, nq: int, nkv: int, group: int, qw, sc, zr, out, stream=None):
+    """qw/sc/zr/out: 3-sequences (q, k, v) of CUDA tensors or device pointers."""
+    arr = lambda xs: (ctypes.c_void_p * 3)(*[_ptr(t) for t in xs])
+    _check(load().qdl_int4_qkv_gemv(_ptr(x), m, k, nq, nkv, group, arr(qw), arr(sc), arr(zr), arr(out),
+                                    _stream(stream)))
+
+
+def check_device_fault(stream=None):
+    _check(load().qdl_check_device_fault(_stream(stream)))

@@ -1,0 +1,79 @@
+"""Build libqdl.so (the C-ABI library) in-tree with nvcc for sm_103a.
+
+Each CUDA translation unit is compiled in parallel, then linked into one shared
+object with the static CUDA runtime (the library loads on machines without a
+GPU driver; the driver is needed only when a call reaches the device).
+"""
+from __future__ import annotations
+
+import concurrent.futures
+import os
+import shutil
+import subprocess
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD_DIR = os.path.join(PKG, "_build")
+LIB_PATH = os.path.join(BUILD_DIR, "libqdl.so")
+
+SOURCES = ["qdl_api.cu", "act_quant.cu", "w8a8_gemv_mma.cu", "int4_qkv.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
+                     "-Xcompiler", "-fvisibility=hidden", f"-I{INCLUDE}"]
+
+
+def _nvcc() -> str:
+    for cand in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libqdl")
+
+
+def _inputs():
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh"))]
+    files.append(os.path.join(INCLUDE, "qdl.h"))
+    return files
+
+
+def up_to_date(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
+        return False
+    t = os.path.getmtime(lib_path)
+    return all(os.path.getmtime(f) <= t for f in _inputs())
+
+
+def build(force: bool = False, extra_flags=(), lib_path: str = LIB_PATH, verbose: bool = False) -> str:
+    """Compile and link libqdl.so; returns its path.  Skips work when the
+    library is newer than every source unless `force`."""
+    if not force and not extra_flags and up_to_date(lib_path):
+        return lib_path
+    nvcc = _nvcc()
+    obj_dir = os.path.join(os.path.dirname(lib_path), "obj")
+    os.makedirs(obj_dir, exist_ok=True)
+    flags = NVCC_FLAGS + list(extra_flags)
+
+    def compile_one(src):
+        obj = os.path.join(obj_dir, src.replace(".cu", ".o"))
+        cmd = [nvcc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        if verbose and (r.stdout or r.stderr):
+            print(r.stdout + r.stderr)
+        return obj
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
+    tmp = lib_path + f".tmp{os.getpid()}"
+    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-Xcompiler", "-fPIC"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, lib_path)
+    return lib_path
+
+
+if __name__ == "__main__":
+    print(build(force=True, verbose=True))

@@ -1,0 +1,160 @@
+// Activation quantisation to FP8 E4M3 (w8a8_decode.rs: w8a8_act_quant and
+// w8a8_act_quant_silu; scale layout from W8a8Scale::act_scales_per_row).
+//
+//   s = absmax / 448            (IEEE binary32 division)
+//   q = e4m3_rne_sat(act / s)   (IEEE division, then cvt.rn.satfinite)
+//   act = x, or SiLU(gate) * up computed with the library's exp
+//
+// A group whose absmax is 0 stores s = 0 and the codes of its signed zeros.
+// Every step is a correctly rounded binary32 operation, so codes and scales
+// are reproducible bit for bit.
+//
+// Two kernels:
+//   - per 128-group (Block128): one warp per group, 4 elements per lane,
+//     absmax by warp shuffles; the grid covers rows x k/128 groups.
+//   - per token row (PerRow): one CTA per row, each thread keeps its
+//     elements in registers (UPT 16-byte units of 8 values), absmax by warp
+//     shuffles plus a shared-memory step, then quantises from registers.
+#include <cuda_bf16.h>
+
+#include "qdl_internal.cuh"
+
+namespace qdl {
+namespace {
+
+template <bool kSilu>
+__device__ __forceinline__ float act_value(uint32_t a_bits, uint32_t b_bits) {
+    const float a = bf16_bits_to_f32(a_bits);
+    if constexpr (kSilu) {
+        return silu_mul(a, bf16_bits_to_f32(b_bits));
+    } else {
+        return a;
+    }
+}
+
+__device__ __forceinline__ float quant_operand(float v, float scale) {
+    return scale == 0.0f ? v : __fdiv_rn(v, scale);
+}
+
+// ---------------------------------------------------------------- Block128
+
+template <bool kSilu>
+__global__ void __launch_bounds__(256) act_quant_g128_kernel(ActQuantArgs a) {
+    const uint32_t groups_per_row = a.k / kKUnit;
+    const uint32_t gid = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const uint32_t lane = threadIdx.x & 31;
+    if (gid >= a.rows * groups_per_row) return;  // warp-uniform
+    const uint32_t row = gid / groups_per_row;
+    const uint32_t col = (gid % groups_per_row) * kKUnit + lane * 4;
+
+    const uint2 xa = *reinterpret_cast<const uint2 *>(a.a + (size_t)row * a.lda + col);
+    uint2 xb = make_uint2(0, 0);
+    if constexpr (kSilu) xb = *reinterpret_cast<const uint2 *>(a.b + (size_t)row * a.ldb + col);
+
+    float v[4];
+    v[0] = act_value<kSilu>(xa.x & 0xFFFFu, xb.x & 0xFFFFu);
+    v[1] = act_value<kSilu>(xa.x >> 16, xb.x >> 16);
+    v[2] = act_value<kSilu>(xa.y & 0xFFFFu, xb.y & 0xFFFFu);
+    v[3] = act_value<kSilu>(xa.y >> 16, xb.y >> 16);
+
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float scale = __fdiv_rn(amax, 448.0f);
+
+    const uint32_t lo = cvt_e4m3x2(quant_operand(v[0], scale), quant_operand(v[1], scale));
+    const uint32_t hi = cvt_e4m3x2(quant_operand(v[2], scale), quant_operand(v[3], scale));
+    *reinterpret_cast<uint32_t *>(a.q + (size_t)row * a.k + col) = lo | (hi << 16);
+    if (lane == 0) a.s[(size_t)row * groups_per_row + col / kKUnit] = scale;
+}
+
+// ---------------------------------------------------------------- PerRow
+
+template <bool kSilu, int UPT>
+__global__ void __launch_bounds__(1024) act_quant_row_kernel(ActQuantArgs a) {
+    __shared__ float warp_max[32];
+    const uint32_t row = blockIdx.x;
+    const uint32_t units = a.k / 8;
+    const uint16_t *xa = a.a + (size_t)row * a.lda;
+    const uint16_t *xb = kSilu ? a.b + (size_t)row * a.ldb : nullptr;
+
+    float v[UPT][8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < UPT; ++i) {
+        const uint32_t u = threadIdx.x + i * blockDim.x;
+        if (u < units) {
+            const uint4 pa = *reinterpret_cast<const uint4 *>(xa + u * 8);
+            uint4 pb = make_uint4(0, 0, 0, 0);
+            if constexpr (kSilu) pb = *reinterpret_cast<const uint4 *>(xb + u * 8);
+            const uint32_t wa[4] = {pa.x, pa.y, pa.z, pa.w};
+            const uint32_t wb[4] = {pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[i][2 * j] = act_value<kSilu>(wa[j] & 0xFFFFu, wb[j] & 0xFFFFu);
+                v[i][2 * j + 1] = act_value<kSilu>(wa[j] >> 16, wb[j] >> 16);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[i][j]));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t nwarps = blockDim.x >> 5;
+    if (lane == 0) warp_max[warp] = amax;
+    __syncthreads();
+    amax = lane < nwarps ? warp_max[lane] : 0.0f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float scale = __fdiv_rn(amax, 448.0f);
+
+    uint8_t *qrow = a.q + (size_t)row * a.k;
+#pragma unroll
+    for (int i = 0; i < UPT; ++i) {
+        const uint32_t u = threadIdx.x + i * blockDim.x;
+        if (u < units) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                w[j] = cvt_e4m3x2(quant_operand(v[i][2 * j], scale),
+                                  quant_operand(v[i][2 * j + 1], scale));
+            *reinterpret_cast<uint2 *>(qrow + u * 8) =
+                make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+        }
+    }
+    if (threadIdx.x == 0) a.s[row] = scale;
+}
+
+template <bool kSilu>
+cudaError_t launch_row(const ActQuantArgs &a, cudaStream_t s) {
+    const uint32_t units = a.k / 8;
+    uint32_t threads = units < 1024 ? ((units + 31) / 32) * 32 : 1024;
+    const uint32_t upt = (units + threads - 1) / threads;
+    dim3 grid(a.rows), block(threads);
+    if (upt <= 1)
+        act_quant_row_kernel<kSilu, 1><<<grid, block, 0, s>>>(a);
+    else if (upt <= 2)
+        act_quant_row_kernel<kSilu, 2><<<grid, block, 0, s>>>(a);
+    else if (upt <= 4)
+        act_quant_row_kernel<kSilu, 4><<<grid, block, 0, s>>>(a);
+    else
+        act_quant_row_kernel<kSilu, 8><<<grid, block, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <bool kSilu>
+cudaError_t launch_g128(const ActQuantArgs &a, cudaStream_t s) {
+    const uint32_t groups = a.rows * (a.k / kKUnit);
+    act_quant_g128_kernel<kSilu><<<(groups + 7) / 8, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_act_quant(const ActQuantArgs &a, int format, bool silu, cudaStream_t s) {
+    if (format == QDL_SCALE_PER_ROW) return silu ? launch_row<true>(a, s) : launch_row<false>(a, s);
+    return silu ? launch_g128<true>(a, s) : launch_g128<false>(a, s);
+}
+
+}  // namespace qdl

@@ -1,0 +1,330 @@
+// C ABI of libqdl: argument validation, dispatch and error reporting.
+// Validation rules follow w8a8_decode.rs (W8a8Weight::new,
+// W8a8Scratch::alloc/fits, w8a8_decode_available, w8a8_act_quant,
+// w8a8_act_quant_silu, w8a8_gemv, w8a8_proj) and the shapes read by
+// fused_int4_qkv.rs.  No entry point touches the device before every check
+// has passed.
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "qdl_internal.cuh"
+
+namespace qdl {
+
+namespace {
+
+constexpr uint32_t kWeightMagic = 0x51444C57u;  // "QDLW"
+thread_local std::string g_last_error;
+
+qdl_status fail(qdl_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+qdl_status ok() {
+    g_last_error.clear();
+    return QDL_OK;
+}
+
+qdl_status cuda_fail(const char *where, cudaError_t e) {
+    return fail(QDL_ERR_CUDA, "%s: CUDA error %d (%s)", where, (int)e, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_format(int32_t f) { return f == QDL_SCALE_PER_ROW || f == QDL_SCALE_BLOCK128; }
+
+const char *format_name(int32_t f) {
+    return f == QDL_SCALE_PER_ROW ? "PerRow" : (f == QDL_SCALE_BLOCK128 ? "Block128" : "invalid");
+}
+
+// W8a8Scale::act_scales_per_row
+size_t scales_per_row(int32_t f, uint32_t k) { return f == QDL_SCALE_PER_ROW ? 1 : k / kKUnit; }
+
+// W8a8Scratch::fits
+bool fits(const void *q, size_t q_bytes, size_t scale_bytes, uint32_t rows, uint32_t k, int32_t f) {
+    return q != nullptr && q_bytes >= (size_t)rows * k && scale_bytes >= (size_t)rows * scales_per_row(f, k) * 4;
+}
+
+qdl_status check_act_args(const char *who, int32_t format, uint32_t rows, uint32_t k, const uint8_t *q,
+                          const float *q_scale, size_t q_bytes, size_t scale_bytes) {
+    if (!valid_format(format)) return fail(QDL_ERR_INVALID_ARG, "%s: scale format %d is not per-row or 128x128 block", who, (int)format);
+    if (rows < 1 || rows > (uint32_t)kMaxRows)
+        return fail(QDL_ERR_INVALID_ARG, "%s: %u rows, want 1..=%d", who, rows, kMaxRows);
+    if (k % kKUnit != 0 || k == 0 || k > QDL_MAX_K)
+        return fail(QDL_ERR_INVALID_ARG, "%s: K=%u (want K %% 128 == 0, 0 < K <= %d)", who, k, QDL_MAX_K);
+    if (q_scale == nullptr) return fail(QDL_ERR_INVALID_ARG, "%s: activation scale pointer is NULL", who);
+    if (!fits(q, q_bytes, scale_bytes, rows, k, format))
+        return fail(QDL_ERR_SCRATCH_TOO_SMALL, "%s: %u rows of K=%u do not fit the scratch", who, rows, k);
+    if (!aligned(q, 16) || !aligned(q_scale, 4))
+        return fail(QDL_ERR_INVALID_ARG, "%s: q must be 16-byte and q_scale 4-byte aligned", who);
+    return QDL_OK;
+}
+
+qdl_status check_input(const char *who, const char *name, const void *p, uint32_t ld, uint32_t k) {
+    if (p == nullptr) return fail(QDL_ERR_INVALID_ARG, "%s: %s is NULL", who, name);
+    if (ld < k || ld % 8 != 0)
+        return fail(QDL_ERR_INVALID_ARG, "%s: K=%u, %s stride=%u (want K %% 128 == 0, stride >= K, stride %% 8 == 0)", who, k, name, ld);
+    if (!aligned(p, 16)) return fail(QDL_ERR_INVALID_ARG, "%s: %s must be 16-byte aligned", who, name);
+    return QDL_OK;
+}
+
+qdl_status check_weight(const char *who, const qdl_w8a8_weight *w) {
+    if (w == nullptr || w->magic != kWeightMagic)
+        return fail(QDL_ERR_INVALID_ARG, "%s: weight descriptor is NULL or was not made by qdl_w8a8_weight_init", who);
+    return QDL_OK;
+}
+
+qdl_status launch_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *q_scale, uint32_t rows, void *out,
+                       int32_t out_dtype, uint32_t ldc, cudaStream_t stream) {
+    const size_t spr = scales_per_row(w->format, w->k);
+    const size_t elt = out_dtype == QDL_OUT_BF16 ? 2 : 4;
+    W8A8Args a = {};
+    a.w0 = w->segs[0].weight;
+    a.sw0 = w->segs[0].scale;
+    a.w1 = w->count > 1 ? w->segs[1].weight : w->segs[0].weight;
+    a.sw1 = w->count > 1 ? w->segs[1].scale : w->segs[0].scale;
+    a.w2 = w->count > 2 ? w->segs[2].weight : w->segs[0].weight;
+    a.sw2 = w->count > 2 ? w->segs[2].scale : w->segs[0].scale;
+    a.ldc = ldc;
+    a.out_bf16 = out_dtype == QDL_OUT_BF16;
+    a.n = w->n;
+    a.k = w->k;
+    a.n1 = w->n1;
+    a.n2 = w->n2;
+    a.kb = w->k / kKUnit;
+    // the register-streaming kernel takes up to 16 token rows per pass
+    for (uint32_t done = 0; done < rows; done += 16) {
+        const uint32_t m = rows - done < 16 ? rows - done : 16;
+        a.q = q + (size_t)done * w->k;
+        a.sa = q_scale + (size_t)done * spr;
+        a.out = static_cast<char *>(out) + (size_t)done * ldc * elt;
+        a.m = m;
+        cudaError_t e = launch_w8a8_gemv_mma(a, w->format, stream);
+        if (e != cudaSuccess) return cuda_fail("qdl_w8a8_gemv", e);
+    }
+    return ok();
+}
+
+}  // namespace
+
+int device_sm_count() {
+    static std::mutex mu;
+    static std::vector<int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)cache.size() <= dev) cache.resize(dev + 1, 0);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+}  // namespace qdl
+
+using namespace qdl;
+
+extern "C" {
+
+const char *qdl_last_error(void) { return g_last_error.c_str(); }
+
+const char *qdl_status_string(qdl_status s) {
+    switch (s) {
+        case QDL_OK: return "QDL_OK";
+        case QDL_ERR_INVALID_ARG: return "QDL_ERR_INVALID_ARG";
+        case QDL_ERR_SCRATCH_TOO_SMALL: return "QDL_ERR_SCRATCH_TOO_SMALL";
+        case QDL_ERR_UNSUPPORTED: return "QDL_ERR_UNSUPPORTED";
+        case QDL_ERR_CUDA: return "QDL_ERR_CUDA";
+        case QDL_ERR_DEVICE_TIMEOUT: return "QDL_ERR_DEVICE_TIMEOUT";
+    }
+    return "QDL_ERR_UNKNOWN";
+}
+
+qdl_status qdl_w8a8_weight_init(qdl_w8a8_weight *out, const qdl_fp8_segment *segs, uint32_t count) {
+    const char *who = "W8a8Weight";
+    if (out == nullptr || segs == nullptr) return fail(QDL_ERR_INVALID_ARG, "%s: NULL descriptor or segment list", who);
+    if (count < 1 || count > 3) return fail(QDL_ERR_INVALID_ARG, "%s: %u segments, want 1..=3", who, count);
+    const int32_t format = segs[0].format;
+    if (!valid_format(format))
+        return fail(QDL_ERR_INVALID_ARG, "%s: scale format %d is not per-row or 128x128 block", who, (int)format);
+    const uint32_t k = segs[0].k;
+    if (k == 0 || k % kKUnit != 0) return fail(QDL_ERR_INVALID_ARG, "%s: K=%u is not a positive multiple of %d", who, k, kKUnit);
+    const uint32_t align = format == QDL_SCALE_PER_ROW ? 16 : 128;  // W8a8Scale::segment_align
+    uint64_t total = 0;
+    for (uint32_t i = 0; i < count; ++i) {
+        const qdl_fp8_segment &s = segs[i];
+        if (s.k != k || s.format != format)
+            return fail(QDL_ERR_INVALID_ARG, "%s: segment %u is [%u, %u] %s, segment 0 is [.., %u] %s", who, i, s.n, s.k,
+                        format_name(s.format), k, format_name(format));
+        if (s.n == 0 || s.weight == nullptr || s.scale == nullptr)
+            return fail(QDL_ERR_INVALID_ARG, "%s: segment %u is empty", who, i);
+        if (i + 1 < count && s.n % align != 0)
+            return fail(QDL_ERR_INVALID_ARG, "%s: segment %u has %u rows, not a multiple of %u", who, i, s.n, align);
+        if (!aligned(s.weight, 16) || !aligned(s.scale, 4))
+            return fail(QDL_ERR_INVALID_ARG, "%s: segment %u weight must be 16-byte and scale 4-byte aligned", who, i);
+        total += s.n;
+    }
+    if (total >= (1ull << 31)) return fail(QDL_ERR_UNSUPPORTED, "%s: total N=%llu exceeds 2^31", who, (unsigned long long)total);
+    qdl_w8a8_weight w = {};
+    for (uint32_t i = 0; i < 3; ++i) w.segs[i] = segs[i < count ? i : 0];
+    w.count = count;
+    w.n = (uint32_t)total;
+    w.k = k;
+    w.format = format;
+    // W8a8Weight::boundaries
+    const uint32_t n0 = segs[0].n;
+    w.n1 = count == 1 ? w.n : n0;
+    w.n2 = count == 3 ? n0 + segs[1].n : w.n;
+    w.magic = kWeightMagic;
+    *out = w;
+    return ok();
+}
+
+qdl_status qdl_scratch_bytes(uint32_t max_k, size_t *q_bytes, size_t *scale_bytes) {
+    const size_t rows = kMaxRows;
+    const size_t groups = (max_k + kKUnit - 1) / kKUnit;
+    if (q_bytes) *q_bytes = rows * max_k;
+    if (scale_bytes) *scale_bytes = rows * (groups > 1 ? groups : 1) * 4;
+    return ok();
+}
+
+qdl_status qdl_act_quant(int32_t format, const void *x, uint32_t ldx, uint32_t rows, uint32_t k, uint8_t *q, float *q_scale,
+                         size_t q_bytes, size_t scale_bytes, void *stream) {
+    const char *who = "w8a8_act_quant";
+    qdl_status st = check_act_args(who, format, rows, k, q, q_scale, q_bytes, scale_bytes);
+    if (st != QDL_OK) return st;
+    if ((st = check_input(who, "x", x, ldx, k)) != QDL_OK) return st;
+    ActQuantArgs a = {static_cast<const uint16_t *>(x), nullptr, ldx, 0, rows, k, q, q_scale};
+    cudaError_t e = launch_act_quant(a, format, false, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(who, e);
+    return ok();
+}
+
+qdl_status qdl_act_quant_silu(int32_t format, const void *gate, const void *up, uint32_t ld_gate, uint32_t ld_up, uint32_t rows,
+                              uint32_t k, uint8_t *q, float *q_scale, size_t q_bytes, size_t scale_bytes, void *stream) {
+    const char *who = "w8a8_act_quant_silu";
+    qdl_status st = check_act_args(who, format, rows, k, q, q_scale, q_bytes, scale_bytes);
+    if (st != QDL_OK) return st;
+    if ((st = check_input(who, "gate", gate, ld_gate, k)) != QDL_OK) return st;
+    if ((st = check_input(who, "up", up, ld_up, k)) != QDL_OK) return st;
+    ActQuantArgs a = {static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up), ld_gate, ld_up, rows, k, q, q_scale};
+    cudaError_t e = launch_act_quant(a, format, true, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(who, e);
+    return ok();
+}
+
+static qdl_status check_gemv(const char *who, const qdl_w8a8_weight *w, const uint8_t *q, const float *q_scale, size_t q_bytes,
+                             size_t scale_bytes, uint32_t rows, const void *out, int32_t out_dtype, uint32_t ldc) {
+    qdl_status st = check_weight(who, w);
+    if (st != QDL_OK) return st;
+    // w8a8_decode_available
+    if (rows < 1 || rows > (uint32_t)kMaxRows || q_scale == nullptr || !fits(q, q_bytes, scale_bytes, rows, w->k, w->format))
+        return fail(rows < 1 || rows > (uint32_t)kMaxRows || q_scale == nullptr ? QDL_ERR_INVALID_ARG : QDL_ERR_SCRATCH_TOO_SMALL,
+                    "%s: not available for %u rows of [%u, %u] %s", who, rows, w->n, w->k, format_name(w->format));
+    if (!aligned(q, 16) || !aligned(q_scale, 4))
+        return fail(QDL_ERR_INVALID_ARG, "%s: q must be 16-byte and q_scale 4-byte aligned", who);
+    if (ldc < w->n) return fail(QDL_ERR_INVALID_ARG, "%s: ldc=%u < N=%u", who, ldc, w->n);
+    if (out_dtype != QDL_OUT_F32 && out_dtype != QDL_OUT_BF16)
+        return fail(QDL_ERR_INVALID_ARG, "%s: output dtype %d is not F32 or BF16", who, (int)out_dtype);
+    if (out == nullptr || !aligned(out, out_dtype == QDL_OUT_BF16 ? 2 : 4))
+        return fail(QDL_ERR_INVALID_ARG, "%s: output is NULL or misaligned", who);
+    return QDL_OK;
+}
+
+qdl_status qdl_w8a8_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *q_scale, size_t q_bytes, size_t scale_bytes,
+                         uint32_t rows, void *out, int32_t out_dtype, uint32_t ldc, void *stream) {
+    qdl_status st = check_gemv("w8a8_gemv", w, q, q_scale, q_bytes, scale_bytes, rows, out, out_dtype, ldc);
+    if (st != QDL_OK) return st;
+    return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, static_cast<cudaStream_t>(stream));
+}
+
+qdl_status qdl_w8a8_proj(const qdl_w8a8_weight *w, const void *x, uint32_t ldx, uint32_t rows, void *out, int32_t out_dtype,
+                         uint32_t ldc, uint8_t *q, float *q_scale, size_t q_bytes, size_t scale_bytes, void *stream) {
+    const char *who = "w8a8_proj";
+    qdl_status st = check_gemv(who, w, q, q_scale, q_bytes, scale_bytes, rows, out, out_dtype, ldc);
+    if (st != QDL_OK) return st;
+    if ((st = check_input(who, "x", x, ldx, w->k)) != QDL_OK) return st;
+    ActQuantArgs a = {static_cast<const uint16_t *>(x), nullptr, ldx, 0, rows, w->k, q, q_scale};
+    cudaError_t e = launch_act_quant(a, w->format, false, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(who, e);
+    return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, static_cast<cudaStream_t>(stream));
+}
+
+qdl_status qdl_w8a8_proj_silu(const qdl_w8a8_weight *w, const void *gate, const void *up, uint32_t ld_gate, uint32_t ld_up,
+                              uint32_t rows, void *out, int32_t out_dtype, uint32_t ldc, uint8_t *q, float *q_scale, size_t q_bytes,
+                              size_t scale_bytes, void *stream) {
+    const char *who = "w8a8_proj_silu";
+    qdl_status st = check_gemv(who, w, q, q_scale, q_bytes, scale_bytes, rows, out, out_dtype, ldc);
+    if (st != QDL_OK) return st;
+    if ((st = check_input(who, "gate", gate, ld_gate, w->k)) != QDL_OK) return st;
+    if ((st = check_input(who, "up", up, ld_up, w->k)) != QDL_OK) return st;
+    ActQuantArgs a = {static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up), ld_gate, ld_up, rows, w->k, q, q_scale};
+    cudaError_t e = launch_act_quant(a, w->format, true, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(who, e);
+    return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, static_cast<cudaStream_t>(stream));
+}
+
+qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq, uint32_t nkv, uint32_t group,
+                             const uint32_t *const *qw, const float *const *sc, const float *const *zr, float *const *out,
+                             void *stream) {
+    const char *who = "fused_int4_qkv";
+    if (x == nullptr || qw == nullptr || sc == nullptr || zr == nullptr || out == nullptr)
+        return fail(QDL_ERR_INVALID_ARG, "%s: NULL pointer argument", who);
+    if (m < 1) return fail(QDL_ERR_INVALID_ARG, "%s: m=%u, want m >= 1", who, m);
+    if (group == 0 || group % 16 != 0 || k == 0 || k % group != 0)
+        return fail(QDL_ERR_INVALID_ARG, "%s: k=%u, group=%u (want group > 0, group %% 16 == 0, k %% group == 0)", who, k, group);
+    if (nq == 0 || nkv == 0 || nq % 8 != 0 || nkv % 8 != 0)
+        return fail(QDL_ERR_INVALID_ARG, "%s: nq=%u, nkv=%u (want positive multiples of 8)", who, nq, nkv);
+    if (!aligned(x, 16)) return fail(QDL_ERR_INVALID_ARG, "%s: x must be 16-byte aligned", who);
+    bool vec2 = nq % 16 == 0 && nkv % 16 == 0;
+    for (int p = 0; p < 3; ++p) {
+        if (qw[p] == nullptr || sc[p] == nullptr || zr[p] == nullptr || out[p] == nullptr)
+            return fail(QDL_ERR_INVALID_ARG, "%s: projection %d has a NULL pointer", who, p);
+        if (!aligned(qw[p], 4) || !aligned(sc[p], 16) || !aligned(zr[p], 16) || !aligned(out[p], 4))
+            return fail(QDL_ERR_INVALID_ARG, "%s: projection %d misaligned (qw 4, sc/zr 16, out 4 bytes)", who, p);
+        vec2 = vec2 && aligned(qw[p], 8);
+    }
+    Int4Args a = {};
+    a.qw0 = qw[0]; a.qw1 = qw[1]; a.qw2 = qw[2];
+    a.sc0 = sc[0]; a.sc1 = sc[1]; a.sc2 = sc[2];
+    a.zr0 = zr[0]; a.zr1 = zr[1]; a.zr2 = zr[2];
+    a.k = k;
+    a.group = group;
+    a.groups = k / group;
+    a.nq = nq;
+    a.nkv = nkv;
+    a.tiles_q = (nq + 127) / 128;
+    a.tiles_kv = (nkv + 127) / 128;
+    a.vec2 = vec2;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (uint32_t done = 0; done < m; done += 16) {
+        const uint32_t mm = m - done < 16 ? m - done : 16;
+        a.x = x + (size_t)done * k;
+        a.out0 = out[0] + (size_t)done * nq;
+        a.out1 = out[1] + (size_t)done * nkv;
+        a.out2 = out[2] + (size_t)done * nkv;
+        a.m = mm;
+        cudaError_t e = launch_int4_qkv(a, s);
+        if (e != cudaSuccess) return cuda_fail(who, e);
+    }
+    return ok();
+}
+
+qdl_status qdl_check_device_fault(void *stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
+    return ok();
+}
+
+}  // extern "C"

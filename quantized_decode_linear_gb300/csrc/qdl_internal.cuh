@@ -1,0 +1,179 @@
+// Internal declarations of libqdl: kernel argument blocks, launchers and
+// small device helpers (inline PTX).  Not part of the public C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qdl.h"
+
+namespace qdl {
+
+constexpr int kMaxRows = QDL_MAX_ROWS;
+constexpr int kKUnit = QDL_K_UNIT;
+
+// ---------------------------------------------------------------- arguments
+
+struct ActQuantArgs {
+    const uint16_t *a;  // x, or gate for the SiLU variant (bf16 bits)
+    const uint16_t *b;  // up for the SiLU variant, else unused
+    uint32_t lda, ldb;  // row strides in elements
+    uint32_t rows, k;
+    uint8_t *q;         // [rows, k]
+    float *s;           // [rows] or [rows, k/128]
+};
+
+struct W8A8Args {
+    const uint8_t *q;   // activation codes [rows, k]
+    const float *sa;    // activation scales [rows] or [rows, k/128]
+    const uint8_t *w0, *w1, *w2;  // segment codes [n_s, k]
+    const float *sw0, *sw1, *sw2; // segment scales
+    void *out;
+    uint32_t ldc;
+    uint32_t out_bf16;
+    uint32_t m;         // token rows in this launch
+    uint32_t n, k;      // total output width, reduction length
+    uint32_t n1, n2;    // segment split points
+    uint32_t kb;        // k / 128
+};
+
+struct Int4Args {
+    const float *x;     // [m, k]
+    const uint32_t *qw0, *qw1, *qw2;
+    const float *sc0, *sc1, *sc2;
+    const float *zr0, *zr1, *zr2;
+    float *out0, *out1, *out2;
+    uint32_t m, k, group, groups;
+    uint32_t nq, nkv;
+    uint32_t tiles_q, tiles_kv;  // 128-column tiles per projection
+    uint32_t vec2;               // 8-byte weight loads allowed
+};
+
+// ---------------------------------------------------------------- launchers
+// Each returns cudaSuccess or the launch error.  Arguments are validated by
+// the C-ABI layer before these are called.
+
+cudaError_t launch_act_quant(const ActQuantArgs &a, int format, bool silu, cudaStream_t s);
+cudaError_t launch_w8a8_gemv_mma(const W8A8Args &a, int format, cudaStream_t s);
+cudaError_t launch_int4_qkv(const Int4Args &a, cudaStream_t s);
+
+int device_sm_count();  // of the current device, cached
+
+// ---------------------------------------------------------------- device helpers
+
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
+
+// Two binary32 values to two E4M3 codes, round to nearest even, saturating
+// to +-448; `lo` lands in the low byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// The library's exp in binary32: Cody and Waite reduction x = n ln2 + r,
+// n = rint(x log2 e), ln2 split into RN32(ln2) and RN32(ln2 - RN32(ln2));
+// e^r by the degree-7 Taylor polynomial (coefficients 1/j! rounded to
+// binary32) in Horner form with fused multiply-adds; then an exact
+// multiplication by 2^n (two steps when the result is subnormal).  Every
+// operation is a correctly rounded binary32 operation, so the result is
+// reproducible bit for bit.  Arguments above RN32(ln FLT_MAX) give +inf,
+// below RN32(ln 2^-150) give +0.
+__device__ __forceinline__ float pow2i(int n) { return __int_as_float((n + 127) << 23); }
+
+__device__ __forceinline__ float qdl_expf(float x) {
+    if (x != x) return x;
+    if (x > __uint_as_float(0x42b17218u)) return __int_as_float(0x7f800000);
+    if (x < __uint_as_float(0xc2cff1b4u)) return 0.0f;
+    const float t = __fmul_rn(x, __uint_as_float(0x3fb8aa3bu));
+    const float n = rintf(t);
+    float r = __fmaf_rn(-n, __uint_as_float(0x3f317218u), x);
+    r = __fmaf_rn(-n, __uint_as_float(0xb102e308u), r);
+    float p = __uint_as_float(0x39500d01u);          // 1/7!
+    p = __fmaf_rn(p, r, __uint_as_float(0x3ab60b61u)); // 1/6!
+    p = __fmaf_rn(p, r, __uint_as_float(0x3c088889u)); // 1/5!
+    p = __fmaf_rn(p, r, __uint_as_float(0x3d2aaaabu)); // 1/4!
+    p = __fmaf_rn(p, r, __uint_as_float(0x3e2aaaabu)); // 1/3!
+    p = __fmaf_rn(p, r, 0.5f);                         // 1/2!
+    p = __fmaf_rn(p, r, 1.0f);                         // 1/1!
+    p = __fmaf_rn(p, r, 1.0f);                         // 1/0!
+    int ni = static_cast<int>(n);
+    if (ni > 127) {
+        p = __fmul_rn(p, 2.0f);
+        ni -= 1;
+    }
+    if (ni >= -126) return __fmul_rn(p, pow2i(ni));
+    return __fmul_rn(__fmul_rn(p, pow2i(ni + 64)), pow2i(-64));
+}
+
+// SiLU(g) * u, one binary32 operation per step.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    const float e = qdl_expf(-g);
+    const float d = __fadd_rn(1.0f, e);
+    const float s = __fdiv_rn(g, d);
+    return __fmul_rn(s, u);
+}
+
+// Streaming 16-byte load of data read exactly once (weights): bypass L1 and
+// mark the lines evict-first in L2 so activations and scales stay resident.
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p, uint64_t policy) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p), "l"(policy));
+    return r;
+}
+
+__device__ __forceinline__ uint2 ld_stream_v2(const void *p, uint64_t policy) {
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
+                 : "=r"(r.x), "=r"(r.y)
+                 : "l"(p), "l"(policy));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u32(const void *p, uint64_t policy) {
+    uint32_t r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;"
+                 : "=r"(r)
+                 : "l"(p), "l"(policy));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Read-only load through L1 (small operands shared by every warp of a CTA).
+__device__ __forceinline__ uint4 ld_ro_v4(const void *p) {
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+// D += A * B on the FP8 tensor-core path: m16n8k32, A row-major (16 x 32
+// e4m3), B column-major (32 x 8 e4m3), f32 accumulators.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D += A * B, m16n8k16, f16 inputs, f32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+#endif  // __CUDACC__
+
+}  // namespace qdl

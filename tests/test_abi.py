@@ -1,0 +1,243 @@
+"""Host-side tests of the C ABI: the library loads without a GPU, exports every
+symbol include/qdl.h declares, the ctypes structs match the C layout, and every
+validation rule of w8a8_decode.rs / fused_int4_qkv.rs rejects bad arguments
+before any device work (no call here reaches the device)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import quantized_decode_linear_gb300 as qdl
+from quantized_decode_linear_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qdl.h")
+
+INVALID, SCRATCH, UNSUPPORTED = 1, 2, 3
+DEV = 0x7F0000000000  # a 256-byte aligned fake device address; never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return qdl.load()
+
+
+def _declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"QDL_API\s+[\w\s\*]*?\b(qdl_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(qdl.EXPORTS) == names
+
+
+def test_struct_layout_matches_c(tmp_path):
+    prog = tmp_path / "sz.c"
+    prog.write_text(f'''#include <stdio.h>
+#include <stddef.h>
+#include "{HEADER}"
+int main(void) {{
+  printf("%zu %zu %zu %zu %zu\\n", sizeof(qdl_fp8_segment), sizeof(qdl_w8a8_weight),
+         offsetof(qdl_w8a8_weight, count), offsetof(qdl_w8a8_weight, n1),
+         offsetof(qdl_w8a8_weight, magic));
+  return 0;
+}}
+''')
+    exe = tmp_path / "sz"
+    subprocess.run(["gcc", str(prog), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
+    W = qdl.W8A8WeightDesc
+    want = [ctypes.sizeof(qdl.Fp8Segment), ctypes.sizeof(W), W.count.offset, W.n1.offset,
+            W.magic.offset]
+    assert got == want
+
+
+def test_status_strings(lib):
+    for code, name in qdl.STATUS_NAMES.items():
+        assert lib.qdl_status_string(code).decode() == name
+
+
+def test_scratch_bytes(lib):
+    # W8a8Scratch::alloc: 256 * max_k and 256 * max(ceil(max_k / 128), 1) * 4
+    assert qdl.scratch_bytes(0) == (0, 1024)
+    assert qdl.scratch_bytes(100) == (25600, 1024)
+    assert qdl.scratch_bytes(128) == (32768, 1024)
+    assert qdl.scratch_bytes(4096) == (256 * 4096, 256 * 32 * 4)
+    assert qdl.scratch_bytes(4097) == (256 * 4097, 256 * 33 * 4)
+
+
+# ---------------------------------------------------------------- weight descriptor
+
+def _segs(specs, fmt=qdl.PER_ROW):
+    arr = (qdl.Fp8Segment * 3)()
+    for i, spec in enumerate(specs):
+        n, k = spec[0], spec[1]
+        w = spec[2] if len(spec) > 2 else DEV + i * 0x100000
+        s = spec[3] if len(spec) > 3 else DEV + 0x8000000 + i * 0x1000
+        f = spec[4] if len(spec) > 4 else fmt
+        arr[i] = qdl.Fp8Segment(w, s, n, k, f)
+    return arr
+
+
+def _init(lib, specs, count=None, fmt=qdl.PER_ROW):
+    desc = qdl.W8A8WeightDesc()
+    st = lib.qdl_w8a8_weight_init(ctypes.byref(desc), _segs(specs, fmt),
+                                  len(specs) if count is None else count)
+    return st, desc, lib.qdl_last_error().decode()
+
+
+def test_weight_init_ok_and_boundaries(lib):
+    st, d, _ = _init(lib, [(4096, 4096)], fmt=qdl.BLOCK128)
+    assert st == 0 and (d.n, d.n1, d.n2, d.count) == (4096, 4096, 4096, 1)
+    st, d, _ = _init(lib, [(4096, 4096), (1024, 4096), (1000, 4096)], fmt=qdl.BLOCK128)
+    assert st == 0 and (d.n, d.n1, d.n2) == (6120, 4096, 5120)
+    st, d, _ = _init(lib, [(32, 256), (40, 256)])
+    assert st == 0 and (d.n, d.n1, d.n2) == (72, 32, 72)
+
+
+@pytest.mark.parametrize("specs,count,fmt,code,msg", [
+    ([(16, 128)], 0, qdl.PER_ROW, INVALID, "0 segments, want 1..=3"),
+    ([(16, 128)] * 3, 4, qdl.PER_ROW, INVALID, "4 segments, want 1..=3"),
+    ([(16, 100)], None, qdl.PER_ROW, INVALID, "K=100 is not a positive multiple of 128"),
+    ([(16, 0)], None, qdl.PER_ROW, INVALID, "K=0 is not a positive multiple of 128"),
+    ([(16, 128), (16, 256)], None, qdl.PER_ROW, INVALID, "segment 1 is [16, 256]"),
+    ([(16, 128), (16, 128, None, None, qdl.BLOCK128)], None, qdl.PER_ROW, INVALID, "segment 1 is"),
+    ([(0, 128)], None, qdl.PER_ROW, INVALID, "segment 0 is empty"),
+    ([(16, 128), (16, 128, 0)], None, qdl.PER_ROW, INVALID, "segment 1 is empty"),
+    ([(16, 128, DEV, 0)], None, qdl.PER_ROW, INVALID, "segment 0 is empty"),
+    ([(24, 128), (16, 128)], None, qdl.PER_ROW, INVALID, "segment 0 has 24 rows, not a multiple of 16"),
+    ([(128, 128), (64, 128), (8, 128)], None, qdl.BLOCK128, INVALID,
+     "segment 1 has 64 rows, not a multiple of 128"),
+    ([(16, 128, DEV + 8)], None, qdl.PER_ROW, INVALID, "16-byte"),
+    ([(16, 128, DEV, DEV + 2)], None, qdl.PER_ROW, INVALID, "4-byte"),
+    ([(16, 128)], None, 7, INVALID, "is not per-row or 128x128 block"),
+])
+def test_weight_init_rejects(lib, specs, count, fmt, code, msg):
+    st, _, err = _init(lib, specs, count, fmt)
+    assert st == code and msg in err, (st, err)
+
+
+def test_last_segment_may_be_ragged(lib):
+    st, d, _ = _init(lib, [(16, 128), (7, 128)])
+    assert st == 0 and d.n == 23
+    st, d, _ = _init(lib, [(128, 128), (128, 128), (5, 128)], fmt=qdl.BLOCK128)
+    assert st == 0 and d.n == 261
+
+
+# ---------------------------------------------------------------- act quant
+
+def _aq(lib, fmt=qdl.PER_ROW, x=DEV, ldx=4096, rows=8, k=4096, q=DEV + 0x1000000,
+        s=DEV + 0x2000000, qb=256 * 4096, sb=256 * 32 * 4):
+    st = lib.qdl_act_quant(fmt, x, ldx, rows, k, q, s, qb, sb, None)
+    return st, lib.qdl_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,code,msg", [
+    (dict(rows=0), INVALID, "0 rows, want 1..=256"),
+    (dict(rows=257), INVALID, "257 rows, want 1..=256"),
+    (dict(k=4000, ldx=4000), INVALID, "K=4000"),
+    (dict(k=0, ldx=0), INVALID, "K=0"),
+    (dict(k=65536 + 128, ldx=65536 + 128, qb=1 << 30, sb=1 << 30), INVALID, "K=65664"),
+    (dict(ldx=4000), INVALID, "x stride=4000"),
+    (dict(ldx=4100), INVALID, "x stride=4100"),
+    (dict(x=0), INVALID, "x is NULL"),
+    (dict(x=DEV + 8), INVALID, "x must be 16-byte aligned"),
+    (dict(q=0), SCRATCH, "do not fit the scratch"),
+    (dict(qb=8 * 4096 - 1), SCRATCH, "8 rows of K=4096 do not fit the scratch"),
+    (dict(fmt=qdl.PER_ROW, sb=8 * 4 - 1), SCRATCH, "do not fit"),
+    (dict(fmt=qdl.BLOCK128, sb=8 * 32 * 4 - 4), SCRATCH, "do not fit"),
+    (dict(s=0), INVALID, "scale pointer is NULL"),
+    (dict(q=DEV + 4), INVALID, "16-byte"),
+    (dict(fmt=5), INVALID, "not per-row or 128x128 block"),
+])
+def test_act_quant_rejects(lib, kw, code, msg):
+    st, err = _aq(lib, **kw)
+    assert st == code and msg in err, (st, err)
+
+
+def test_act_quant_silu_checks_both_strides(lib):
+    args = dict(rows=4, k=256, q=DEV + 0x1000000, s=DEV + 0x2000000, qb=1 << 20, sb=1 << 16)
+
+    def call(gate, up, ldg, ldu):
+        st = lib.qdl_act_quant_silu(qdl.BLOCK128, gate, up, ldg, ldu, args["rows"], args["k"],
+                                    args["q"], args["s"], args["qb"], args["sb"], None)
+        return st, lib.qdl_last_error().decode()
+
+    assert call(DEV, DEV, 256, 250) == (INVALID, call(DEV, DEV, 256, 250)[1])
+    assert "up stride=250" in call(DEV, DEV, 256, 250)[1]
+    assert "gate stride=100" in call(DEV, DEV, 100, 256)[1]
+    assert "up is NULL" in call(DEV, 0, 256, 256)[1]
+
+
+# ---------------------------------------------------------------- GEMV
+
+def _weight(lib, fmt=qdl.BLOCK128):
+    st, d, _ = _init(lib, [(4096, 4096), (1024, 4096), (1024, 4096)], fmt=fmt)
+    assert st == 0
+    return d
+
+
+def _gemv(lib, d, rows=8, q=DEV + 0x1000000, s=DEV + 0x2000000, qb=1 << 24, sb=1 << 20,
+          out=DEV + 0x4000000, dtype=qdl.OUT_F32, ldc=6144):
+    st = lib.qdl_w8a8_gemv(ctypes.byref(d), q, s, qb, sb, rows, out, dtype, ldc, None)
+    return st, lib.qdl_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,code,msg", [
+    (dict(rows=0), INVALID, "not available for 0 rows of [6144, 4096] Block128"),
+    (dict(rows=300), INVALID, "not available for 300 rows"),
+    (dict(qb=8 * 4096 - 1), SCRATCH, "not available for 8 rows"),
+    (dict(sb=8 * 32 * 4 - 1), SCRATCH, "not available"),
+    (dict(ldc=6143), INVALID, "ldc=6143 < N=6144"),
+    (dict(dtype=3), INVALID, "output dtype 3"),
+    (dict(out=0), INVALID, "output is NULL"),
+    (dict(out=DEV + 2), INVALID, "misaligned"),
+])
+def test_gemv_rejects(lib, kw, code, msg):
+    st, err = _gemv(lib, _weight(lib), **kw)
+    assert st == code and msg in err, (st, err)
+
+
+def test_gemv_rejects_uninitialised_weight(lib):
+    st, err = _gemv(lib, qdl.W8A8WeightDesc())
+    assert st == INVALID and "qdl_w8a8_weight_init" in err
+
+
+def test_proj_checks_input(lib):
+    d = _weight(lib)
+    st = lib.qdl_w8a8_proj(ctypes.byref(d), DEV, 4095, 8, DEV + 0x4000000, 0, 6144,
+                           DEV + 0x1000000, DEV + 0x2000000, 1 << 24, 1 << 20, None)
+    assert st == INVALID and "x stride=4095" in lib.qdl_last_error().decode()
+
+
+# ---------------------------------------------------------------- INT4
+
+def _int4(lib, x=DEV, m=1, k=4096, nq=4096, nkv=1024, group=128, qw=None, sc=None, zr=None, out=None):
+    arr = lambda v, base: (ctypes.c_void_p * 3)(*([base + i * 0x100000 for i in range(3)] if v is None else v))
+    st = lib.qdl_int4_qkv_gemv(x, m, k, nq, nkv, group, arr(qw, DEV + 0x1000000), arr(sc, DEV + 0x2000000),
+                               arr(zr, DEV + 0x3000000), arr(out, DEV + 0x4000000), None)
+    return st, lib.qdl_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(m=0), "m=0"),
+    (dict(group=0), "group=0"),
+    (dict(group=24, k=48), "group=24"),
+    (dict(k=4000), "k=4000"),
+    (dict(nq=4100), "nq=4100"),
+    (dict(nkv=0), "nkv=0"),
+    (dict(x=0), "NULL"),
+    (dict(x=DEV + 4), "x must be 16-byte aligned"),
+    (dict(qw=[DEV, 0, DEV]), "projection 1 has a NULL pointer"),
+    (dict(sc=[DEV, DEV, DEV + 4]), "projection 2 misaligned"),
+])
+def test_int4_rejects(lib, kw, msg):
+    st, err = _int4(lib, **kw)
+    assert st == INVALID and msg in err, (st, err)

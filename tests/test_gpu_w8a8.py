@@ -1,0 +1,175 @@
+"""GPU parity: W8A8 GEMV and the fused decode projections against the oracle
+(w8a8_decode.rs: w8a8_gemv, w8a8_proj, W8a8Weight::boundaries).
+
+Outputs must be within 2e-3 * sum_k |x_hat w_hat| of the oracle's double
+result; activation codes are bit-exact (test_gpu_act_quant.py), so both sides
+see the same x_hat.  Small shapes compare every output; full-size workloads
+compare a sample of outputs the oracle computes one by one."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_decode_linear_gb300 as qdl
+from quantized_decode_linear_gb300 import synthetic as syn
+from _gpu import BF16_REL, bf16_dev, check_close, dev, f32_bits_equal, host, scratch, upload_weight
+
+pytestmark = pytest.mark.gpu
+
+ROWS = [1, 2, 7, 8, 9, 16, 17, 33, 64, 100, 128, 129, 256]
+
+
+def _segments(fmt, k, sizes, seed, std=0.02):
+    return [syn.fp8_weight(n, k, fmt, std, seed + i) for i, n in enumerate(sizes)]
+
+
+def _aligned_sizes(fmt, sizes):
+    a = 16 if fmt == qdl.PER_ROW else 128
+    return [n if i == len(sizes) - 1 else (n + a - 1) // a * a for i, n in enumerate(sizes)]
+
+
+@pytest.mark.parametrize("fmt", [qdl.PER_ROW, qdl.BLOCK128])
+@pytest.mark.parametrize("rows", ROWS)
+def test_gemv_small_all_outputs(fmt, rows):
+    k = 384
+    sizes = _aligned_sizes(fmt, [256, 128, 200])
+    segs = _segments(fmt, k, sizes, seed=rows)
+    x = syn.bf16_normal((rows, k), seed=100 + rows)
+    qo, so = oracle.act_quant(fmt, x, k)
+    yo, bo = oracle.w8a8_gemv(fmt, qo, so, segs)
+    w, _keep = upload_weight(segs, fmt)
+    q = dev(qo)
+    s = dev(so if fmt == qdl.BLOCK128 else so[:, None])
+    out = torch.full((rows, w.n), float("nan"), device="cuda")
+    qdl.w8a8_gemv(w, q, s, rows, out)
+    torch.cuda.synchronize()
+    check_close(host(out), yo, bo, what=f"fmt={fmt} rows={rows}")
+
+
+@pytest.mark.parametrize("fmt", [qdl.PER_ROW, qdl.BLOCK128])
+@pytest.mark.parametrize("sizes,k", [([16], 128), ([48], 256), ([7], 128), ([128, 128, 5], 256),
+                                     ([256, 1000], 1024), ([4096, 1024, 1024], 4096)])
+@pytest.mark.parametrize("rows", [1, 8, 16, 40])
+def test_proj_segments_and_ragged_n(fmt, sizes, k, rows):
+    sizes = _aligned_sizes(fmt, sizes)
+    segs = _segments(fmt, k, sizes, seed=7 + len(sizes))
+    ldx = k + 8
+    x = syn.bf16_normal((rows, ldx), seed=rows * 3 + k)
+    qo, so = oracle.act_quant(fmt, x, k)
+    yo, bo = oracle.w8a8_gemv(fmt, qo, so, segs)
+    w, _keep = upload_weight(segs, fmt)
+    ldc = w.n + 5
+    out = torch.full((rows, ldc), -7.0, device="cuda")
+    q, s = scratch(rows, k, fmt)
+    qdl.w8a8_proj(w, bf16_dev(x), rows, out, q, s, ldx=ldx, ldc=ldc)
+    torch.cuda.synchronize()
+    o = host(out)
+    assert np.all(o[:, w.n:] == -7.0), "columns past N were written"
+    assert np.array_equal(host(q), qo)
+    check_close(o[:, :w.n], yo, bo, what=f"fmt={fmt} sizes={sizes} rows={rows}")
+
+
+@pytest.mark.parametrize("fmt", [qdl.PER_ROW, qdl.BLOCK128])
+def test_bf16_output(fmt):
+    rows, k = 9, 512
+    segs = _segments(fmt, k, [256, 128], seed=3)
+    x = syn.bf16_normal((rows, k), seed=4)
+    qo, so = oracle.act_quant(fmt, x, k)
+    yo, bo = oracle.w8a8_gemv(fmt, qo, so, segs)
+    w, _keep = upload_weight(segs, fmt)
+    out = torch.zeros((rows, w.n), dtype=torch.bfloat16, device="cuda")
+    q, s = scratch(rows, k, fmt)
+    qdl.w8a8_proj(w, bf16_dev(x), rows, out, q, s, out_dtype=qdl.OUT_BF16)
+    torch.cuda.synchronize()
+    check_close(host(out.float()), yo, bo, extra_rel=BF16_REL, what="bf16 out")
+
+
+def test_segment_identities_on_gpu():
+    """3 segments == 3 single-segment calls concatenated; rows == single-row calls"""
+    fmt, k, rows = qdl.BLOCK128, 256, 5
+    segs = _segments(fmt, k, [128, 128, 64], seed=11)
+    x = syn.bf16_normal((rows, k), seed=12)
+    qo, so = oracle.act_quant(fmt, x, k)
+    q, s = dev(qo), dev(so)
+    w, _k1 = upload_weight(segs, fmt)
+    full = torch.empty((rows, w.n), device="cuda")
+    qdl.w8a8_gemv(w, q, s, rows, full)
+    parts = []
+    for seg in segs:
+        ws, _k2 = upload_weight([seg], fmt)
+        o = torch.empty((rows, ws.n), device="cuda")
+        qdl.w8a8_gemv(ws, q, s, rows, o)
+        parts.append(o)
+    torch.cuda.synchronize()
+    yo, bo = oracle.w8a8_gemv(fmt, qo, so, segs)
+    check_close(host(full), yo, bo)
+    check_close(host(torch.cat(parts, 1)), yo, bo)
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+def _samples(rows, n, segments, count, seed):
+    rng = np.random.default_rng(seed)
+    r = [0, rows - 1, 0, rows - 1]
+    c = [0, n - 1, n - 1, 0]
+    start = 0
+    for sz in segments:  # first and last column of every segment
+        r += [rng.integers(rows), rng.integers(rows)]
+        c += [start, start + sz - 1]
+        start += sz
+    r = np.array(r + list(rng.integers(0, rows, count)), np.int32)
+    c = np.array(c + list(rng.integers(0, n, count)), np.int32)
+    return r, c
+
+
+def _full_workload(name, rows_list=None, samples=1500):
+    wl = syn.WORKLOADS[name]
+    segs = syn.w8a8_weights(wl)
+    w, _keep = upload_weight(segs, wl.fmt)
+    for rows in rows_list or wl.rows:
+        xb = syn.w8a8_activations(wl, rows)
+        q, s = scratch(rows, wl.k, wl.fmt)
+        out = torch.empty((rows, wl.n), device="cuda")
+        if wl.silu:
+            d = bf16_dev(xb)
+            qdl.w8a8_proj_silu(w, d[:, :wl.k], d[:, wl.k:], rows, out, q, s, ld_gate=2 * wl.k,
+                               ld_up=2 * wl.k)
+            qo, so = oracle.act_quant_silu(wl.fmt, xb[:, :wl.k], xb[:, wl.k:], wl.k)
+        else:
+            qdl.w8a8_proj(w, bf16_dev(xb), rows, out, q, s)
+            qo, so = oracle.act_quant(wl.fmt, xb, wl.k)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(q), qo), f"{name} rows={rows}: activation codes differ"
+        sh = host(s)
+        assert f32_bits_equal(sh[:, 0] if wl.fmt == qdl.PER_ROW else sh, so)
+        r, c = _samples(rows, wl.n, wl.segments, samples, seed=rows)
+        ys, bs = oracle.w8a8_gemv_sampled(wl.fmt, qo, so, segs, r, c)
+        o = host(out)
+        check_close(o[r, c], ys, bs, what=f"{name} rows={rows}")
+        assert np.all(np.isfinite(o))
+
+
+def test_full_perrow_m1_k1024_n1024_every_output():
+    wl = syn.WORKLOADS["w8a8_perrow_m1_k1024_n1024"]
+    segs = syn.w8a8_weights(wl)
+    w, _keep = upload_weight(segs, wl.fmt)
+    xb = syn.w8a8_activations(wl, 1)
+    q, s = scratch(1, wl.k, wl.fmt)
+    out = torch.empty((1, wl.n), device="cuda")
+    qdl.w8a8_proj(w, bf16_dev(xb), 1, out, q, s)
+    torch.cuda.synchronize()
+    qo, so = oracle.act_quant(wl.fmt, xb, wl.k)
+    yo, bo = oracle.w8a8_gemv(wl.fmt, qo, so, segs)
+    check_close(host(out), yo, bo)
+
+
+def test_full_block128_qkv_m8():
+    _full_workload("w8a8_block128_qkv_m8_k4096_n4096+1024+1024")
+
+
+def test_full_perrow_silu_down_m64():
+    _full_workload("w8a8_perrow_silu_down_m64_k14336_n4096")
+
+
+def test_full_block128_gateup_sweep():
+    _full_workload("w8a8_block128_gateup_k8192_n14336+14336", samples=600)
