@@ -185,6 +185,35 @@ QDL_API qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uin
                              uint32_t group, const uint32_t *const *qw, const float *const *sc,
                              const float *const *zr, float *const *out, void *stream);
 
+/* Size of the library's own device array used by qdl_w8a8_proj_static. */
+#define QDL_STATIC_SCRATCH_BYTES (4 << 20)
+
+/* Decode projection that allocates nothing: qdl_w8a8_proj without caller
+ * scratch.  The pages have no counterpart; this entry point exists for
+ * callers that cannot allocate device memory -- for example a plugin that a
+ * host framework hands only its input and output buffers (the framework owns
+ * every allocation and offers no workspace), or a latency-critical decode
+ * loop that may not risk cudaMalloc's implicit device synchronisation or an
+ * allocation failure mid-step.
+ *   The activation codes and scales are kept in one device array built into
+ * the library, QDL_STATIC_SCRATCH_BYTES (4 MiB) long, which every GPU that
+ * loads the library holds until the process exits.  Calls need
+ * rows*K bytes (rounded up to 256) plus rows*scales_per_row*4 bytes of it;
+ * larger calls return QDL_ERR_UNSUPPORTED (256 rows fit up to K = 15872).
+ *   The first call on a device, made with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call before
+ * any stream capture.  The call never uses cudaMalloc, cudaFree or any
+ * allocating routine.
+ *   All calls share the one array and it keeps the last call's contents:
+ * calls that can overlap on the GPU (different streams, or several host
+ * threads) race on it and must be serialised by the caller.  Each call
+ * overwrites every byte it later reads, so no clearing is needed.
+ * Arguments and checks are those of qdl_w8a8_proj for w, x, ldx, rows, out,
+ * out_dtype and ldc. */
+QDL_API qdl_status qdl_w8a8_proj_static(const qdl_w8a8_weight *w, const void *x, uint32_t ldx,
+                                        uint32_t rows, void *out, int32_t out_dtype, uint32_t ldc,
+                                        void *stream);
+
 /* Reads and clears the device-side fault word that bounded waits in the
  * kernels set when they give up (synchronises `stream`).  Returns QDL_OK or
  * QDL_ERR_DEVICE_TIMEOUT. */

@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "QDL_OK", 1: "QDL_ERR_INVALID_ARG", 2: "QDL_ERR_SCRATCH_TOO_S
 # every symbol include/qdl.h declares
 EXPORTS = ("qdl_w8a8_weight_init", "qdl_scratch_bytes", "qdl_act_quant", "qdl_act_quant_silu",
            "qdl_w8a8_gemv", "qdl_w8a8_proj", "qdl_w8a8_proj_silu", "qdl_int4_qkv_gemv",
-           "qdl_check_device_fault", "qdl_last_error", "qdl_status_string")
+           "qdl_w8a8_proj_static", "qdl_check_device_fault", "qdl_last_error",
+           "qdl_status_string")
 
 
 class QdlError(RuntimeError):
@@ -74,6 +75,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "qdl_w8a8_proj": [P, P, U32, U32, P, I32, U32, P, P, SZ, SZ, P],
             "qdl_w8a8_proj_silu": [P, P, P, U32, U32, U32, P, I32, U32, P, P, SZ, SZ, P],
             "qdl_int4_qkv_gemv": [P, U32, U32, U32, U32, U32, P, P, P, P, P],
+            "qdl_w8a8_proj_static": [P, P, U32, U32, P, I32, U32, P],
             "qdl_check_device_fault": [P],
             "qdl_last_error": [],
             "qdl_status_string": [ctypes.c_int],
@@ -199,6 +201,23 @@ def w8a8_proj_silu(w: W8A8Weight, gate, up, rows: int, out, q, q_scale, out_dtyp
     _check(load().qdl_w8a8_proj_silu(ctypes.byref(w.desc), _ptr(gate), _ptr(up), ld_gate, ld_up, rows,
                                      _ptr(out), out_dtype, ldc, _ptr(q), _ptr(q_scale), _nbytes(q),
                                      _nbytes(q_scale), _stream(stream)))
+
+
+STATIC_SCRATCH_BYTES = 4 << 20
+
+
+def w8a8_proj_static(w: W8A8Weight, x, rows: int, out, out_dtype: int = OUT_F32,
+                     ldx: int | None = None, ldc: int | None = None, stream=None):
+    """qdl_w8a8_proj without caller scratch, for callers that cannot allocate
+    device memory (a plugin handed only input and output buffers, or a decode
+    loop that must not risk cudaMalloc's synchronisation or failure).  Uses the
+    library's built-in 4 MiB device array, shared by every call: calls that may
+    overlap on the GPU must be serialised by the caller.  Make the first call on
+    each device before any stream capture (it looks up the array's address)."""
+    ldx = x.stride(0) if ldx is None else ldx
+    ldc = out.stride(0) if ldc is None else ldc
+    _check(load().qdl_w8a8_proj_static(ctypes.byref(w.desc), _ptr(x), ldx, rows, _ptr(out), out_dtype,
+                                       ldc, _stream(stream)))
 
 
 # ---------------------------------------------------------------- INT4

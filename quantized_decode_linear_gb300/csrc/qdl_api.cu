@@ -321,6 +321,70 @@ qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq
     return ok();
 }
 
+// ---------------------------------------------------------------- no-allocation variant
+//
+// qdl_w8a8_proj_static: the decode projection for callers that cannot
+// allocate device memory.  Its activation codes and scales live in the
+// fixed device array below instead of caller scratch.  The array's host-side
+// name is only a stand-in for the symbol; the device address is looked up
+// once per device (cudaGetSymbolAddress, on the first call made with that
+// device current) and then passed to the kernels like any scratch pointer.
+
+static __device__ __align__(256) uint8_t g_static_scratch[QDL_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_static_mu;
+std::vector<void *> g_static_addr;  // per device; nullptr until looked up
+
+qdl_status static_scratch_address(void **addr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail("w8a8_proj_static", e);
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if ((int)g_static_addr.size() <= dev) g_static_addr.resize(dev + 1, nullptr);
+    if (g_static_addr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess || p == nullptr) return cuda_fail("w8a8_proj_static: cudaGetSymbolAddress", e);
+        g_static_addr[dev] = p;
+    }
+    *addr = g_static_addr[dev];
+    return QDL_OK;
+}
+
+}  // namespace
+
+qdl_status qdl_w8a8_proj_static(const qdl_w8a8_weight *w, const void *x, uint32_t ldx, uint32_t rows, void *out,
+                                int32_t out_dtype, uint32_t ldc, void *stream) {
+    const char *who = "w8a8_proj_static";
+    qdl_status st = check_weight(who, w);
+    if (st != QDL_OK) return st;
+    if (rows < 1 || rows > (uint32_t)kMaxRows) return fail(QDL_ERR_INVALID_ARG, "%s: %u rows, want 1..=%d", who, rows, kMaxRows);
+    const size_t q_bytes = (size_t)rows * w->k;
+    const size_t scale_off = (q_bytes + 255) / 256 * 256;
+    const size_t scale_bytes = (size_t)rows * scales_per_row(w->format, w->k) * 4;
+    if (scale_off + scale_bytes > (size_t)QDL_STATIC_SCRATCH_BYTES)
+        return fail(QDL_ERR_UNSUPPORTED, "%s: %u rows of K=%u need %zu bytes of static scratch, the limit is %d", who, rows,
+                    w->k, scale_off + scale_bytes, QDL_STATIC_SCRATCH_BYTES);
+    if (ldc < w->n) return fail(QDL_ERR_INVALID_ARG, "%s: ldc=%u < N=%u", who, ldc, w->n);
+    if (out_dtype != QDL_OUT_F32 && out_dtype != QDL_OUT_BF16)
+        return fail(QDL_ERR_INVALID_ARG, "%s: output dtype %d is not F32 or BF16", who, (int)out_dtype);
+    if (out == nullptr || !aligned(out, out_dtype == QDL_OUT_BF16 ? 2 : 4))
+        return fail(QDL_ERR_INVALID_ARG, "%s: output is NULL or misaligned", who);
+    if ((st = check_input(who, "x", x, ldx, w->k)) != QDL_OK) return st;
+    void *base = nullptr;
+    if ((st = static_scratch_address(&base)) != QDL_OK) return st;
+    uint8_t *q = static_cast<uint8_t *>(base);
+    float *q_scale = reinterpret_cast<float *>(static_cast<uint8_t *>(base) + scale_off);
+    // every code and scale the GEMV reads is written by the quantiser first,
+    // so nothing left over from an earlier call is ever read
+    ActQuantArgs a = {static_cast<const uint16_t *>(x), nullptr, ldx, 0, rows, w->k, q, q_scale};
+    cudaError_t e = launch_act_quant(a, w->format, false, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(who, e);
+    return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, static_cast<cudaStream_t>(stream));
+}
+
 qdl_status qdl_check_device_fault(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
