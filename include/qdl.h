@@ -219,6 +219,19 @@ QDL_API qdl_status qdl_w8a8_proj_static(const qdl_w8a8_weight *w, const void *x,
  * QDL_ERR_DEVICE_TIMEOUT. */
 QDL_API qdl_status qdl_check_device_fault(void *stream);
 
+/* Self-test of the bounded device-side waits (no counterpart on the pages).
+ * Runs qdl_w8a8_gemv on valid arguments (ldc = N) with its first pipeline
+ * stage deliberately never loaded, so the kernel's waits give up after
+ * limit_us microseconds (1..1000000); the kernel records the timeout,
+ * drains its in-flight copies with bounded waits and returns normally, and
+ * the call then reads the fault word like qdl_check_device_fault.  Returns
+ * QDL_ERR_DEVICE_TIMEOUT when the mechanism worked.  `out` receives
+ * unspecified values.  Synchronises `stream`. */
+QDL_API qdl_status qdl_selftest_bounded_wait(const qdl_w8a8_weight *w, const uint8_t *q,
+                                             const float *q_scale, size_t q_bytes,
+                                             size_t scale_bytes, uint32_t rows, float *out,
+                                             uint32_t limit_us, void *stream);
+
 /* Message for the last error on the calling thread ("" if none). */
 QDL_API const char *qdl_last_error(void);
 

@@ -29,8 +29,8 @@ STATUS_NAMES = {0: "QDL_OK", 1: "QDL_ERR_INVALID_ARG", 2: "QDL_ERR_SCRATCH_TOO_S
 # every symbol include/qdl.h declares
 EXPORTS = ("qdl_w8a8_weight_init", "qdl_scratch_bytes", "qdl_act_quant", "qdl_act_quant_silu",
            "qdl_w8a8_gemv", "qdl_w8a8_proj", "qdl_w8a8_proj_silu", "qdl_int4_qkv_gemv",
-           "qdl_w8a8_proj_static", "qdl_check_device_fault", "qdl_last_error",
-           "qdl_status_string")
+           "qdl_w8a8_proj_static", "qdl_check_device_fault", "qdl_selftest_bounded_wait",
+           "qdl_last_error", "qdl_status_string")
 
 
 class QdlError(RuntimeError):
@@ -77,6 +77,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "qdl_int4_qkv_gemv": [P, U32, U32, U32, U32, U32, P, P, P, P, P],
             "qdl_w8a8_proj_static": [P, P, U32, U32, P, I32, U32, P],
             "qdl_check_device_fault": [P],
+            "qdl_selftest_bounded_wait": [P, P, P, SZ, SZ, U32, P, U32, P],
             "qdl_last_error": [],
             "qdl_status_string": [ctypes.c_int],
         }
@@ -228,6 +229,14 @@ def int4_qkv_gemv(x, m: int, k: int, nq: int, nkv: int, group: int, qw, sc, zr, 
     arr = lambda xs: (ctypes.c_void_p * 3)(*[_ptr(t) for t in xs])
     _check(load().qdl_int4_qkv_gemv(_ptr(x), m, k, nq, nkv, group, arr(qw), arr(sc), arr(zr), arr(out),
                                     _stream(stream)))
+
+
+def selftest_bounded_wait(w: W8A8Weight, q, q_scale, rows: int, out, limit_us: int = 20000,
+                          stream=None) -> int:
+    """Run the GEMV with one pipeline stage withheld so that its bounded waits
+    give up; returns the status (QDL_ERR_DEVICE_TIMEOUT = 5 when they did)."""
+    return load().qdl_selftest_bounded_wait(ctypes.byref(w.desc), _ptr(q), _ptr(q_scale), _nbytes(q),
+                                            _nbytes(q_scale), rows, _ptr(out), limit_us, _stream(stream))
 
 
 def check_device_fault(stream=None):

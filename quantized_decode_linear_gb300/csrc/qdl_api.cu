@@ -10,7 +10,7 @@
 #include <string>
 #include <vector>
 
-#include "qdl_internal.cuh"
+#include "tma_pipe.cuh"
 
 namespace qdl {
 
@@ -84,7 +84,8 @@ qdl_status check_weight(const char *who, const qdl_w8a8_weight *w) {
 }
 
 qdl_status launch_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *q_scale, uint32_t rows, void *out,
-                       int32_t out_dtype, uint32_t ldc, cudaStream_t stream) {
+                       int32_t out_dtype, uint32_t ldc, cudaStream_t stream, uint32_t debug_skip_iter = ~0u,
+                       uint64_t wait_limit_ns = kWaitLimitNs) {
     const size_t spr = scales_per_row(w->format, w->k);
     const size_t elt = out_dtype == QDL_OUT_BF16 ? 2 : 4;
     W8A8Args a = {};
@@ -94,6 +95,9 @@ qdl_status launch_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *
     a.sw1 = w->count > 1 ? w->segs[1].scale : w->segs[0].scale;
     a.w2 = w->count > 2 ? w->segs[2].weight : w->segs[0].weight;
     a.sw2 = w->count > 2 ? w->segs[2].scale : w->segs[0].scale;
+    const uint8_t *seg_w[3] = {a.w0, a.w1, a.w2};
+    const uint32_t seg_n[3] = {w->segs[0].n, w->count > 1 ? w->segs[1].n : w->segs[0].n,
+                               w->count > 2 ? w->segs[2].n : w->segs[0].n};
     a.ldc = ldc;
     a.out_bf16 = out_dtype == QDL_OUT_BF16;
     a.n = w->n;
@@ -101,14 +105,16 @@ qdl_status launch_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *
     a.n1 = w->n1;
     a.n2 = w->n2;
     a.kb = w->k / kKUnit;
-    // the register-streaming kernel takes up to 16 token rows per pass
+    a.debug_skip_iter = debug_skip_iter;
+    a.wait_limit_ns = wait_limit_ns;
+    // the streaming kernel takes up to 16 token rows per pass
     for (uint32_t done = 0; done < rows; done += 16) {
         const uint32_t m = rows - done < 16 ? rows - done : 16;
         a.q = q + (size_t)done * w->k;
         a.sa = q_scale + (size_t)done * spr;
         a.out = static_cast<char *>(out) + (size_t)done * ldc * elt;
         a.m = m;
-        cudaError_t e = launch_w8a8_gemv_mma(a, w->format, stream);
+        cudaError_t e = launch_w8a8_gemv_tma(a, w->format, seg_w, seg_n, stream);
         if (e != cudaSuccess) return cuda_fail("qdl_w8a8_gemv", e);
     }
     return ok();
@@ -388,7 +394,24 @@ qdl_status qdl_w8a8_proj_static(const qdl_w8a8_weight *w, const void *x, uint32_
 qdl_status qdl_check_device_fault(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
+    uint32_t word = 0;
+    if ((e = read_and_clear_gemv_fault(&word)) != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
+    if (word != 0)
+        return fail(QDL_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up (fault word 0x%x: 1 = producer, 2 = consumer)",
+                    word);
     return ok();
+}
+
+qdl_status qdl_selftest_bounded_wait(const qdl_w8a8_weight *w, const uint8_t *q, const float *q_scale, size_t q_bytes,
+                                     size_t scale_bytes, uint32_t rows, float *out, uint32_t limit_us, void *stream) {
+    const char *who = "selftest_bounded_wait";
+    qdl_status st = check_gemv(who, w, q, q_scale, q_bytes, scale_bytes, rows, out, QDL_OUT_F32, w ? w->n : 0);
+    if (st != QDL_OK) return st;
+    if (limit_us == 0 || limit_us > 1000000) return fail(QDL_ERR_INVALID_ARG, "%s: limit_us=%u, want 1..1000000", who, limit_us);
+    st = launch_gemv(w, q, q_scale, rows, out, QDL_OUT_F32, w->n, static_cast<cudaStream_t>(stream), 0,
+                     (uint64_t)limit_us * 1000ull);
+    if (st != QDL_OK) return st;
+    return qdl_check_device_fault(stream);
 }
 
 }  // extern "C"

@@ -35,6 +35,8 @@ struct W8A8Args {
     uint32_t n, k;      // total output width, reduction length
     uint32_t n1, n2;    // segment split points
     uint32_t kb;        // k / 128
+    uint32_t debug_skip_iter;  // self-test only: pipeline stage never loaded (else ~0u)
+    uint64_t wait_limit_ns;    // limit of every device-side wait
 };
 
 struct Int4Args {
@@ -54,7 +56,9 @@ struct Int4Args {
 // the C-ABI layer before these are called.
 
 cudaError_t launch_act_quant(const ActQuantArgs &a, int format, bool silu, cudaStream_t s);
-cudaError_t launch_w8a8_gemv_mma(const W8A8Args &a, int format, cudaStream_t s);
+cudaError_t launch_w8a8_gemv_tma(const W8A8Args &a, int format, const uint8_t *const seg_w[3],
+                                 const uint32_t seg_n[3], cudaStream_t s);
+cudaError_t read_and_clear_gemv_fault(uint32_t *value);
 cudaError_t launch_int4_qkv(const Int4Args &a, cudaStream_t s);
 
 int device_sm_count();  // of the current device, cached
