@@ -17,6 +17,10 @@ namespace qdl {
 namespace {
 
 constexpr uint32_t kWeightMagic = 0x51444C57u;  // "QDLW"
+#ifndef QDL_MMA_MAX_ROWS
+#define QDL_MMA_MAX_ROWS 0
+#endif
+constexpr uint32_t kMmaMaxRows = QDL_MMA_MAX_ROWS;  // <= 16
 thread_local std::string g_last_error;
 
 qdl_status fail(qdl_status s, const char *fmt, ...) {
@@ -107,16 +111,25 @@ qdl_status launch_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *
     a.kb = w->k / kKUnit;
     a.debug_skip_iter = debug_skip_iter;
     a.wait_limit_ns = wait_limit_ns;
-    // the streaming kernel takes up to 16 token rows per pass
-    for (uint32_t done = 0; done < rows; done += 16) {
-        const uint32_t m = rows - done < 16 ? rows - done : 16;
-        a.q = q + (size_t)done * w->k;
-        a.sa = q_scale + (size_t)done * spr;
-        a.out = static_cast<char *>(out) + (size_t)done * ldc * elt;
-        a.m = m;
-        cudaError_t e = launch_w8a8_gemv_tma(a, w->format, seg_w, seg_n, stream);
+    // Token rows up to QDL_MMA_MAX_ROWS go to the mma.sync streaming kernel;
+    // all others take one pass of the tcgen05 kernel (rows <= 256).
+    if (rows > kMmaMaxRows) {
+        a.q = q;
+        a.sa = q_scale;
+        a.out = out;
+        a.m = rows;
+        cudaError_t e = launch_w8a8_gemm_tc(a, w->format, seg_w, seg_n, stream);
         if (e != cudaSuccess) return cuda_fail("qdl_w8a8_gemv", e);
+        return ok();
     }
+    (void)spr;
+    (void)elt;
+    a.q = q;
+    a.sa = q_scale;
+    a.out = out;
+    a.m = rows;
+    cudaError_t e = launch_w8a8_gemv_tma(a, w->format, seg_w, seg_n, stream);
+    if (e != cudaSuccess) return cuda_fail("qdl_w8a8_gemv", e);
     return ok();
 }
 
@@ -394,10 +407,12 @@ qdl_status qdl_w8a8_proj_static(const qdl_w8a8_weight *w, const void *x, uint32_
 qdl_status qdl_check_device_fault(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
-    uint32_t word = 0;
+    uint32_t word = 0, word_tc = 0;
     if ((e = read_and_clear_gemv_fault(&word)) != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
+    if ((e = read_and_clear_tc_fault(&word_tc)) != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
+    word |= word_tc;
     if (word != 0)
-        return fail(QDL_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up (fault word 0x%x: 1 = producer, 2 = consumer)",
+        return fail(QDL_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up (fault word 0x%x: 1 = producer, 2/8 = consumer or MMA, 4/16/32 = accumulator)",
                     word);
     return ok();
 }

@@ -59,6 +59,11 @@ cudaError_t launch_act_quant(const ActQuantArgs &a, int format, bool silu, cudaS
 cudaError_t launch_w8a8_gemv_tma(const W8A8Args &a, int format, const uint8_t *const seg_w[3],
                                  const uint32_t seg_n[3], cudaStream_t s);
 cudaError_t read_and_clear_gemv_fault(uint32_t *value);
+cudaError_t launch_w8a8_gemm_tc(const W8A8Args &a, int format, const uint8_t *const seg_w[3],
+                                const uint32_t seg_n[3], cudaStream_t s);
+cudaError_t read_and_clear_tc_fault(uint32_t *value);
+uint32_t tc_bucket(uint32_t m);  // MMA N of the tensor-core kernel for m token rows
+uint32_t choose_split_k(uint32_t tiles, uint32_t kb, uint32_t slots);
 cudaError_t launch_int4_qkv(const Int4Args &a, cudaStream_t s);
 
 int device_sm_count();  // of the current device, cached

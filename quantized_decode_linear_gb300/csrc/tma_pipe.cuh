@@ -16,6 +16,9 @@ namespace qdl {
 cudaError_t make_tmap_u8(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t stride,
                          uint32_t box_cols, uint32_t box_rows);
 
+// CTAs of a kernel that can be resident on one SM at once.
+int resident_ctas(const void *func, int threads, size_t smem, int tmem_cols);
+
 // Default limit of every bounded device-side wait.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 

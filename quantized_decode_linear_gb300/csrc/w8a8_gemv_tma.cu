@@ -285,7 +285,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (uint32_t idx = threadIdx.x; idx < span * L::kActRows; idx += blockDim.x) {
         const uint32_t tok = idx / span, lrow = r_lo + idx % span;
         float sum = 0.0f;
-        for (uint32_t rk = 0; rk < split; ++rk) sum += cluster.map_shared_rank(red, rk)[tok * kRowsPerCta + lrow];
+        float v[8];
+#pragma unroll
+        for (int rk = 0; rk < 8; ++rk)
+            v[rk] = rk < (int)split ? cluster.map_shared_rank(red, rk)[tok * kRowsPerCta + lrow] : 0.0f;
+#pragma unroll
+        for (int rk = 0; rk < 8; ++rk) sum += v[rk];  // rank order; absent ranks add +0
         store(tok, tile_row0 + lrow, sum);
     }
     cluster.sync();
@@ -318,20 +323,17 @@ int occupancy() {
     if (cache[dev] == 0) {
         cudaFuncSetAttribute(w8a8_gemv_tma_kernel<NT, kBlock>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)Layout<NT>::kAlloc);
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, w8a8_gemv_tma_kernel<NT, kBlock>, kThreads,
-                                                          Layout<NT>::kAlloc) != cudaSuccess ||
-            n < 1)
-            n = 1;
-        cache[dev] = n;
+        cache[dev] = resident_ctas((const void *)w8a8_gemv_tma_kernel<NT, kBlock>, kThreads, Layout<NT>::kAlloc, 0);
     }
     return cache[dev];
 }
 
+}  // namespace
+
 // Split of K over a cluster of CTAs.  Work is in 128-blocks; a CTA of a split
 // s takes ceil(kb/s) of them.  Choose s in 1..8 that minimises the slowest
 // SM's work, waves x ceil(kb/s), with `slots` co-resident CTAs.
-uint32_t choose_split(uint32_t tiles, uint32_t kb, uint32_t slots) {
+uint32_t choose_split_k(uint32_t tiles, uint32_t kb, uint32_t slots) {
 #ifdef QDL_TUNE_SPLIT
     if (QDL_TUNE_SPLIT > 0) return QDL_TUNE_SPLIT < kb ? QDL_TUNE_SPLIT : kb;
 #endif
@@ -349,11 +351,13 @@ uint32_t choose_split(uint32_t tiles, uint32_t kb, uint32_t slots) {
     return best;
 }
 
+namespace {
+
 template <int NT, bool kBlock>
 cudaError_t launch_variant(const W8A8Args &a, const CUtensorMap (&maps)[4], cudaStream_t s) {
     const uint32_t tiles = (a.n + kRowsPerCta - 1) / kRowsPerCta;
     const uint32_t slots = (uint32_t)(device_sm_count() * occupancy<NT, kBlock>());
-    const uint32_t split = choose_split(tiles, a.kb, slots);
+    const uint32_t split = choose_split_k(tiles, a.kb, slots);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tiles, split, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -370,6 +374,25 @@ cudaError_t launch_variant(const W8A8Args &a, const CUtensorMap (&maps)[4], cuda
 }
 
 }  // namespace
+
+// CTAs of a kernel that fit on one SM at once: shared memory (with the per-CTA
+// reservation), threads, registers and tensor-memory columns (512 per SM).
+int resident_ctas(const void *func, int threads, size_t smem, int tmem_cols) {
+    int dev = 0, smem_sm = 0, reserved = 0, threads_sm = 0, regs_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev);
+    cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+    cudaFuncAttributes fa = {};
+    cudaFuncGetAttributes(&fa, func);
+    int n = smem_sm > 0 ? smem_sm / (int)(smem + reserved) : 1;
+    if (threads_sm > 0) n = n < threads_sm / threads ? n : threads_sm / threads;
+    const int regs_cta = ((fa.numRegs > 0 ? fa.numRegs : 32) + 7) / 8 * 8 * threads;
+    if (regs_sm > 0) n = n < regs_sm / regs_cta ? n : regs_sm / regs_cta;
+    if (tmem_cols > 0) n = n < 512 / tmem_cols ? n : 512 / tmem_cols;
+    return n < 1 ? 1 : n;
+}
 
 cudaError_t make_tmap_u8(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t stride,
                          uint32_t box_cols, uint32_t box_rows) {
