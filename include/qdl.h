@@ -214,6 +214,23 @@ QDL_API qdl_status qdl_w8a8_proj_static(const qdl_w8a8_weight *w, const void *x,
                                         uint32_t rows, void *out, int32_t out_dtype, uint32_t ldc,
                                         void *stream);
 
+/* Launch plan of qdl_w8a8_gemv for `rows` token rows on the current device:
+ * which kernel runs and how the work is cut (no counterpart on the pages;
+ * for tuning and tests).  Queries the device's occupancy tables; launches
+ * nothing. */
+typedef struct {
+    int32_t kernel;      /* 0 = tcgen05 (tensor memory), 1 = mma.sync streaming */
+    uint32_t mma_n;      /* token columns per MMA (tcgen05: 16..256) */
+    uint32_t tiles;      /* 128-row output tiles */
+    uint32_t split_k;    /* CTAs per tile along K (one cluster) */
+    uint32_t stages;     /* shared-memory pipeline stages per CTA */
+    uint32_t threads;    /* threads per CTA */
+    uint32_t smem_bytes; /* dynamic shared memory per CTA */
+    int32_t resident_clusters; /* clusters of split_k CTAs that fit the device at once */
+} qdl_plan;
+
+QDL_API qdl_status qdl_w8a8_plan(const qdl_w8a8_weight *w, uint32_t rows, qdl_plan *plan);
+
 /* Reads and clears the device-side fault word that bounded waits in the
  * kernels set when they give up (synchronises `stream`).  Returns QDL_OK or
  * QDL_ERR_DEVICE_TIMEOUT. */

@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "QDL_OK", 1: "QDL_ERR_INVALID_ARG", 2: "QDL_ERR_SCRATCH_TOO_S
 # every symbol include/qdl.h declares
 EXPORTS = ("qdl_w8a8_weight_init", "qdl_scratch_bytes", "qdl_act_quant", "qdl_act_quant_silu",
            "qdl_w8a8_gemv", "qdl_w8a8_proj", "qdl_w8a8_proj_silu", "qdl_int4_qkv_gemv",
-           "qdl_w8a8_proj_static", "qdl_check_device_fault", "qdl_selftest_bounded_wait",
+           "qdl_w8a8_proj_static", "qdl_w8a8_plan", "qdl_check_device_fault", "qdl_selftest_bounded_wait",
            "qdl_last_error", "qdl_status_string")
 
 
@@ -43,6 +43,15 @@ class QdlError(RuntimeError):
 class Fp8Segment(ctypes.Structure):
     _fields_ = [("weight", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("n", ctypes.c_uint32),
                 ("k", ctypes.c_uint32), ("format", ctypes.c_int32)]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("mma_n", ctypes.c_uint32), ("tiles", ctypes.c_uint32),
+                ("split_k", ctypes.c_uint32), ("stages", ctypes.c_uint32), ("threads", ctypes.c_uint32),
+                ("smem_bytes", ctypes.c_uint32), ("resident_clusters", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
 
 
 class W8A8WeightDesc(ctypes.Structure):
@@ -77,6 +86,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "qdl_int4_qkv_gemv": [P, U32, U32, U32, U32, U32, P, P, P, P, P],
             "qdl_w8a8_proj_static": [P, P, U32, U32, P, I32, U32, P],
             "qdl_check_device_fault": [P],
+            "qdl_w8a8_plan": [P, U32, P],
             "qdl_selftest_bounded_wait": [P, P, P, SZ, SZ, U32, P, U32, P],
             "qdl_last_error": [],
             "qdl_status_string": [ctypes.c_int],
@@ -155,6 +165,13 @@ def w8a8_weight_init(segments, fmt: int) -> W8A8Weight:
     desc = W8A8WeightDesc()
     _check(load().qdl_w8a8_weight_init(ctypes.byref(desc), segs, len(segments)))
     return W8A8Weight(desc, keep)
+
+
+def w8a8_plan(w: W8A8Weight, rows: int) -> dict:
+    """Kernel and work split that qdl_w8a8_gemv would use for `rows` rows."""
+    p = Plan()
+    _check(load().qdl_w8a8_plan(ctypes.byref(w.desc), rows, ctypes.byref(p)))
+    return p.as_dict()
 
 
 def scratch_bytes(max_k: int):

@@ -38,8 +38,17 @@ __device__ __forceinline__ float quant_operand(float v, float scale) {
 
 // ---------------------------------------------------------------- Block128
 
+// Programmatic launch overlap: the input comes from the previous kernel and
+// the scratch written here may still be read by it, so wait for it first;
+// then let the next kernel (the GEMV) start streaming its weights at once.
+__device__ __forceinline__ void dependent_launch_prologue() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 template <bool kSilu>
 __global__ void __launch_bounds__(256) act_quant_g128_kernel(ActQuantArgs a) {
+    dependent_launch_prologue();
     const uint32_t groups_per_row = a.k / kKUnit;
     const uint32_t gid = blockIdx.x * 8 + (threadIdx.x >> 5);
     const uint32_t lane = threadIdx.x & 31;
@@ -73,6 +82,7 @@ __global__ void __launch_bounds__(256) act_quant_g128_kernel(ActQuantArgs a) {
 template <bool kSilu, int UPT>
 __global__ void __launch_bounds__(1024) act_quant_row_kernel(ActQuantArgs a) {
     __shared__ float warp_max[32];
+    dependent_launch_prologue();
     const uint32_t row = blockIdx.x;
     const uint32_t units = a.k / 8;
     const uint16_t *xa = a.a + (size_t)row * a.lda;
@@ -126,28 +136,36 @@ __global__ void __launch_bounds__(1024) act_quant_row_kernel(ActQuantArgs a) {
     if (threadIdx.x == 0) a.s[row] = scale;
 }
 
+template <typename Kernel>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, cudaStream_t s, const ActQuantArgs &a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = QDL_TUNE_PDL ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 template <bool kSilu>
 cudaError_t launch_row(const ActQuantArgs &a, cudaStream_t s) {
     const uint32_t units = a.k / 8;
     uint32_t threads = units < 1024 ? ((units + 31) / 32) * 32 : 1024;
     const uint32_t upt = (units + threads - 1) / threads;
     dim3 grid(a.rows), block(threads);
-    if (upt <= 1)
-        act_quant_row_kernel<kSilu, 1><<<grid, block, 0, s>>>(a);
-    else if (upt <= 2)
-        act_quant_row_kernel<kSilu, 2><<<grid, block, 0, s>>>(a);
-    else if (upt <= 4)
-        act_quant_row_kernel<kSilu, 4><<<grid, block, 0, s>>>(a);
-    else
-        act_quant_row_kernel<kSilu, 8><<<grid, block, 0, s>>>(a);
-    return cudaGetLastError();
+    if (upt <= 1) return launch_pdl(act_quant_row_kernel<kSilu, 1>, grid, block, s, a);
+    if (upt <= 2) return launch_pdl(act_quant_row_kernel<kSilu, 2>, grid, block, s, a);
+    if (upt <= 4) return launch_pdl(act_quant_row_kernel<kSilu, 4>, grid, block, s, a);
+    return launch_pdl(act_quant_row_kernel<kSilu, 8>, grid, block, s, a);
 }
 
 template <bool kSilu>
 cudaError_t launch_g128(const ActQuantArgs &a, cudaStream_t s) {
     const uint32_t groups = a.rows * (a.k / kKUnit);
-    act_quant_g128_kernel<kSilu><<<(groups + 7) / 8, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(act_quant_g128_kernel<kSilu>, dim3((groups + 7) / 8), dim3(256), s, a);
 }
 
 }  // namespace

@@ -89,7 +89,7 @@ qdl_status check_weight(const char *who, const qdl_w8a8_weight *w) {
 
 qdl_status launch_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *q_scale, uint32_t rows, void *out,
                        int32_t out_dtype, uint32_t ldc, cudaStream_t stream, uint32_t debug_skip_iter = ~0u,
-                       uint64_t wait_limit_ns = kWaitLimitNs) {
+                       uint64_t wait_limit_ns = kWaitLimitNs, const void *fused_x = nullptr, uint32_t fused_ldx = 0) {
     const size_t spr = scales_per_row(w->format, w->k);
     const size_t elt = out_dtype == QDL_OUT_BF16 ? 2 : 4;
     W8A8Args a = {};
@@ -118,6 +118,15 @@ qdl_status launch_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *
         a.sa = q_scale;
         a.out = out;
         a.m = rows;
+        if (fused_x != nullptr) {  // Block128, rows <= 16: quantise inside the GEMV
+            a.x = fused_x;
+            a.ldx = fused_ldx;
+            a.q_out = const_cast<uint8_t *>(q);
+            a.sa_out = const_cast<float *>(q_scale);
+            cudaError_t e = launch_w8a8_proj_fused(a, seg_w, seg_n, stream);
+            if (e != cudaSuccess) return cuda_fail("qdl_w8a8_proj", e);
+            return ok();
+        }
         cudaError_t e = launch_w8a8_gemm_tc(a, w->format, seg_w, seg_n, stream);
         if (e != cudaSuccess) return cuda_fail("qdl_w8a8_gemv", e);
         return ok();
@@ -274,6 +283,11 @@ qdl_status qdl_w8a8_proj(const qdl_w8a8_weight *w, const void *x, uint32_t ldx, 
     qdl_status st = check_gemv(who, w, q, q_scale, q_bytes, scale_bytes, rows, out, out_dtype, ldc);
     if (st != QDL_OK) return st;
     if ((st = check_input(who, "x", x, ldx, w->k)) != QDL_OK) return st;
+    if (QDL_TUNE_FUSED && w->format == QDL_SCALE_BLOCK128 && rows <= 16 && kMmaMaxRows == 0) {
+        // one launch: the GEMV quantises its own activation blocks
+        return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, static_cast<cudaStream_t>(stream), ~0u,
+                           kWaitLimitNs, x, ldx);
+    }
     ActQuantArgs a = {static_cast<const uint16_t *>(x), nullptr, ldx, 0, rows, w->k, q, q_scale};
     cudaError_t e = launch_act_quant(a, w->format, false, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(who, e);
@@ -402,6 +416,31 @@ qdl_status qdl_w8a8_proj_static(const qdl_w8a8_weight *w, const void *x, uint32_
     cudaError_t e = launch_act_quant(a, w->format, false, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(who, e);
     return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, static_cast<cudaStream_t>(stream));
+}
+
+qdl_status qdl_w8a8_plan(const qdl_w8a8_weight *w, uint32_t rows, qdl_plan *plan) {
+    const char *who = "w8a8_plan";
+    qdl_status st = check_weight(who, w);
+    if (st != QDL_OK) return st;
+    if (plan == nullptr) return fail(QDL_ERR_INVALID_ARG, "%s: plan is NULL", who);
+    if (rows < 1 || rows > (uint32_t)kMaxRows) return fail(QDL_ERR_INVALID_ARG, "%s: %u rows, want 1..=%d", who, rows, kMaxRows);
+    W8A8Args a = {};
+    a.n = w->n;
+    a.k = w->k;
+    a.kb = w->k / kKUnit;
+    a.m = rows;
+    PlanInfo p = {};
+    cudaError_t e = rows > kMmaMaxRows ? plan_w8a8_gemm_tc(a, w->format, &p) : plan_w8a8_gemv_tma(a, w->format, &p);
+    if (e != cudaSuccess) return cuda_fail(who, e);
+    plan->kernel = p.kernel;
+    plan->mma_n = p.mma_n;
+    plan->tiles = p.tiles;
+    plan->split_k = p.split;
+    plan->stages = p.stages;
+    plan->threads = p.threads;
+    plan->smem_bytes = p.smem;
+    plan->resident_clusters = p.clusters;
+    return ok();
 }
 
 qdl_status qdl_check_device_fault(void *stream) {

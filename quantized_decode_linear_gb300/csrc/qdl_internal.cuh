@@ -9,6 +9,13 @@
 
 namespace qdl {
 
+#ifndef QDL_TUNE_FUSED
+#define QDL_TUNE_FUSED 0  // quantise Block128 activations inside the GEMV (rows <= 16)
+#endif
+#ifndef QDL_TUNE_PDL
+#define QDL_TUNE_PDL 1  // programmatic dependent launch between the library's kernels
+#endif
+
 constexpr int kMaxRows = QDL_MAX_ROWS;
 constexpr int kKUnit = QDL_K_UNIT;
 
@@ -37,6 +44,11 @@ struct W8A8Args {
     uint32_t kb;        // k / 128
     uint32_t debug_skip_iter;  // self-test only: pipeline stage never loaded (else ~0u)
     uint64_t wait_limit_ns;    // limit of every device-side wait
+    // fused projection only: bf16 input [m, ldx] and the scratch it fills
+    const void *x;
+    uint32_t ldx;
+    uint8_t *q_out;
+    float *sa_out;
 };
 
 struct Int4Args {
@@ -55,6 +67,14 @@ struct Int4Args {
 // Each returns cudaSuccess or the launch error.  Arguments are validated by
 // the C-ABI layer before these are called.
 
+struct PlanInfo {
+    int kernel;
+    uint32_t mma_n, tiles, split, stages, threads, smem;
+    int clusters;
+};
+cudaError_t plan_w8a8_gemm_tc(const W8A8Args &a, int format, PlanInfo *p);
+cudaError_t plan_w8a8_gemv_tma(const W8A8Args &a, int format, PlanInfo *p);
+
 cudaError_t launch_act_quant(const ActQuantArgs &a, int format, bool silu, cudaStream_t s);
 cudaError_t launch_w8a8_gemv_tma(const W8A8Args &a, int format, const uint8_t *const seg_w[3],
                                  const uint32_t seg_n[3], cudaStream_t s);
@@ -63,6 +83,8 @@ cudaError_t launch_w8a8_gemm_tc(const W8A8Args &a, int format, const uint8_t *co
                                 const uint32_t seg_n[3], cudaStream_t s);
 cudaError_t read_and_clear_tc_fault(uint32_t *value);
 uint32_t tc_bucket(uint32_t m);  // MMA N of the tensor-core kernel for m token rows
+cudaError_t launch_w8a8_proj_fused(const W8A8Args &a, const uint8_t *const seg_w[3], const uint32_t seg_n[3],
+                                   cudaStream_t s);
 uint32_t choose_split_k(uint32_t tiles, uint32_t kb, uint32_t slots);
 cudaError_t launch_int4_qkv(const Int4Args &a, cudaStream_t s);
 

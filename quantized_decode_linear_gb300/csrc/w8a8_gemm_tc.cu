@@ -1,27 +1,39 @@
 // W8A8 decode GEMV / skinny GEMM on the 5th-generation tensor cores
-// (w8a8_decode.rs fn w8a8_gemv; segment routing from W8a8Weight::boundaries;
-// scale layouts from enum W8a8Scale).  One pass over the weights for any
-// token count up to 256.
+// (w8a8_decode.rs fn w8a8_gemv and fn w8a8_proj; segment routing from
+// W8a8Weight::boundaries; scale layouts from enum W8a8Scale).  One pass over
+// the weights for any token count up to 256.
 //
 //   y[m, j] = sum_kb Sa(m, kb) Sw(j, kb) sum_{k in kb} dec(q[m,k]) dec(W[j,k])
 //
 // Roles (one CTA = 128 output rows x a range of 128-wide K blocks):
-//   warp 0, one lane : TMA producer.  Per K block, eight 16-row x 128-byte
-//                      weight boxes (from the segment holding those rows) and
-//                      one NTOK-row activation box land in a shared-memory
-//                      stage (128-byte swizzle = the canonical K-major SW128
-//                      operand layout), completing on the stage's mbarrier.
+//   warp 0, one lane : TMA producer.  Per K block, the 128 x 128-byte weight
+//                      tile (one box, or eight 16-row boxes when the tile
+//                      spans two segments) and, unless fused, the NTOK-row
+//                      activation box land in a shared-memory stage (128-byte
+//                      swizzle = the canonical K-major SW128 operand layout).
 //   warp 1           : allocates the tensor memory; one lane issues
 //                      tcgen05.mma kind::f8f6f4 (M = 128 weight rows,
 //                      N = NTOK tokens, K = 32 per instruction, four per
 //                      block) and commits each stage back to its `empty`
 //                      mbarrier.
-//   warps 2..        : epilogue, reading the f32 accumulators with tcgen05.ld.
+//   warp 2 (fused)   : quantises the bf16 activations of each K block
+//                      (absmax/448 per token and 128-group, RNE satfinite E4M3,
+//                      the arithmetic of the act-quant kernel) straight into
+//                      the stage's swizzled operand and the block's scales into
+//                      shared memory; the CTAs of tile 0 also write the codes
+//                      and scales to the caller's scratch.
+//   other warps      : epilogue, reading the f32 accumulators with tcgen05.ld.
 //
 // Scales.  PerRow: the accumulator sums the CTA's whole K range; the epilogue
 // multiplies by sa[m] sw[j].  Block128: each 128-block accumulates into one of
-// two TMEM buffers (ping-pong); the epilogue folds buffer b into register
-// totals with sa[m, kb] sw[j/128, kb] while the tensor core fills the other.
+// 2-4 TMEM buffers in turn; the epilogue folds a finished buffer into
+// register totals with sa[m, kb] sw[j/128, kb] while the tensor core fills
+// the next ones.
+//
+// Launch overlap.  Kernels are launched with programmatic stream
+// serialisation: the weight stream (independent of earlier kernels) starts at
+// once; every read of activations or scales and every output write comes
+// after griddepcontrol.wait.
 //
 // Split-K CTAs of one cluster reduce their partials through distributed shared
 // memory in rank order (deterministic).  Every wait is bounded; after a
@@ -37,6 +49,13 @@
 
 namespace cg = cooperative_groups;
 
+#ifndef QDL_TC_STAGE_BYTES
+#define QDL_TC_STAGE_BYTES (64 * 1024)
+#endif
+#ifndef QDL_TC_BIGBOX
+#define QDL_TC_BIGBOX 1
+#endif
+
 namespace qdl {
 
 static __device__ uint32_t g_tc_fault;
@@ -46,12 +65,6 @@ namespace {
 constexpr int kTileRows = 128;
 constexpr uint32_t kWBytes = kTileRows * 128;  // weight tile per stage
 constexpr uint32_t kWBox = 16 * 128;
-#ifndef QDL_TC_STAGE_BYTES
-#define QDL_TC_STAGE_BYTES (64 * 1024)
-#endif
-#ifndef QDL_TC_BIGBOX
-#define QDL_TC_BIGBOX 1
-#endif
 
 constexpr uint32_t pow2_at_least(uint32_t v) {
     uint32_t p = 32;
@@ -59,25 +72,32 @@ constexpr uint32_t pow2_at_least(uint32_t v) {
     return p;
 }
 
-template <int NTOK, bool kBlock>
+template <int NTOK, bool kBlock, bool kFused>
 struct Tc {
     static constexpr uint32_t kABytes = NTOK * 128;
     static constexpr uint32_t kStage = kWBytes + kABytes;  // multiple of 1024 (NTOK % 8 == 0)
     // pipeline depth: as many stages as fit a per-CTA budget, at least 3
     static constexpr int kStages = (QDL_TC_STAGE_BYTES / kStage) < 3 ? 3 : (QDL_TC_STAGE_BYTES / kStage);
+    // Block128 accumulator buffers: the MMA may run kAcc-1 blocks ahead of
+    // the epilogue that folds each block's scales
+    static constexpr int kAcc = kBlock ? (NTOK <= 64 ? 4 : 2) : 1;
     static constexpr uint32_t kBarOff = kStages * kStage;
-    static constexpr uint32_t kBytes = kBarOff + 256;
+    static constexpr uint32_t kScaleOff = kBarOff + 512;  // fused: [kAcc][NTOK] block scales
+    static constexpr uint32_t kBytes = kScaleOff + (kFused ? kAcc * NTOK * 4 : 0);
     static constexpr uint32_t kAlloc = kBytes + 1024;
+    static constexpr int kEpiBase = kFused ? 3 : 2;                          // first epilogue warp
     static constexpr int kEpi = kBlock ? (NTOK <= 64 ? 4 : NTOK / 16) : 4;  // epilogue warps
     static constexpr int kCpt = kBlock ? NTOK * 4 / kEpi : 16;               // columns per epilogue thread
-    static constexpr int kThreads = (2 + kEpi) * 32;
-    static constexpr uint32_t kTmemCols = pow2_at_least(kBlock ? 2 * NTOK : NTOK);
+    static constexpr int kThreads = (kEpiBase + kEpi) * 32;
+    static constexpr uint32_t kTmemCols = pow2_at_least(kAcc * NTOK);
     static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
     static_assert(kTileRows * NTOK * 4 <= kBarOff, "reduction buffer must fit in the stage area");
     static_assert(kTmemCols <= 512, "tensor memory");
+    static_assert((3 * kStages + 3 * kAcc + 1) * 8 + 8 <= 512, "barrier area");
+    static_assert(!kFused || (kBlock && NTOK == 16), "fused quantisation: Block128, up to 16 rows");
 };
 
-// ---------------------------------------------------------------- tcgen05 PTX
+// ---------------------------------------------------------------- tcgen05 / PDL PTX
 
 // Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle
 // layout (8-row x 128-byte atoms stacked at 1024-byte stride).
@@ -129,25 +149,44 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// generic-proxy shared-memory writes -> visible to the tensor core (async proxy)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void sts64(uint32_t addr, uint32_t lo, uint32_t hi) {
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(lo), "r"(hi) : "memory");
+}
+
+__device__ __forceinline__ float quant_operand(float v, float scale) {
+    return scale == 0.0f ? v : __fdiv_rn(v, scale);
+}
+
 // ---------------------------------------------------------------- kernel
 
-template <int NTOK, bool kBlock>
-__global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1)
+template <int NTOK, bool kBlock, bool kFused>
+__global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1)
     w8a8_gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                         const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_b0,
                         const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_b2,
                         const __grid_constant__ CUtensorMap tm_a, const W8A8Args a) {
-    using C = Tc<NTOK, kBlock>;
+    using C = Tc<NTOK, kBlock, kFused>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
     uint64_t *empty = full + C::kStages;
-    uint64_t *accf = empty + C::kStages;  // [2] accumulator buffer ready
-    uint64_t *acce = accf + 2;           // [2] accumulator buffer drained
-    uint64_t *done = acce + 2;           // all MMAs complete
+    uint64_t *qfull = empty + C::kStages;  // fused: activation operand written
+    uint64_t *accf = qfull + C::kStages;   // [kAcc] accumulator buffer ready
+    uint64_t *acce = accf + C::kAcc;      // [kAcc] accumulator buffer drained
+    uint64_t *scal = acce + C::kAcc;      // [kAcc] fused: block scales written
+    uint64_t *done = scal + C::kAcc;      // all MMAs complete
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     volatile uint32_t *abort_flag = tmem_slot + 1;
-    float *red = reinterpret_cast<float *>(smem);  // [NTOK][128], reuses the stages at the end
+    float *sbuf = reinterpret_cast<float *>(smem + C::kScaleOff);  // fused: [kAcc][NTOK]
+    float *red = reinterpret_cast<float *>(smem);                   // [NTOK][128], reuses the stages at the end
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t tile_row0 = blockIdx.x * kTileRows;
@@ -159,10 +198,12 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&qfull[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < C::kAcc; ++b) {
             mbar_init(&accf[b], 1);
             mbar_init(&acce[b], C::kEpi);
+            mbar_init(&scal[b], 1);
         }
         mbar_init(done, 1);
         *abort_flag = 0;
@@ -198,7 +239,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1)
     } else {
         tile_scale = a.sw2; tile_lrow0 = tile_row0 - a.n2; tile_big = &tm_b2; seg_end = a.n;
     }
-    // true when rows tile_row0 .. tile_row0+127 that exist all belong to that segment
+    // true when the rows tile_row0 .. tile_row0+127 that exist all belong to that segment
     const bool tile_single = tile_row0 + kTileRows <= seg_end || seg_end == a.n;
 
     uint32_t issued = 0;
@@ -211,38 +252,56 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1)
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             prefetch_tmap(tile_big);
-            prefetch_tmap(&tm_a);
+            if (!kFused) prefetch_tmap(&tm_a);
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_a = policy_evict_last();
-            for (uint32_t it = 0; it < niter; ++it) {
+            auto load_weights = [&](uint32_t it, uint8_t *st, uint64_t *bar) {
+                const int32_t kk = (int32_t)((kb0 + it) * 128);
+                if (QDL_TC_BIGBOX && tile_single) {  // the whole tile lies in one segment: one box
+                    tma_load_2d(st, tile_big, kk, (int32_t)tile_lrow0, bar, pol_w);
+                    return;
+                }
+#pragma unroll 1
+                for (int b = 0; b < kTileRows / 16; ++b) {
+                    const uint32_t r0 = tile_row0 + 16 * b;
+                    const CUtensorMap *m;
+                    uint32_t lr;
+                    if (r0 < a.n1) {
+                        m = &tm_w0; lr = r0;
+                    } else if (r0 < a.n2) {
+                        m = &tm_w1; lr = r0 - a.n1;
+                    } else {
+                        m = &tm_w2; lr = r0 - a.n2;
+                    }
+                    tma_load_2d(st + b * kWBox, m, kk, (int32_t)lr, bar, pol_w);
+                }
+            };
+            constexpr uint32_t kTx = kFused ? kWBytes : C::kStage;
+            // weights of the first stages before waiting for the previous kernel
+            const uint32_t head = niter < (uint32_t)C::kStages ? niter : (uint32_t)C::kStages;
+            for (uint32_t it = 0; it < head; ++it) {
+                mbar_arrive_expect_tx(&full[it], kTx);
+                issued = it + 1;
+                if (it == a.debug_skip_iter) continue;  // self-test: this stage never lands
+                load_weights(it, smem + it * C::kStage, &full[it]);
+            }
+            if (!kFused) {
+                grid_dep_wait();  // activations are written by the previous kernel
+                for (uint32_t it = 0; it < head; ++it)
+                    if (it != a.debug_skip_iter)
+                        tma_load_2d(smem + it * C::kStage + kWBytes, &tm_a, (int32_t)((kb0 + it) * 128), 0, &full[it],
+                                    pol_a);
+            }
+            for (uint32_t it = head; it < niter; ++it) {
                 const uint32_t slot = it % C::kStages, ph = (it / C::kStages) & 1;
                 wait(&empty[slot], ph ^ 1, 1);
                 if (*abort_flag) break;
-                mbar_arrive_expect_tx(&full[slot], C::kStage);
+                mbar_arrive_expect_tx(&full[slot], kTx);
                 issued = it + 1;
-                if (it == a.debug_skip_iter) continue;  // self-test: this stage never lands
+                if (it == a.debug_skip_iter) continue;
                 uint8_t *st = smem + slot * C::kStage;
-                const int32_t kk = (int32_t)((kb0 + it) * 128);
-                if (QDL_TC_BIGBOX && tile_single) {
-                    // the whole tile lies in one segment: one 128-row box
-                    tma_load_2d(st, tile_big, kk, (int32_t)tile_lrow0, &full[slot], pol_w);
-                } else {
-#pragma unroll 1
-                    for (int b = 0; b < kTileRows / 16; ++b) {
-                        const uint32_t r0 = tile_row0 + 16 * b;
-                        const CUtensorMap *m;
-                        uint32_t lr;
-                        if (r0 < a.n1) {
-                            m = &tm_w0; lr = r0;
-                        } else if (r0 < a.n2) {
-                            m = &tm_w1; lr = r0 - a.n1;
-                        } else {
-                            m = &tm_w2; lr = r0 - a.n2;
-                        }
-                        tma_load_2d(st + b * kWBox, m, kk, (int32_t)lr, &full[slot], pol_w);
-                    }
-                }
-                tma_load_2d(st + kWBytes, &tm_a, kk, 0, &full[slot], pol_a);
+                load_weights(it, st, &full[slot]);
+                if (!kFused) tma_load_2d(st + kWBytes, &tm_a, (int32_t)((kb0 + it) * 128), 0, &full[slot], pol_a);
             }
         }
     } else if (warp == 1) {
@@ -252,9 +311,10 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1)
             const uint32_t sbase = smem_u32(smem);
             for (uint32_t it = 0; it < niter; ++it) {
                 const uint32_t slot = it % C::kStages, ph = (it / C::kStages) & 1;
-                const uint32_t b = kBlock ? (it & 1) : 0;
-                if (kBlock) wait(&acce[b], ((it >> 1) & 1) ^ 1, 4);
+                const uint32_t b = kBlock ? it % C::kAcc : 0;
+                if (kBlock) wait(&acce[b], ((it / C::kAcc) & 1) ^ 1, 4);
                 wait(&full[slot], ph, 8);
+                if (kFused) wait(&qfull[slot], ph, 8);
                 if (*abort_flag) break;
                 tc_fence_after();
                 const uint64_t ad = sw128_desc(sbase + slot * C::kStage);
@@ -268,28 +328,89 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1)
             }
             tc_commit(done);  // completes once every MMA issued above has
         }
+    } else if (kFused && warp == 2) {
+        // ------------------------------------------------------------ quantiser
+        // 16 lanes per token row: lane h = lane & 15 holds elements 8h .. 8h+7
+        // of the row's 128-group; two rows per pass.
+        grid_dep_wait();
+        const int h = lane & 15, half = lane >> 4;
+        const uint32_t sbase = smem_u32(smem);
+        const uint16_t *x = reinterpret_cast<const uint16_t *>(a.x);
+        for (uint32_t it = 0; it < niter; ++it) {
+            const uint32_t slot = it % C::kStages, ph = (it / C::kStages) & 1;
+            const uint32_t b = it % C::kAcc, kb = kb0 + it;
+            // load this block of x for every row first (independent loads)
+            uint4 raw[NTOK / 2];
+#pragma unroll
+            for (int p = 0; p < NTOK / 2; ++p) {
+                const uint32_t r = 2 * p + half;
+                raw[p] = r < a.m ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)r * a.ldx + kb * 128 + 8 * h))
+                                 : make_uint4(0, 0, 0, 0);
+            }
+            wait(&empty[slot], ph ^ 1, 64);                // operand slot free
+            wait(&acce[b], ((it / C::kAcc) & 1) ^ 1, 64);  // scale buffer free
+#pragma unroll
+            for (int p = 0; p < NTOK / 2; ++p) {
+                const uint32_t r = 2 * p + half;
+                const uint32_t w[4] = {raw[p].x, raw[p].y, raw[p].z, raw[p].w};
+                float v[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    v[2 * j] = bf16_bits_to_f32(w[j] & 0xFFFFu);
+                    v[2 * j + 1] = bf16_bits_to_f32(w[j] >> 16);
+                }
+                float amax = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+                const float scale = __fdiv_rn(amax, 448.0f);
+                uint32_t c[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    c[j] = cvt_e4m3x2(quant_operand(v[2 * j], scale), quant_operand(v[2 * j + 1], scale));
+                const uint32_t lo = c[0] | (c[1] << 16), hi = c[2] | (c[3] << 16);
+                // row r, bytes 8h..8h+7: 16-byte chunk h>>1 (swizzled by r & 7), half h&1
+                const uint32_t addr = sbase + slot * C::kStage + kWBytes + r * 128 +
+                                      ((((uint32_t)h >> 1) ^ (r & 7)) << 4) + ((uint32_t)h & 1) * 8;
+                sts64(addr, lo, hi);
+                if (h == 0) sbuf[b * NTOK + r] = r < a.m ? scale : 0.0f;
+                if (blockIdx.x == 0 && r < a.m) {  // tile-0 CTAs also fill the caller's scratch
+                    *reinterpret_cast<uint2 *>(a.q_out + (size_t)r * a.k + kb * 128 + 8 * h) = make_uint2(lo, hi);
+                    if (h == 0) a.sa_out[(size_t)r * a.kb + kb] = scale;
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&qfull[slot]);
+                mbar_arrive(&scal[b]);
+            }
+        }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int e = warp - 2;
-        const int quad = warp & 3;                // TMEM lanes 32*quad .. 32*quad+31
-        const int cgrp = e >> 2;                  // column group
-        const uint32_t lrow = 32 * quad + lane;   // row within the tile
-        const uint32_t row = tile_row0 + lrow;
+        const int e = warp - C::kEpiBase;
+        const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+        const int cgrp = e >> 2;    // column group
         const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16);
+        if (!kFused) grid_dep_wait();  // activation scales come from the previous kernel
         if constexpr (kBlock) {
             constexpr int kSRegs = (kCpt + 31) / 32;  // scale registers per lane
             for (uint32_t it = 0; it < niter; ++it) {
-                const uint32_t b = it & 1, kb = kb0 + it;
+                const uint32_t b = it % C::kAcc, kb = kb0 + it;
                 // lane l holds sa[token cgrp*kCpt + 32r + l, kb] * sw; shuffled out below
                 const float sw = tile_row0 < a.n ? __ldg(tile_scale + (size_t)(tile_lrow0 >> 7) * a.kb + kb) : 0.0f;
                 float sreg[kSRegs];
+                if (kFused) wait(&scal[b], (it / C::kAcc) & 1, 32);
 #pragma unroll
                 for (int r = 0; r < kSRegs; ++r) {
                     const uint32_t tok = cgrp * kCpt + 32 * r + lane;
-                    sreg[r] = (32 * r + lane < (uint32_t)kCpt && tok < a.m) ? __ldg(a.sa + (size_t)tok * a.kb + kb) * sw
-                                                                            : 0.0f;
+                    float sa = 0.0f;
+                    if (32 * r + lane < (uint32_t)kCpt && tok < a.m)
+                        sa = kFused ? sbuf[b * NTOK + tok] : __ldg(a.sa + (size_t)tok * a.kb + kb);
+                    sreg[r] = sa * sw;
                 }
-                wait(&accf[b], (it >> 1) & 1, 16);
+                wait(&accf[b], (it / C::kAcc) & 1, 16);
                 tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < kCpt / 16; ++c) {
@@ -315,15 +436,18 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1)
 
     // ---------------------------------------------------------------- drain after a timeout
     __syncthreads();
+    grid_dep_launch();  // the next kernel may start streaming its weights
     if (*abort_flag) {
         if (warp == 0 && lane == 0) {
             const uint32_t first = issued > (uint32_t)C::kStages ? issued - C::kStages : 0;
             for (uint32_t it = first; it < issued; ++it)
-                if (it != a.debug_skip_iter) mbar_wait(&full[it % C::kStages], (it / C::kStages) & 1, a.wait_limit_ns);
+                if (it != a.debug_skip_iter)
+                    mbar_wait(&full[it % C::kStages], (it / C::kStages) & 1, a.wait_limit_ns);
         }
         if (warp == 1 && lane == 0) mbar_wait(done, 0, a.wait_limit_ns);
         __syncthreads();
     }
+    grid_dep_wait();  // outputs may be read or written by earlier kernels
 
     auto store = [&](uint32_t tok, uint32_t r, float v) {
         if (tok < a.m && r < a.n) {
@@ -337,8 +461,8 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1)
     // ---------------------------------------------------------------- output
     // Each epilogue thread owns one row and a range of token columns; with
     // split > 1 it writes them to red[token][row] for the cluster reduction.
-    if (warp >= 2) {
-        const int e = warp - 2;
+    if (warp >= C::kEpiBase) {
+        const int e = warp - C::kEpiBase;
         const int quad = warp & 3;
         const int cgrp = e >> 2;
         const uint32_t lrow = 32 * quad + lane;
@@ -418,56 +542,93 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-template <int NTOK, bool kBlock>
-int occupancy_tc() {
-    using C = Tc<NTOK, kBlock>;
+template <int NTOK, bool kBlock, bool kFused>
+uint32_t cta_slots_tc() {
+    using C = Tc<NTOK, kBlock, kFused>;
     static std::mutex mu;
-    static std::vector<int> cache;
+    static std::vector<uint32_t> cache;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    cudaGetDevice(&dev);
     std::lock_guard<std::mutex> lock(mu);
     if ((int)cache.size() <= dev) cache.resize(dev + 1, 0);
     if (cache[dev] == 0) {
-        cudaFuncSetAttribute(w8a8_gemm_tc_kernel<NTOK, kBlock>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(w8a8_gemm_tc_kernel<NTOK, kBlock, kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::kAlloc);
-        cache[dev] = resident_ctas((const void *)w8a8_gemm_tc_kernel<NTOK, kBlock>, C::kThreads, C::kAlloc,
-                                   C::kTmemCols);
+        cache[dev] = (uint32_t)(device_sm_count() *
+                                resident_ctas((const void *)w8a8_gemm_tc_kernel<NTOK, kBlock, kFused>, C::kThreads,
+                                              C::kAlloc, C::kTmemCols));
     }
     return cache[dev];
 }
 
-template <int NTOK, bool kBlock>
+template <int NTOK, bool kBlock, bool kFused>
 cudaError_t launch_tc_variant(const W8A8Args &a, const CUtensorMap (&maps)[7], cudaStream_t s) {
-    using C = Tc<NTOK, kBlock>;
+    using C = Tc<NTOK, kBlock, kFused>;
     const uint32_t tiles = (a.n + kTileRows - 1) / kTileRows;
-    const uint32_t slots = (uint32_t)(device_sm_count() * occupancy_tc<NTOK, kBlock>());
-    const uint32_t split = choose_split_k(tiles, a.kb, slots);
-    (void)sizeof(C);
+    const uint32_t split = choose_split_k(tiles, a.kb, cta_slots_tc<NTOK, kBlock, kFused>());
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tiles, split, 1);
     cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kAlloc;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = split;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, w8a8_gemm_tc_kernel<NTOK, kBlock>, maps[0], maps[1], maps[2], maps[3], maps[4],
-                              maps[5], maps[6], a);
+    cfg.numAttrs = QDL_TUNE_PDL ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, w8a8_gemm_tc_kernel<NTOK, kBlock, kFused>, maps[0], maps[1], maps[2], maps[3],
+                              maps[4], maps[5], maps[6], a);
+}
+
+template <int NTOK, bool kBlock, bool kFused>
+void plan_tc_variant(const W8A8Args &a, PlanInfo *p) {
+    using C = Tc<NTOK, kBlock, kFused>;
+    const uint32_t slots = cta_slots_tc<NTOK, kBlock, kFused>();
+    p->kernel = 0;
+    p->mma_n = NTOK;
+    p->tiles = (a.n + kTileRows - 1) / kTileRows;
+    p->split = choose_split_k(p->tiles, a.kb, slots);
+    p->stages = C::kStages;
+    p->threads = C::kThreads;
+    p->smem = C::kAlloc;
+    p->clusters = (int)(slots / p->split);
+}
+
+template <bool kBlock>
+void plan_tc_rows(const W8A8Args &a, uint32_t ntok, PlanInfo *p) {
+    switch (ntok) {
+        case 16: return plan_tc_variant<16, kBlock, false>(a, p);
+        case 32: return plan_tc_variant<32, kBlock, false>(a, p);
+        case 64: return plan_tc_variant<64, kBlock, false>(a, p);
+        case 128: return plan_tc_variant<128, kBlock, false>(a, p);
+        default: return plan_tc_variant<256, kBlock, false>(a, p);
+    }
 }
 
 template <bool kBlock>
 cudaError_t launch_tc_rows(const W8A8Args &a, const CUtensorMap (&maps)[7], uint32_t ntok, cudaStream_t s) {
     switch (ntok) {
-        case 16: return launch_tc_variant<16, kBlock>(a, maps, s);
-        case 32: return launch_tc_variant<32, kBlock>(a, maps, s);
-        case 64: return launch_tc_variant<64, kBlock>(a, maps, s);
-        case 128: return launch_tc_variant<128, kBlock>(a, maps, s);
-        default: return launch_tc_variant<256, kBlock>(a, maps, s);
+        case 16: return launch_tc_variant<16, kBlock, false>(a, maps, s);
+        case 32: return launch_tc_variant<32, kBlock, false>(a, maps, s);
+        case 64: return launch_tc_variant<64, kBlock, false>(a, maps, s);
+        case 128: return launch_tc_variant<128, kBlock, false>(a, maps, s);
+        default: return launch_tc_variant<256, kBlock, false>(a, maps, s);
     }
+}
+
+cudaError_t weight_maps(const W8A8Args &a, const uint8_t *const seg_w[3], const uint32_t seg_n[3],
+                        CUtensorMap (&maps)[7]) {
+    for (int i = 0; i < 3; ++i) {  // 16-row boxes x3, 128-row boxes x3
+        cudaError_t e = make_tmap_u8(&maps[i], seg_w[i], a.k, seg_n[i], a.k, 128, 16);
+        if (e != cudaSuccess) return e;
+        e = make_tmap_u8(&maps[3 + i], seg_w[i], a.k, seg_n[i], a.k, 128, kTileRows);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -482,16 +643,32 @@ uint32_t tc_bucket(uint32_t m) {
 cudaError_t launch_w8a8_gemm_tc(const W8A8Args &a, int format, const uint8_t *const seg_w[3], const uint32_t seg_n[3],
                                 cudaStream_t s) {
     CUtensorMap maps[7];  // 16-row boxes x3, 128-row boxes x3, activations
-    for (int i = 0; i < 3; ++i) {
-        cudaError_t e = make_tmap_u8(&maps[i], seg_w[i], a.k, seg_n[i], a.k, 128, 16);
-        if (e != cudaSuccess) return e;
-        e = make_tmap_u8(&maps[3 + i], seg_w[i], a.k, seg_n[i], a.k, 128, kTileRows);
-        if (e != cudaSuccess) return e;
-    }
+    cudaError_t e = weight_maps(a, seg_w, seg_n, maps);
+    if (e != cudaSuccess) return e;
     const uint32_t ntok = tc_bucket(a.m);
-    cudaError_t e = make_tmap_u8(&maps[6], a.q, a.k, a.m, a.k, 128, ntok);
+    e = make_tmap_u8(&maps[6], a.q, a.k, a.m, a.k, 128, ntok);
     if (e != cudaSuccess) return e;
     return format == QDL_SCALE_BLOCK128 ? launch_tc_rows<true>(a, maps, ntok, s) : launch_tc_rows<false>(a, maps, ntok, s);
+}
+
+// Block128 projection with the activation quantisation fused in (rows <= 16):
+// a.x is the bf16 input, a.q / a.sa the caller's scratch that tile-0 CTAs fill.
+cudaError_t launch_w8a8_proj_fused(const W8A8Args &a, const uint8_t *const seg_w[3], const uint32_t seg_n[3],
+                                   cudaStream_t s) {
+    CUtensorMap maps[7];
+    cudaError_t e = weight_maps(a, seg_w, seg_n, maps);
+    if (e != cudaSuccess) return e;
+    maps[6] = maps[0];  // unused: activations are quantised in the kernel
+    return launch_tc_variant<16, true, true>(a, maps, s);
+}
+
+cudaError_t plan_w8a8_gemm_tc(const W8A8Args &a, int format, PlanInfo *p) {
+    const uint32_t ntok = tc_bucket(a.m);
+    if (format == QDL_SCALE_BLOCK128)
+        plan_tc_rows<true>(a, ntok, p);
+    else
+        plan_tc_rows<false>(a, ntok, p);
+    return cudaGetLastError();
 }
 
 cudaError_t read_and_clear_tc_fault(uint32_t *value) {

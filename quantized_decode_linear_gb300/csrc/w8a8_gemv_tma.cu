@@ -313,36 +313,41 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 template <int NT, bool kBlock>
-int occupancy() {
+uint32_t cta_slots() {
     static std::mutex mu;
-    static std::vector<int> cache;
+    static std::vector<uint32_t> cache;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    cudaGetDevice(&dev);
     std::lock_guard<std::mutex> lock(mu);
     if ((int)cache.size() <= dev) cache.resize(dev + 1, 0);
     if (cache[dev] == 0) {
         cudaFuncSetAttribute(w8a8_gemv_tma_kernel<NT, kBlock>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)Layout<NT>::kAlloc);
-        cache[dev] = resident_ctas((const void *)w8a8_gemv_tma_kernel<NT, kBlock>, kThreads, Layout<NT>::kAlloc, 0);
+        cache[dev] = (uint32_t)(device_sm_count() *
+                                resident_ctas((const void *)w8a8_gemv_tma_kernel<NT, kBlock>, kThreads,
+                                              Layout<NT>::kAlloc, 0));
     }
     return cache[dev];
 }
 
 }  // namespace
 
-// Split of K over a cluster of CTAs.  Work is in 128-blocks; a CTA of a split
-// s takes ceil(kb/s) of them.  Choose s in 1..8 that minimises the slowest
-// SM's work, waves x ceil(kb/s), with `slots` co-resident CTAs.
+// Split of K over a cluster of CTAs.  Work is in 128-blocks; a CTA of split s
+// takes up to ceil(kb/s) of them plus about two blocks' worth of pipeline
+// fill and drain.  `slots` CTAs are resident at once (all SMs).  Choose s in
+// 1..8 that minimises waves x per-CTA work, with a small charge for the
+// cluster reduction.
 uint32_t choose_split_k(uint32_t tiles, uint32_t kb, uint32_t slots) {
 #ifdef QDL_TUNE_SPLIT
     if (QDL_TUNE_SPLIT > 0) return QDL_TUNE_SPLIT < kb ? QDL_TUNE_SPLIT : kb;
 #endif
     uint32_t best = 1;
     double best_cost = 1e300;
+    if (slots < 1) slots = 1;
     for (uint32_t s = 1; s <= 8 && s <= kb; ++s) {
         const uint32_t units = tiles * s;
         const uint32_t waves = (units + slots - 1) / slots;
-        const double cost = (double)waves * ((kb + s - 1) / s) * (1.0 + 0.03 * (s - 1));
+        const double cost = (double)waves * (((kb + s - 1) / s) + 2.0) * (1.0 + 0.03 * (s - 1));
         if (cost < best_cost) {
             best_cost = cost;
             best = s;
@@ -356,8 +361,7 @@ namespace {
 template <int NT, bool kBlock>
 cudaError_t launch_variant(const W8A8Args &a, const CUtensorMap (&maps)[4], cudaStream_t s) {
     const uint32_t tiles = (a.n + kRowsPerCta - 1) / kRowsPerCta;
-    const uint32_t slots = (uint32_t)(device_sm_count() * occupancy<NT, kBlock>());
-    const uint32_t split = choose_split_k(tiles, a.kb, slots);
+    const uint32_t split = choose_split_k(tiles, a.kb, cta_slots<NT, kBlock>());
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tiles, split, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -423,6 +427,21 @@ cudaError_t launch_w8a8_gemv_tma(const W8A8Args &a, int format, const uint8_t *c
     const bool blk = format == QDL_SCALE_BLOCK128;
     if (a.m <= 8) return blk ? launch_variant<1, true>(a, maps, s) : launch_variant<1, false>(a, maps, s);
     return blk ? launch_variant<2, true>(a, maps, s) : launch_variant<2, false>(a, maps, s);
+}
+
+cudaError_t plan_w8a8_gemv_tma(const W8A8Args &a, int format, PlanInfo *p) {
+    const bool blk = format == QDL_SCALE_BLOCK128;
+    const uint32_t slots = a.m <= 8 ? (blk ? cta_slots<1, true>() : cta_slots<1, false>())
+                                    : (blk ? cta_slots<2, true>() : cta_slots<2, false>());
+    p->kernel = 1;
+    p->mma_n = a.m <= 8 ? 8 : 16;
+    p->tiles = (a.n + kRowsPerCta - 1) / kRowsPerCta;
+    p->split = choose_split_k(p->tiles, a.kb, slots);
+    p->stages = kStages;
+    p->threads = kThreads;
+    p->smem = a.m <= 8 ? Layout<1>::kAlloc : Layout<2>::kAlloc;
+    p->clusters = (int)(slots / p->split);
+    return cudaGetLastError();
 }
 
 cudaError_t read_and_clear_gemv_fault(uint32_t *value) {
