@@ -179,8 +179,9 @@ QDL_API qdl_status qdl_w8a8_proj_silu(const qdl_w8a8_weight *w, const void *gate
  * and applies zeros and scales per group in f32 (error within 2^-11 of
  * sum |x w|).  Checks: m >= 1; k >= 1; group > 0, group % 16 == 0,
  * k % group == 0; nq, nkv > 0 and multiples of 8; no NULL pointer;
- * alignments above.  Rows are processed 16 at a time (one weight pass per
- * 16 rows). */
+ * alignments above.  With group 128 and nq, nkv multiples of 32 the
+ * tcgen05 kernel streams the weights once per 32 rows; other shapes take an
+ * mma.sync kernel, once per 16 rows. */
 QDL_API qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq, uint32_t nkv,
                              uint32_t group, const uint32_t *const *qw, const float *const *sc,
                              const float *const *zr, float *const *out, void *stream);

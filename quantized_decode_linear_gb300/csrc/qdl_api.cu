@@ -341,14 +341,18 @@ qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq
     a.tiles_kv = (nkv + 127) / 128;
     a.vec2 = vec2;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    for (uint32_t done = 0; done < m; done += 16) {
-        const uint32_t mm = m - done < 16 ? m - done : 16;
+    // tensor-core path (group 128, widths multiples of 32): 32 rows per pass;
+    // otherwise the mma.sync kernel, 16 rows per pass
+    const bool tc = int4_tc_supported(nq, nkv, group);
+    const uint32_t chunk = tc ? 32 : 16;
+    for (uint32_t done = 0; done < m; done += chunk) {
+        const uint32_t mm = m - done < chunk ? m - done : chunk;
         a.x = x + (size_t)done * k;
         a.out0 = out[0] + (size_t)done * nq;
         a.out1 = out[1] + (size_t)done * nkv;
         a.out2 = out[2] + (size_t)done * nkv;
         a.m = mm;
-        cudaError_t e = launch_int4_qkv(a, s);
+        cudaError_t e = tc ? launch_int4_qkv_tc(a, s) : launch_int4_qkv(a, s);
         if (e != cudaSuccess) return cuda_fail(who, e);
     }
     return ok();
@@ -449,6 +453,8 @@ qdl_status qdl_check_device_fault(void *stream) {
     uint32_t word = 0, word_tc = 0;
     if ((e = read_and_clear_gemv_fault(&word)) != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
     if ((e = read_and_clear_tc_fault(&word_tc)) != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
+    word |= word_tc;
+    if ((e = read_and_clear_int4_fault(&word_tc)) != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
     word |= word_tc;
     if (word != 0)
         return fail(QDL_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up (fault word 0x%x: 1 = producer, 2/8 = consumer or MMA, 4/16/32 = accumulator)",

@@ -87,6 +87,9 @@ cudaError_t launch_w8a8_proj_fused(const W8A8Args &a, const uint8_t *const seg_w
                                    cudaStream_t s);
 uint32_t choose_split_k(uint32_t tiles, uint32_t kb, uint32_t slots);
 cudaError_t launch_int4_qkv(const Int4Args &a, cudaStream_t s);
+bool int4_tc_supported(uint32_t nq, uint32_t nkv, uint32_t group);
+cudaError_t launch_int4_qkv_tc(const Int4Args &a, cudaStream_t s);  // up to 32 token rows
+cudaError_t read_and_clear_int4_fault(uint32_t *value);
 
 int device_sm_count();  // of the current device, cached
 
