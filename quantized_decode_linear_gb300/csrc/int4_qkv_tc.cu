@@ -12,21 +12,26 @@
 // the AWQ bit pattern gives for free: (w >> 4i) & 0x000F000F | 0x64006400 is the
 // f16 pair (1024 + nib(col 2i), 1024 + nib(col 2i+1)) of one packed word.
 //
-// Roles (one CTA = 128 output columns of one projection x a range of groups):
-//   warp 0, one lane : TMA producer of the packed words, [128 K rows x 16
-//                      words] per group, 64-byte swizzle, into a ring of
-//                      stages (evict-first).
+// Roles (one CTA = 256 output columns of one projection x a range of groups;
+// one pipeline stage = half a group, 64 K rows):
+//   warp 0, one lane : TMA producer of the packed words, [64 K rows x 32
+//                      words] = 128-byte rows per stage, 128-byte swizzle,
+//                      into a ring of stages (evict-first).
 //   warp 1           : allocates tensor memory; one lane issues tcgen05.mma
-//                      kind::f16 (M = 128 columns, N = NTOK tokens, K = 16 per
-//                      instruction, eight per group), A = weights MN-major,
-//                      B = x~ K-major.
-//   warps 2..9       : converters.  Unpack each group's words into the f16 A
-//                      operand (one 16-byte store per word), convert the group's
-//                      x to f16 into the B operand (128-byte swizzle) and sum
-//                      x~ per token (fixed order).
-//   warps 10..13     : epilogue.  Per group, read the accumulator (tcgen05.ld)
-//                      and fold s (acc - (1024 + z) sum x~) into register
-//                      totals.
+//                      kind::f16, two column halves (M = 128 each) x four
+//                      K = 16 steps per stage, N = NTOK tokens; A = weights
+//                      MN-major, B = x~ K-major.  The two stages of a group
+//                      accumulate into the same TMEM buffer.
+//   warps 2..9       : converters.  Unpack each stage's words into the f16 A
+//                      operand (a 16-byte load of four words, four 16-byte
+//                      stores) and convert x to f16 into the B operand
+//                      (128-byte swizzle).
+//   warps 10..13     : epilogue.  Per group, read both halves' accumulators
+//                      and the all-ones accumulator (= sum x~ per token) with
+//                      tcgen05.ld and fold s (acc - (1024 + z) sum x~) into
+//                      register totals.
+// sum_k x~ comes from one more MMA per K step against a constant all-ones A
+// operand, so it is the tensor core's own sum of the same x~.
 // Split-K CTAs of one cluster reduce their partials through distributed shared
 // memory in rank order.  Every wait is bounded (fault word + drain + return).
 #include <cooperative_groups.h>
@@ -45,46 +50,54 @@ static __device__ uint32_t g_int4_fault;
 
 namespace {
 
-constexpr int kCols = 128;             // output columns per tile (MMA M)
-constexpr int kGroupK = 128;           // K per stage = group size
+constexpr int kCols = 256;             // output columns per tile (two MMA halves of 128)
+constexpr int kGroupK = 128;           // group size
+constexpr int kStageK = 64;            // K rows per pipeline stage (half a group)
 constexpr int kConvWarps = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kThreadsI4 = (2 + kConvWarps + kEpiWarps) * 32;
-constexpr uint32_t kPacked = kGroupK * 64;  // 128 rows x 16 words
-constexpr uint32_t kAOp = kCols * kGroupK * 2;  // f16 A operand, 32 KB
+constexpr uint32_t kPacked = kStageK * 128;      // 64 rows x 32 words
+constexpr uint32_t kAOp = kCols * kStageK * 2;   // f16 A operand, 32 KB
 // A (MN-major, no swizzle): core matrix (8 k rows x 8 columns x 2 B = 128 B)
 // (mi, ki) at mi * kAStrideM + ki * kAStrideK
 constexpr uint32_t kAStrideM = 128;   // next 8 columns
-constexpr uint32_t kAStrideK = 2048;  // next 8 k
+constexpr uint32_t kAStrideK = 4096;  // next 8 k (32 core matrices of columns)
+// all-ones A operand for the per-token sums: 16 x 2 core matrices (M = 128, K = 16)
+constexpr uint32_t kOnesStrideK = 2048;
+constexpr uint32_t kOnes = 2 * kOnesStrideK;
 
 template <int NTOK>
 struct I4 {
-    static constexpr int kRing = 8;                              // packed stages
-    static constexpr uint32_t kBOp = NTOK * 256;                 // f16 B operand: 2 SW128 atoms of NTOK rows
-    static constexpr uint32_t kOpBuf = kAOp + kBOp;              // one operand buffer (A then B)
-    static constexpr int kAcc = NTOK <= 64 ? 4 : 2;
+    static constexpr uint32_t kXBox = NTOK * 128;                // one x box: NTOK rows x 32 f32 (128-byte swizzle)
+    static constexpr uint32_t kRingStage = kPacked + 2 * kXBox;  // packed words + x for 64 K
+    static constexpr int kRing = NTOK <= 16 ? 6 : 4;             // ring stages
+    static constexpr uint32_t kBOp = NTOK * 128;                 // f16 B operand: one SW128 atom of NTOK rows
+    static constexpr uint32_t kOpBuf = kAOp + (kBOp + 1023) / 1024 * 1024;  // one operand buffer (A then B)
+    static constexpr int kOps = NTOK <= 16 ? 4 : 3;              // operand buffers: converters run ahead
+    static constexpr int kAcc = 4;                               // accumulator buffers (one per group)
     static constexpr uint32_t kRingOff = 0;
-    static constexpr uint32_t kOpOff = kRing * kPacked;          // 64 KB
-    static constexpr uint32_t kBarOff = kOpOff + 2 * kOpBuf;
-    static constexpr uint32_t kSumOff = kBarOff + 512;           // [kAcc][NTOK] sum x~
-    static constexpr uint32_t kPartOff = kSumOff + kAcc * NTOK * 4;  // [NTOK][16] partial sums
-    static constexpr uint32_t kBytes = kPartOff + NTOK * 16 * 4;
+    static constexpr uint32_t kOpOff = kRing * kRingStage;
+    static constexpr uint32_t kOnesOff = kOpOff + kOps * kOpBuf;  // all-ones A operand, M=128 x K=16
+    static constexpr uint32_t kBarOff = kOnesOff + kOnes;
+    static constexpr uint32_t kBytes = kBarOff + 512;
     static constexpr uint32_t kAlloc = kBytes + 1024;
-    static constexpr int kCpt = NTOK;  // columns per epilogue thread (NTOK <= 64)
-    static constexpr uint32_t kTmemCols = NTOK * kAcc <= 32 ? 32 : (NTOK * kAcc <= 64 ? 64 : (NTOK * kAcc <= 128 ? 128 : 256));
+    static constexpr int kCpt = NTOK;  // token columns per epilogue thread and half
+    // per accumulator buffer: column half 0, column half 1, all-ones (sum x~)
+    static constexpr uint32_t kTmemCols = 3 * NTOK * kAcc <= 64 ? 64 : (3 * NTOK * kAcc <= 128 ? 128 : (3 * NTOK * kAcc <= 256 ? 256 : 512));
     static_assert(NTOK <= 32, "tokens per pass");
     static_assert(kCols * NTOK * 4 <= kOpOff, "reduction buffer fits the ring");
     static_assert(kOpOff % 1024 == 0 && kOpBuf % 1024 == 0, "alignment");
+    static_assert(kAlloc <= 232448, "shared memory per CTA");
 };
 
 // MN-major operand without swizzle: the leading byte offset is the stride
 // between core matrices along K, the stride byte offset the stride along M
 // (measured on sm_103a with an operand whose nibbles encode their own
 // coordinates).
-__device__ __forceinline__ uint64_t desc_mn_noswz(uint32_t saddr) {
+__device__ __forceinline__ uint64_t desc_mn_noswz(uint32_t saddr, uint32_t stride_k = kAStrideK) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)(kAStrideK >> 4) << 16;  // leading byte offset: next 8 k
+    d |= (uint64_t)(stride_k >> 4) << 16;   // leading byte offset: next 8 k
     d |= (uint64_t)(kAStrideM >> 4) << 32;  // stride byte offset: next 8 columns
     d |= (uint64_t)1 << 46;                 // descriptor version
     return d;                               // swizzle none
@@ -103,7 +116,7 @@ __device__ __forceinline__ uint64_t desc_k_sw128(uint32_t saddr, uint32_t atom_s
 // kind::f16: D f32, A and B f16, A MN-major (transposed), B K-major.
 template <int NTOK>
 __device__ __forceinline__ constexpr uint32_t idesc_f16() {
-    return (1u << 4) | (1u << 15) | ((uint32_t)(NTOK >> 3) << 17) | ((uint32_t)(kCols >> 4) << 24);
+    return (1u << 4) | (1u << 15) | ((uint32_t)(NTOK >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -138,20 +151,6 @@ __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
 
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ void conv_barrier() {  // the converter warps only
-    asm volatile("bar.sync 1, %0;" ::"n"(kConvWarps * 32) : "memory");
-}
-
 __device__ __forceinline__ uint32_t h2_bits(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&h);
@@ -160,23 +159,21 @@ __device__ __forceinline__ uint32_t h2_bits(float lo, float hi) {
 template <int NTOK>
 __global__ void __launch_bounds__(kThreadsI4, 1)
     int4_qkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const Int4Args a) {
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_x,
+                       const Int4Args a) {
     using C = I4<NTOK>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);  // [kRing] packed words landed
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);  // [kRing] packed words and x landed
     uint64_t *empty = full + C::kRing;                                  // [kRing] packed slot free
-    uint64_t *opfull = empty + C::kRing;                                // [2] operands written
-    uint64_t *opempty = opfull + 2;                                     // [2] operands consumed
-    uint64_t *accf = opempty + 2;                                       // [kAcc]
-    uint64_t *acce = accf + C::kAcc;                                    // [kAcc]
-    uint64_t *sums = acce + C::kAcc;                                    // [kAcc] sum x~ written
-    uint64_t *done = sums + C::kAcc;
+    uint64_t *opfull = empty + C::kRing;                                // [kOps] operands written
+    uint64_t *opempty = opfull + C::kOps;                               // [kOps] operands consumed
+    uint64_t *accf = opempty + C::kOps;                                 // [kAcc] group accumulated
+    uint64_t *acce = accf + C::kAcc;                                    // [kAcc] group drained
+    uint64_t *done = acce + C::kAcc;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     volatile uint32_t *abort_flag = tmem_slot + 1;
-    float *sbuf = reinterpret_cast<float *>(smem + C::kSumOff);
-    float *part = reinterpret_cast<float *>(smem + C::kPartOff);
-    float *red = reinterpret_cast<float *>(smem);  // [NTOK][128] at the end
+    float *red = reinterpret_cast<float *>(smem);  // [NTOK][256] at the end
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -198,21 +195,21 @@ __global__ void __launch_bounds__(kThreadsI4, 1)
     const uint32_t col0 = tile * kCols;
     const uint32_t split = gridDim.y, sidx = blockIdx.y;
     const uint32_t g0 = (a.groups * sidx) / split, g1 = (a.groups * (sidx + 1)) / split;
-    const uint32_t niter = g1 - g0;
+    const uint32_t ngroups = g1 - g0;
+    const uint32_t nstage = 2 * ngroups;  // two stages of 64 K rows per group
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kRing; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConvWarps);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < C::kOps; ++b) {
             mbar_init(&opfull[b], kConvWarps);
             mbar_init(&opempty[b], 1);
         }
         for (int b = 0; b < C::kAcc; ++b) {
             mbar_init(&accf[b], 1);
             mbar_init(&acce[b], kEpiWarps);
-            mbar_init(&sums[b], 1);
         }
         mbar_init(done, 1);
         *abort_flag = 0;
@@ -224,11 +221,16 @@ __global__ void __launch_bounds__(kThreadsI4, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // token rows >= m of both B operands stay zero for the whole kernel
-    for (uint32_t i = threadIdx.x; i < 2 * C::kBOp / 16; i += blockDim.x) {
+    // token rows >= m of every B operand stay zero for the whole kernel; the
+    // all-ones operand is written once (f16 1.0 = 0x3C00)
+    for (uint32_t i = threadIdx.x; i < C::kOps * C::kBOp / 16; i += blockDim.x) {
         const uint32_t buf = i / (C::kBOp / 16), off = (i % (C::kBOp / 16)) * 16;
-        sts128(smem_u32(smem + C::kOpOff + buf * C::kOpBuf + kAOp + off), 0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(smem + C::kOpOff + buf * C::kOpBuf + kAOp + off) = make_uint4(0, 0, 0, 0);
     }
+    for (uint32_t i = threadIdx.x; i < kOnes / 16; i += blockDim.x)
+        *reinterpret_cast<uint4 *>(smem + C::kOnesOff + i * 16) =
+            make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+    fence_proxy_async_smem();
     fence_before();
     __syncthreads();
     fence_after();
@@ -243,23 +245,30 @@ __global__ void __launch_bounds__(kThreadsI4, 1)
     };
 
     uint32_t issued = 0;
-    float total[C::kCpt];
+    float total[2][C::kCpt];  // [column half][token]
 #pragma unroll
-    for (int j = 0; j < C::kCpt; ++j) total[j] = 0.0f;
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int j = 0; j < C::kCpt; ++j) total[hh][j] = 0.0f;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             prefetch_tmap(tmap);
+            prefetch_tmap(&tm_x);
             const uint64_t pol = policy_evict_first();
-            for (uint32_t it = 0; it < niter; ++it) {
-                const uint32_t slot = it % C::kRing, ph = (it / C::kRing) & 1;
+            const uint64_t pol_x = policy_evict_last();
+            for (uint32_t st = 0; st < nstage; ++st) {
+                const uint32_t slot = st % C::kRing, ph = (st / C::kRing) & 1;
                 wait(&empty[slot], ph ^ 1, 1);
                 if (*abort_flag) break;
-                mbar_arrive_expect_tx(&full[slot], kPacked);
-                issued = it + 1;
-                tma_load_2d(smem + C::kRingOff + slot * kPacked, tmap, (int32_t)(col0 / 8),
-                            (int32_t)((g0 + it) * kGroupK), &full[slot], pol);
+                mbar_arrive_expect_tx(&full[slot], C::kRingStage);
+                issued = st + 1;
+                uint8_t *rs = smem + C::kRingOff + slot * C::kRingStage;
+                const int32_t k0 = (int32_t)(g0 * kGroupK + st * kStageK);
+                tma_load_2d(rs, tmap, (int32_t)(col0 / 8), k0, &full[slot], pol);
+                tma_load_2d(rs + kPacked, &tm_x, k0, 0, &full[slot], pol_x);            // x[:, k0 .. k0+31]
+                tma_load_2d(rs + kPacked + C::kXBox, &tm_x, k0 + 32, 0, &full[slot], pol_x);  // x[:, k0+32 .. k0+63]
             }
         }
     } else if (warp == 1) {
@@ -267,135 +276,119 @@ __global__ void __launch_bounds__(kThreadsI4, 1)
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16<NTOK>();
             const uint32_t obase = smem_u32(smem + C::kOpOff);
-            for (uint32_t it = 0; it < niter; ++it) {
-                const uint32_t o = it & 1, b = it % C::kAcc;
-                wait(&acce[b], ((it / C::kAcc) & 1) ^ 1, 2);
-                wait(&opfull[o], (it >> 1) & 1, 4);
+            const uint32_t ones = smem_u32(smem + C::kOnesOff);
+            for (uint32_t st = 0; st < nstage; ++st) {
+                const uint32_t o = st % C::kOps, gi = st >> 1, b = gi % C::kAcc, half_k = st & 1;
+                if (half_k == 0) wait(&acce[b], ((gi / C::kAcc) & 1) ^ 1, 2);
+                wait(&opfull[o], (st / C::kOps) & 1, 4);
                 if (*abort_flag) break;
                 fence_after();
                 const uint32_t abuf = obase + o * C::kOpBuf, bbuf = abuf + kAOp;
+                const uint32_t dbase = tmem + b * 3 * NTOK;
 #pragma unroll
-                for (int i = 0; i < kGroupK / 16; ++i) {
-                    // A: +16 k = two core matrices along K; B: 32 bytes inside a
-                    // 64-element atom, next atom every four instructions
-                    const uint64_t ad = desc_mn_noswz(abuf + i * 2 * kAStrideK);
-                    const uint64_t bd = desc_k_sw128(bbuf + (i >> 2) * (NTOK * 128) + (i & 3) * 32, NTOK * 128);
-                    mma_f16(tmem + b * NTOK, ad, bd, idesc, i > 0 ? 1u : 0u);
+                for (int i = 0; i < kStageK / 16; ++i) {
+                    // A: +16 k = two core matrices along K; B: 32 bytes inside the 64-element atom
+                    const uint64_t bd = desc_k_sw128(bbuf + i * 32, NTOK * 128);
+                    const uint32_t acc = (half_k | i) != 0 ? 1u : 0u;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh)  // column halves
+                        mma_f16(dbase + hh * NTOK, desc_mn_noswz(abuf + hh * 16 * kAStrideM + i * 2 * kAStrideK), bd,
+                                idesc, acc);
+                    mma_f16(dbase + 2 * NTOK, desc_mn_noswz(ones, kOnesStrideK), bd, idesc, acc);  // sum x~
                 }
                 commit(&opempty[o]);
-                commit(&accf[b]);
+                if (half_k == 1) commit(&accf[b]);
             }
             commit(done);
         }
     } else if (warp < 2 + kConvWarps) {
         // ------------------------------------------------------------ converters
-        const int t = threadIdx.x - 64;  // 0 .. 255
-        const uint32_t kl = t & 7, wc = (t >> 3) & 15, kh = t >> 7;
-        const uint32_t rbase = smem_u32(smem + C::kRingOff);
-        const uint32_t obase = smem_u32(smem + C::kOpOff);
-        const bool word_ok = col0 / 8 + wc < n / 8;
-        for (uint32_t it = 0; it < niter; ++it) {
-            const uint32_t slot = it % C::kRing, ph = (it / C::kRing) & 1;
-            const uint32_t o = it & 1, b = it % C::kAcc;
-            const uint32_t g = g0 + it;
-            // x for this group: token tok = (t & 7) + 8i, 8 K values at chunk t >> 3 (0..15 -> 16 x 8 = 128)
-            float4 xv[NTOK / 8][2];
+        const int t = threadIdx.x - 64;                   // 0 .. 255
+        const uint32_t kr = t & 7, wq = (t >> 3) & 7, kq = t >> 6;  // K row in a core matrix, word quad, K quarter
+        for (uint32_t st = 0; st < nstage; ++st) {
+            const uint32_t slot = st % C::kRing, ph = (st / C::kRing) & 1;
+            const uint32_t o = st % C::kOps;
+            wait(&opempty[o], ((st / C::kOps) & 1) ^ 1, 16);
+            wait(&full[slot], ph, 16);
+            // A: words (k, 4wq .. 4wq+3) for k = 8 (kq + 4j) + kr: one 16-byte load,
+            // then row k & 7 of core matrices (4wq + i, k / 8).  Plain shared-memory
+            // accesses (ordered by the barrier waits' memory clobbers).
+            const uint8_t *ring = smem + C::kRingOff + slot * C::kRingStage;
+            uint8_t *abuf = smem + C::kOpOff + o * C::kOpBuf;
+            uint4 wv[2];
 #pragma unroll
-            for (int i = 0; i < NTOK / 8; ++i) {
-                const uint32_t tok = (t & 7) + 8 * i;
-                const uint32_t kc = t >> 3;
-                if (tok < a.m && kc < 16) {
-                    const float4 *p = reinterpret_cast<const float4 *>(a.x + (size_t)tok * a.k + g * kGroupK + kc * 8);
-                    xv[i][0] = __ldg(p);
-                    xv[i][1] = __ldg(p + 1);
-                } else {
-                    xv[i][0] = xv[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < 2; ++j) {
+                const uint32_t k = 8 * (kq + 4 * j) + kr;
+                // 128-byte swizzle of the TMA tile: 16-byte chunk index ^= row & 7
+                wv[j] = *reinterpret_cast<const uint4 *>(ring + k * 128 + ((wq ^ (k & 7)) << 4));
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const uint32_t k = 8 * (kq + 4 * j) + kr;
+                const uint32_t w4[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t w = w4[i];  // words beyond the projection width read as zero (TMA fill)
+                    uint4 h;
+                    h.x = (w & 0x000F000Fu) | 0x64006400u;
+                    h.y = ((w >> 4) & 0x000F000Fu) | 0x64006400u;
+                    h.z = ((w >> 8) & 0x000F000Fu) | 0x64006400u;
+                    h.w = ((w >> 12) & 0x000F000Fu) | 0x64006400u;
+                    *reinterpret_cast<uint4 *>(abuf + (4 * wq + i) * kAStrideM + (k >> 3) * kAStrideK + kr * 16) = h;
                 }
             }
-            wait(&opempty[o], ((it >> 1) & 1) ^ 1, 16);
-            wait(&acce[b], ((it / C::kAcc) & 1) ^ 1, 16);
-            wait(&full[slot], ph, 16);
-            // A: words (k, wc) for k = 8 (2j + kh) + kl -> 16-byte row kl of core matrix (wc, k / 8)
-            const uint32_t ring = rbase + slot * kPacked;
-            const uint32_t abuf = obase + o * C::kOpBuf;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t k = 8 * (2 * j + kh) + kl;
-                // 64-byte swizzle of the TMA tile: 16-byte chunk index ^= (row >> 1) & 3
-                const uint32_t w = word_ok ? lds32(ring + k * 64 + ((((wc >> 2) ^ ((k >> 1) & 3))) << 4) + (wc & 3) * 4)
-                                           : 0u;
-                uint32_t h[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) h[i] = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
-                sts128(abuf + wc * kAStrideM + (k >> 3) * kAStrideK + kl * 16, h[0], h[1], h[2], h[3]);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);  // packed words consumed
-            // B: x~ (f16) in the K-major 128-byte-swizzle layout, plus partial sums
-            const uint32_t bbuf = abuf + kAOp;
+            // B: x~ (f16) in the K-major 128-byte-swizzle layout.  x of this stage
+            // sits in the ring stage as two [NTOK x 32 f32] boxes (128-byte
+            // swizzle); only valid token rows are written.
+            uint8_t *bbuf = abuf + kAOp;
 #pragma unroll
             for (int i = 0; i < NTOK / 8; ++i) {
                 const uint32_t tok = (t & 7) + 8 * i;
-                const uint32_t kc = t >> 3;  // 0..31; chunks >= 16 idle
-                if (kc < 16) {
-                    const float4 u = xv[i][0], v = xv[i][1];
-                    const uint32_t p0 = h2_bits(u.x, u.y), p1 = h2_bits(u.z, u.w), p2 = h2_bits(v.x, v.y),
-                                   p3 = h2_bits(v.z, v.w);
-                    if (tok < a.m) {
-                        const uint32_t atom = kc >> 3, chunk = kc & 7;
-                        sts128(bbuf + atom * (NTOK * 128) + tok * 128 + ((chunk ^ (tok & 7)) << 4), p0, p1, p2, p3);
-                    }
-                    // partial sum of the rounded values, in a fixed order
-                    const __half2 *hp0 = reinterpret_cast<const __half2 *>(&p0);
-                    const __half2 *hp1 = reinterpret_cast<const __half2 *>(&p1);
-                    const __half2 *hp2 = reinterpret_cast<const __half2 *>(&p2);
-                    const __half2 *hp3 = reinterpret_cast<const __half2 *>(&p3);
-                    float ps = 0.0f;
-                    ps += __low2float(*hp0); ps += __high2float(*hp0);
-                    ps += __low2float(*hp1); ps += __high2float(*hp1);
-                    ps += __low2float(*hp2); ps += __high2float(*hp2);
-                    ps += __low2float(*hp3); ps += __high2float(*hp3);
-                    part[tok * 16 + kc] = ps;
+                const uint32_t kc = t >> 3;  // 8-value chunk 0..7 of the stage; threads with kc >= 8 idle
+                if (kc < 8 && tok < a.m) {
+                    const uint8_t *xb = ring + kPacked + (kc >> 2) * C::kXBox + tok * 128;
+                    const uint32_t c0 = (2 * (kc & 3)) ^ (tok & 7), c1 = (2 * (kc & 3) + 1) ^ (tok & 7);
+                    const float4 u = *reinterpret_cast<const float4 *>(xb + (c0 << 4));
+                    const float4 v = *reinterpret_cast<const float4 *>(xb + (c1 << 4));
+                    *reinterpret_cast<uint4 *>(bbuf + tok * 128 + ((kc ^ (tok & 7)) << 4)) =
+                        make_uint4(h2_bits(u.x, u.y), h2_bits(u.z, u.w), h2_bits(v.x, v.y), h2_bits(v.z, v.w));
                 }
             }
             fence_proxy_async_smem();
-            conv_barrier();
-            if (t < NTOK) {  // sum x~ of token t over the group's 16 chunks, in order
-                float s = 0.0f;
-#pragma unroll
-                for (int c = 0; c < 16; ++c) s += part[t * 16 + c];
-                sbuf[b * NTOK + t] = s;
-            }
-            conv_barrier();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&opfull[o]);
-            if (t == 0) mbar_arrive(&sums[b]);
-            (void)g;
+            if (lane == 0) {
+                mbar_arrive(&empty[slot]);  // ring stage (words and x) consumed
+                mbar_arrive(&opfull[o]);    // operands written
+            }
         }
     } else {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;
-        const uint32_t lrow = 32 * quad + lane;  // column within the tile
-        const uint32_t col = col0 + lrow;
-        const bool col_ok = col < n;
+        const uint32_t lrow = 32 * quad + lane;  // column within a half
         const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16);
-        for (uint32_t it = 0; it < niter; ++it) {
-            const uint32_t b = it % C::kAcc, g = g0 + it;
-            const float s_c = col_ok ? __ldg(sc + (size_t)g * n + col) : 0.0f;
-            const float z_c = col_ok ? __ldg(zr + (size_t)g * n + col) : 0.0f;
-            const float zc = 1024.0f + z_c;
-            wait(&sums[b], (it / C::kAcc) & 1, 32);
-            wait(&accf[b], (it / C::kAcc) & 1, 32);
+        for (uint32_t gi = 0; gi < ngroups; ++gi) {
+            const uint32_t b = gi % C::kAcc, g = g0 + gi;
+            float s_c[2], zc[2];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t col = col0 + hh * 128 + lrow;
+                const bool ok = col < n;
+                s_c[hh] = ok ? __ldg(sc + (size_t)g * n + col) : 0.0f;
+                zc[hh] = 1024.0f + (ok ? __ldg(zr + (size_t)g * n + col) : 0.0f);
+            }
+            wait(&accf[b], (gi / C::kAcc) & 1, 32);
             fence_after();
 #pragma unroll
             for (int c = 0; c < C::kCpt / 16; ++c) {
-                float v[16];
-                ld16(taddr + b * NTOK + 16 * c, v);
+                float sx[16], v0[16], v1[16];
+                ld16(taddr + b * 3 * NTOK + 2 * NTOK + 16 * c, sx);  // sum x~ per token (any row)
+                ld16(taddr + b * 3 * NTOK + 16 * c, v0);
+                ld16(taddr + b * 3 * NTOK + NTOK + 16 * c, v1);
                 wait_ld();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float sx = sbuf[b * NTOK + 16 * c + i];
-                    total[16 * c + i] = fmaf(s_c, fmaf(-zc, sx, v[i]), total[16 * c + i]);
+                    total[0][16 * c + i] = fmaf(s_c[0], fmaf(-zc[0], sx[i], v0[i]), total[0][16 * c + i]);
+                    total[1][16 * c + i] = fmaf(s_c[1], fmaf(-zc[1], sx[i], v1[i]), total[1][16 * c + i]);
                 }
             }
             fence_before();
@@ -409,8 +402,8 @@ __global__ void __launch_bounds__(kThreadsI4, 1)
     if (*abort_flag) {
         if (warp == 0 && lane == 0) {
             const uint32_t first = issued > (uint32_t)C::kRing ? issued - C::kRing : 0;
-            for (uint32_t it = first; it < issued; ++it)
-                mbar_wait(&full[it % C::kRing], (it / C::kRing) & 1, kWaitLimitNs);
+            for (uint32_t st = first; st < issued; ++st)
+                mbar_wait(&full[st % C::kRing], (st / C::kRing) & 1, kWaitLimitNs);
         }
         if (warp == 1 && lane == 0) mbar_wait(done, 0, kWaitLimitNs);
         __syncthreads();
@@ -422,12 +415,14 @@ __global__ void __launch_bounds__(kThreadsI4, 1)
     if (warp >= 2 + kConvWarps) {
         const uint32_t lrow = 32 * (warp & 3) + lane;
 #pragma unroll
-        for (int j = 0; j < C::kCpt; ++j) {
-            if (split == 1)
-                store(j, lrow, total[j]);
-            else
-                red[j * kCols + lrow] = total[j];
-        }
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int j = 0; j < C::kCpt; ++j) {
+                if (split == 1)
+                    store(j, hh * 128 + lrow, total[hh][j]);
+                else
+                    red[j * kCols + hh * 128 + lrow] = total[hh][j];
+            }
     }
     if (split > 1) {
         cg::cluster_group cluster = cg::this_cluster();
@@ -463,7 +458,7 @@ __global__ void __launch_bounds__(kThreadsI4, 1)
 // ---------------------------------------------------------------- host side
 
 cudaError_t make_tmap_words(CUtensorMap *map, const void *base, uint64_t words, uint64_t rows) {
-    // packed words [rows, words] u32, box 16 words x 128 rows, 64-byte swizzle
+    // packed words [rows, words] u32, box 32 words x 64 rows, 128-byte swizzle
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -477,35 +472,63 @@ cudaError_t make_tmap_words(CUtensorMap *map, const void *base, uint64_t words, 
     if (fn == nullptr) return cudaErrorNotSupported;
     cuuint64_t gdim[2] = {words, rows};
     cuuint64_t gstride[1] = {words * 4};
-    cuuint32_t box[2] = {16, (cuuint32_t)kGroupK};
+    cuuint32_t box[2] = {32, (cuuint32_t)kStageK};
     cuuint32_t estride[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), gdim, gstride, box, estride,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Resident CTAs for each cluster size (one CTA per SM: the cluster
+// occupancy query accounts for how clusters pack into GPCs).
+cudaError_t make_tmap_f32(CUtensorMap *map, const float *x, uint64_t k, uint64_t rows, uint32_t box_rows) {
+    // x [rows, k] f32, box 32 values x box_rows rows, 128-byte swizzle; rows
+    // past the end read as zero
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (fn == nullptr) return cudaErrorNotSupported;
+    cuuint64_t gdim[2] = {k, rows};
+    cuuint64_t gstride[1] = {k * 4};
+    cuuint32_t box[2] = {32, box_rows};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(x), gdim, gstride, box, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <int NTOK>
-uint32_t slots_i4() {
+const uint32_t *cluster_fit() {
     static std::mutex mu;
-    static std::vector<uint32_t> cache;
+    static std::vector<std::vector<uint32_t>> cache;
     int dev = 0;
     cudaGetDevice(&dev);
     std::lock_guard<std::mutex> lock(mu);
-    if ((int)cache.size() <= dev) cache.resize(dev + 1, 0);
-    if (cache[dev] == 0) {
+    if ((int)cache.size() <= dev) cache.resize(dev + 1);
+    if (cache[dev].empty()) {
+        const void *f = (const void *)int4_qkv_tc_kernel<NTOK>;
         cudaFuncSetAttribute(int4_qkv_tc_kernel<NTOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)I4<NTOK>::kAlloc);
-        cache[dev] = (uint32_t)(device_sm_count() * resident_ctas((const void *)int4_qkv_tc_kernel<NTOK>, kThreadsI4,
-                                                                  I4<NTOK>::kAlloc, I4<NTOK>::kTmemCols));
+        const int per_sm = resident_ctas(f, kThreadsI4, I4<NTOK>::kAlloc, I4<NTOK>::kTmemCols);
+        cache[dev].assign(8, 0);
+        resident_cta_slots(f, kThreadsI4, I4<NTOK>::kAlloc, per_sm, cache[dev].data());
     }
-    return cache[dev];
+    return cache[dev].data();
 }
 
 template <int NTOK>
-cudaError_t launch_i4(const Int4Args &a, const CUtensorMap (&maps)[3], cudaStream_t s) {
+cudaError_t launch_i4(const Int4Args &a, const CUtensorMap (&maps)[4], cudaStream_t s) {
     const uint32_t tiles = a.tiles_q + 2 * a.tiles_kv;
-    const uint32_t split = choose_split_k(tiles, a.groups, slots_i4<NTOK>());
+    const uint32_t split = choose_split_k(tiles, a.groups, cluster_fit<NTOK>());
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tiles, split, 1);
     cfg.blockDim = dim3(kThreadsI4, 1, 1);
@@ -518,7 +541,7 @@ cudaError_t launch_i4(const Int4Args &a, const CUtensorMap (&maps)[3], cudaStrea
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, int4_qkv_tc_kernel<NTOK>, maps[0], maps[1], maps[2], a);
+    return cudaLaunchKernelEx(&cfg, int4_qkv_tc_kernel<NTOK>, maps[0], maps[1], maps[2], maps[3], a);
 }
 
 }  // namespace
@@ -529,14 +552,20 @@ bool int4_tc_supported(uint32_t nq, uint32_t nkv, uint32_t group) {
 
 // One launch for up to 32 token rows.
 cudaError_t launch_int4_qkv_tc(const Int4Args &a, cudaStream_t s) {
-    CUtensorMap maps[3];
+    CUtensorMap maps[4];
     const uint32_t ns[3] = {a.nq, a.nkv, a.nkv};
     const uint32_t *qw[3] = {a.qw0, a.qw1, a.qw2};
     for (int p = 0; p < 3; ++p) {
         cudaError_t e = make_tmap_words(&maps[p], qw[p], ns[p] / 8, a.k);
         if (e != cudaSuccess) return e;
     }
-    return a.m <= 16 ? launch_i4<16>(a, maps, s) : launch_i4<32>(a, maps, s);
+    const uint32_t ntok = a.m <= 16 ? 16 : 32;
+    cudaError_t e = make_tmap_f32(&maps[3], a.x, a.k, a.m, ntok);
+    if (e != cudaSuccess) return e;
+    Int4Args b = a;  // this kernel's tiles are 256 columns wide
+    b.tiles_q = (a.nq + kCols - 1) / kCols;
+    b.tiles_kv = (a.nkv + kCols - 1) / kCols;
+    return ntok == 16 ? launch_i4<16>(b, maps, s) : launch_i4<32>(b, maps, s);
 }
 
 cudaError_t read_and_clear_int4_fault(uint32_t *value) {

@@ -538,22 +538,23 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1)
 // ---------------------------------------------------------------- host side
 
 template <int NTOK, bool kBlock, bool kFused>
-uint32_t cta_slots_tc() {
+const uint32_t *cta_slots_tc() {
     using C = Tc<NTOK, kBlock, kFused>;
     static std::mutex mu;
-    static std::vector<uint32_t> cache;
+    static std::vector<std::vector<uint32_t>> cache;
     int dev = 0;
     cudaGetDevice(&dev);
     std::lock_guard<std::mutex> lock(mu);
-    if ((int)cache.size() <= dev) cache.resize(dev + 1, 0);
-    if (cache[dev] == 0) {
+    if ((int)cache.size() <= dev) cache.resize(dev + 1);
+    if (cache[dev].empty()) {
+        const void *f = (const void *)w8a8_gemm_tc_kernel<NTOK, kBlock, kFused>;
         cudaFuncSetAttribute(w8a8_gemm_tc_kernel<NTOK, kBlock, kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::kAlloc);
-        cache[dev] = (uint32_t)(device_sm_count() *
-                                resident_ctas((const void *)w8a8_gemm_tc_kernel<NTOK, kBlock, kFused>, C::kThreads,
-                                              C::kAlloc, C::kTmemCols));
+        cache[dev].assign(8, 0);
+        resident_cta_slots(f, C::kThreads, C::kAlloc, resident_ctas(f, C::kThreads, C::kAlloc, C::kTmemCols),
+                           cache[dev].data());
     }
-    return cache[dev];
+    return cache[dev].data();
 }
 
 template <int NTOK, bool kBlock, bool kFused>
@@ -582,7 +583,7 @@ cudaError_t launch_tc_variant(const W8A8Args &a, const CUtensorMap (&maps)[7], c
 template <int NTOK, bool kBlock, bool kFused>
 void plan_tc_variant(const W8A8Args &a, PlanInfo *p) {
     using C = Tc<NTOK, kBlock, kFused>;
-    const uint32_t slots = cta_slots_tc<NTOK, kBlock, kFused>();
+    const uint32_t *slots = cta_slots_tc<NTOK, kBlock, kFused>();
     p->kernel = 0;
     p->mma_n = NTOK;
     p->tiles = (a.n + kTileRows - 1) / kTileRows;
@@ -590,7 +591,7 @@ void plan_tc_variant(const W8A8Args &a, PlanInfo *p) {
     p->stages = C::kStages;
     p->threads = C::kThreads;
     p->smem = C::kAlloc;
-    p->clusters = (int)(slots / p->split);
+    p->clusters = (int)(slots[p->split - 1] / p->split);
 }
 
 template <bool kBlock>

@@ -313,40 +313,41 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 template <int NT, bool kBlock>
-uint32_t cta_slots() {
+const uint32_t *cta_slots() {
     static std::mutex mu;
-    static std::vector<uint32_t> cache;
+    static std::vector<std::vector<uint32_t>> cache;
     int dev = 0;
     cudaGetDevice(&dev);
     std::lock_guard<std::mutex> lock(mu);
-    if ((int)cache.size() <= dev) cache.resize(dev + 1, 0);
-    if (cache[dev] == 0) {
+    if ((int)cache.size() <= dev) cache.resize(dev + 1);
+    if (cache[dev].empty()) {
+        const void *f = (const void *)w8a8_gemv_tma_kernel<NT, kBlock>;
         cudaFuncSetAttribute(w8a8_gemv_tma_kernel<NT, kBlock>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)Layout<NT>::kAlloc);
-        cache[dev] = (uint32_t)(device_sm_count() *
-                                resident_ctas((const void *)w8a8_gemv_tma_kernel<NT, kBlock>, kThreads,
-                                              Layout<NT>::kAlloc, 0));
+        cache[dev].assign(8, 0);
+        resident_cta_slots(f, kThreads, Layout<NT>::kAlloc, resident_ctas(f, kThreads, Layout<NT>::kAlloc, 0),
+                           cache[dev].data());
     }
-    return cache[dev];
+    return cache[dev].data();
 }
 
 }  // namespace
 
 // Split of K over a cluster of CTAs.  Work is in 128-blocks; a CTA of split s
 // takes up to ceil(kb/s) of them plus about two blocks' worth of pipeline
-// fill and drain.  `slots` CTAs are resident at once (all SMs).  Choose s in
-// 1..8 that minimises waves x per-CTA work, with a small charge for the
-// cluster reduction.
-uint32_t choose_split_k(uint32_t tiles, uint32_t kb, uint32_t slots) {
+// fill and drain.  slots[s-1] CTAs of clusters of s can be resident at once.
+// Choose s in 1..8 that minimises waves x per-CTA work, with a small charge
+// for the cluster reduction.
+uint32_t choose_split_k(uint32_t tiles, uint32_t kb, const uint32_t *slots) {
 #ifdef QDL_TUNE_SPLIT
     if (QDL_TUNE_SPLIT > 0) return QDL_TUNE_SPLIT < kb ? QDL_TUNE_SPLIT : kb;
 #endif
     uint32_t best = 1;
     double best_cost = 1e300;
-    if (slots < 1) slots = 1;
     for (uint32_t s = 1; s <= 8 && s <= kb; ++s) {
+        const uint32_t fit = slots[s - 1] >= s ? slots[s - 1] : s;
         const uint32_t units = tiles * s;
-        const uint32_t waves = (units + slots - 1) / slots;
+        const uint32_t waves = (units + fit - 1) / fit;
         const double cost = (double)waves * (((kb + s - 1) / s) + 2.0) * (1.0 + 0.03 * (s - 1));
         if (cost < best_cost) {
             best_cost = cost;
@@ -354,6 +355,34 @@ uint32_t choose_split_k(uint32_t tiles, uint32_t kb, uint32_t slots) {
         }
     }
     return best;
+}
+
+// CTAs that can be resident at once when launched in clusters of s = 1..8.
+// With one CTA per SM the cluster occupancy query is used, since clusters must
+// fit inside one GPC; with several per SM the SM count times CTAs per SM.
+void resident_cta_slots(const void *func, int threads, size_t smem, int per_sm, uint32_t *out) {
+    const uint32_t flat = (uint32_t)(device_sm_count() * (per_sm > 0 ? per_sm : 1));
+    for (int s = 1; s <= 8; ++s) {
+        uint32_t fit = flat / s * s;
+        if (per_sm <= 1) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(1, s, 1);
+            cfg.blockDim = dim3(threads, 1, 1);
+            cfg.dynamicSmemBytes = smem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 1;
+            attr[0].val.clusterDim.y = s;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) == cudaSuccess && n > 0 && (uint32_t)(n * s) < fit)
+                fit = (uint32_t)(n * s);
+            cudaGetLastError();
+        }
+        out[s - 1] = fit;
+    }
 }
 
 namespace {
@@ -431,8 +460,8 @@ cudaError_t launch_w8a8_gemv_tma(const W8A8Args &a, int format, const uint8_t *c
 
 cudaError_t plan_w8a8_gemv_tma(const W8A8Args &a, int format, PlanInfo *p) {
     const bool blk = format == QDL_SCALE_BLOCK128;
-    const uint32_t slots = a.m <= 8 ? (blk ? cta_slots<1, true>() : cta_slots<1, false>())
-                                    : (blk ? cta_slots<2, true>() : cta_slots<2, false>());
+    const uint32_t *slots = a.m <= 8 ? (blk ? cta_slots<1, true>() : cta_slots<1, false>())
+                                     : (blk ? cta_slots<2, true>() : cta_slots<2, false>());
     p->kernel = 1;
     p->mma_n = a.m <= 8 ? 8 : 16;
     p->tiles = (a.n + kRowsPerCta - 1) / kRowsPerCta;
@@ -440,7 +469,7 @@ cudaError_t plan_w8a8_gemv_tma(const W8A8Args &a, int format, PlanInfo *p) {
     p->stages = kStages;
     p->threads = kThreads;
     p->smem = a.m <= 8 ? Layout<1>::kAlloc : Layout<2>::kAlloc;
-    p->clusters = (int)(slots / p->split);
+    p->clusters = (int)(slots[p->split - 1] / p->split);
     return cudaGetLastError();
 }
 
