@@ -528,7 +528,7 @@ const uint32_t *cluster_fit() {
 template <int NTOK>
 cudaError_t launch_i4(const Int4Args &a, const CUtensorMap (&maps)[4], cudaStream_t s) {
     const uint32_t tiles = a.tiles_q + 2 * a.tiles_kv;
-    const uint32_t split = choose_split_k(tiles, a.groups, cluster_fit<NTOK>());
+    const uint32_t split = choose_split_k(tiles, a.groups, cluster_fit<NTOK>(), 0.0);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tiles, split, 1);
     cfg.blockDim = dim3(kThreadsI4, 1, 1);

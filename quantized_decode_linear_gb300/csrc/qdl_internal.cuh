@@ -85,7 +85,10 @@ cudaError_t read_and_clear_tc_fault(uint32_t *value);
 uint32_t tc_bucket(uint32_t m);  // MMA N of the tensor-core kernel for m token rows
 cudaError_t launch_w8a8_proj_fused(const W8A8Args &a, const uint8_t *const seg_w[3], const uint32_t seg_n[3],
                                    cudaStream_t s);
-uint32_t choose_split_k(uint32_t tiles, uint32_t kb, const uint32_t *slots);  // slots[s-1]: split s
+// Split-K factor minimising waves x (K blocks per CTA + fixed cost), where a
+// split CTA also pays reduce_cost (in K-block units) for the cluster reduction;
+// slots[s-1]: CTAs resident at once when launched in clusters of s.
+uint32_t choose_split_k(uint32_t tiles, uint32_t kb, const uint32_t *slots, double reduce_cost);
 void resident_cta_slots(const void *func, int threads, size_t smem, int per_sm, uint32_t *out);
 cudaError_t launch_int4_qkv(const Int4Args &a, cudaStream_t s);
 bool int4_tc_supported(uint32_t nq, uint32_t nkv, uint32_t group);

@@ -16,7 +16,9 @@
 //                      N = NTOK tokens, K = 32 per instruction, four per
 //                      block) and commits each stage back to its `empty`
 //                      mbarrier.
-//   warp 2 (fused)   : quantises the bf16 activations of each K block
+//   warp 2 (Block128): stages sa[m, kb] * sw[kb] for each K block in shared
+//                      memory for the epilogue (one buffer per accumulator).
+//   warp 2 (fused)   : instead quantises the bf16 activations of each K block
 //                      (absmax/448 per token and 128-group, RNE satfinite E4M3,
 //                      the arithmetic of the act-quant kernel) straight into
 //                      the stage's swizzled operand and the block's scales into
@@ -50,7 +52,31 @@
 namespace cg = cooperative_groups;
 
 #ifndef QDL_TC_STAGE_BYTES
-#define QDL_TC_STAGE_BYTES (64 * 1024)
+#define QDL_TC_STAGE_BYTES (72 * 1024)
+#endif
+// ... and for the wide variants (NTOK >= QDL_TC_BIG_NTOK) that run one CTA per SM
+#ifndef QDL_TC_STAGE_BYTES_BIG
+#define QDL_TC_STAGE_BYTES_BIG (72 * 1024)
+#endif
+#ifndef QDL_TC_BIG_NTOK
+#define QDL_TC_BIG_NTOK 128
+#endif
+// Block128 epilogue: accumulator columns read from tensor memory per wait
+// (loads in flight), and register caps that let several CTAs share an SM
+#ifndef QDL_TC_INFLIGHT_SMALL
+#define QDL_TC_INFLIGHT_SMALL 32  // NTOK <= 64
+#endif
+#ifndef QDL_TC_INFLIGHT_128
+#define QDL_TC_INFLIGHT_128 64
+#endif
+#ifndef QDL_TC_INFLIGHT_256
+#define QDL_TC_INFLIGHT_256 16
+#endif
+#ifndef QDL_TC_REGS_32
+#define QDL_TC_REGS_32 96  // 3 CTAs of 7 warps
+#endif
+#ifndef QDL_TC_REGS_64
+#define QDL_TC_REGS_64 144  // 2 CTAs of 7 warps
 #endif
 #ifndef QDL_TC_BIGBOX
 #define QDL_TC_BIGBOX 1
@@ -77,24 +103,34 @@ struct Tc {
     static constexpr uint32_t kABytes = NTOK * 128;
     static constexpr uint32_t kStage = kWBytes + kABytes;  // multiple of 1024 (NTOK % 8 == 0)
     // pipeline depth: as many stages as fit a per-CTA budget, at least 3
-    static constexpr int kStages = (QDL_TC_STAGE_BYTES / kStage) < 3 ? 3 : (QDL_TC_STAGE_BYTES / kStage);
+    static constexpr uint32_t kBudget = NTOK >= QDL_TC_BIG_NTOK ? QDL_TC_STAGE_BYTES_BIG : QDL_TC_STAGE_BYTES;
+    static constexpr int kStages = (kBudget / kStage) < 3 ? 3 : (kBudget / kStage);
     // Block128 accumulator buffers: the MMA may run kAcc-1 blocks ahead of
     // the epilogue that folds each block's scales
     static constexpr int kAcc = kBlock ? (NTOK <= 64 ? 4 : 2) : 1;
     static constexpr uint32_t kBarOff = kStages * kStage;
-    static constexpr uint32_t kScaleOff = kBarOff + 512;  // fused: [kAcc][NTOK] block scales
-    static constexpr uint32_t kBytes = kScaleOff + (kFused ? kAcc * NTOK * 4 : 0);
+    static constexpr uint32_t kScaleOff = kBarOff + 512;  // Block128: [kAcc][NTOK] block scales
+    static constexpr uint32_t kBytes = kScaleOff + (kBlock ? kAcc * NTOK * 4 : 0);
     static constexpr uint32_t kAlloc = kBytes + 1024;
-    static constexpr int kEpiBase = kFused ? 3 : 2;                          // first epilogue warp
+    static constexpr int kEpiBase = kBlock ? 3 : 2;                          // first epilogue warp
     static constexpr int kEpi = kBlock ? (NTOK <= 64 ? 4 : NTOK / 16) : 4;  // epilogue warps
     static constexpr int kCpt = kBlock ? NTOK * 4 / kEpi : 16;               // columns per epilogue thread
     static constexpr int kThreads = (kEpiBase + kEpi) * 32;
+    // columns per tensor-memory wait in the Block128 epilogue
+    static constexpr int kInFlight =
+        kCpt < (NTOK <= 64 ? QDL_TC_INFLIGHT_SMALL : NTOK == 128 ? QDL_TC_INFLIGHT_128 : QDL_TC_INFLIGHT_256)
+            ? kCpt
+            : (NTOK <= 64 ? QDL_TC_INFLIGHT_SMALL : NTOK == 128 ? QDL_TC_INFLIGHT_128 : QDL_TC_INFLIGHT_256);
+    // register cap per thread, so that several CTAs fit an SM (255: none)
+    static constexpr int kMaxRegs = !kBlock || kFused ? 255 : NTOK == 32 ? QDL_TC_REGS_32 : NTOK == 64 ? QDL_TC_REGS_64 : 255;
     static constexpr uint32_t kTmemCols = pow2_at_least(kAcc * NTOK);
     static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
-    static_assert(kTileRows * NTOK * 4 <= kBarOff, "reduction buffer must fit in the stage area");
+    static_assert(kTileRows * NTOK * 4 <= kBarOff, "split-K partials must fit in the stage ring");
     static_assert(kTmemCols <= 512, "tensor memory");
     static_assert((3 * kStages + 3 * kAcc + 1) * 8 + 8 <= 512, "barrier area");
+    static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
     static_assert(!kFused || (kBlock && NTOK == 16), "fused quantisation: Block128, up to 16 rows");
+    static_assert(kInFlight % 16 == 0 && kCpt % kInFlight == 0, "epilogue load groups");
 };
 
 // ---------------------------------------------------------------- tcgen05 / PDL PTX
@@ -163,7 +199,7 @@ __device__ __forceinline__ float quant_operand(float v, float scale) {
 // ---------------------------------------------------------------- kernel
 
 template <int NTOK, bool kBlock, bool kFused>
-__global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1)
+__global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnreg__((Tc<NTOK, kBlock, kFused>::kMaxRegs))
     w8a8_gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                         const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_b0,
                         const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_b2,
@@ -180,8 +216,8 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1)
     uint64_t *done = scal + C::kAcc;      // all MMAs complete
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     volatile uint32_t *abort_flag = tmem_slot + 1;
-    float *sbuf = reinterpret_cast<float *>(smem + C::kScaleOff);  // fused: [kAcc][NTOK]
-    float *red = reinterpret_cast<float *>(smem);                   // [NTOK][128], reuses the stages at the end
+    float *sbuf = reinterpret_cast<float *>(smem + C::kScaleOff);  // Block128: [kAcc][NTOK] sa * sw
+    float *red = reinterpret_cast<float *>(smem);  // split-K partials [NTOK][128], reuse the ring at the end
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t tile_row0 = blockIdx.x * kTileRows;
@@ -237,6 +273,10 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1)
     // true when the rows tile_row0 .. tile_row0+127 that exist all belong to that segment
     const bool tile_single = tile_row0 + kTileRows <= seg_end || seg_end == a.n;
 
+    // weight scale of this tile for K block kb (Block128 tiles lie in one segment)
+    auto tile_sw = [&](uint32_t kb) -> float {
+        return tile_row0 < a.n ? __ldg(tile_scale + (size_t)(tile_lrow0 >> 7) * a.kb + kb) : 0.0f;
+    };
     uint32_t issued = 0;
     constexpr int kCpt = C::kCpt;
     float total[kBlock ? kCpt : 1];
@@ -323,6 +363,39 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1)
             }
             tc_commit(done);  // completes once every MMA issued above has
         }
+    } else if (kBlock && !kFused && warp == 2) {
+        // ------------------------------------------------------------ scale warp
+        // sa[token, kb] * sw[tile, kb] of each K block into sbuf[b], one block
+        // ahead in registers; lane l covers tokens l, l + 32, ...
+        constexpr int kPer = (NTOK + 31) / 32;
+        grid_dep_wait();  // activation scales come from the previous kernel
+        auto load = [&](uint32_t it, float (&v)[kPer]) {
+            const uint32_t kb = kb0 + it;
+            const float sw = (it < niter && tile_row0 < a.n)
+                                 ? __ldg(tile_scale + (size_t)(tile_lrow0 >> 7) * a.kb + kb)
+                                 : 0.0f;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const uint32_t tok = 32 * j + lane;
+                v[j] = (it < niter && tok < a.m && tok < (uint32_t)NTOK) ? __ldg(a.sa + (size_t)tok * a.kb + kb) * sw
+                                                                      : 0.0f;
+            }
+        };
+        float next[kPer];
+        load(0, next);
+        for (uint32_t it = 0; it < niter; ++it) {
+            const uint32_t b = it % C::kAcc;
+            float cur[kPer];
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) cur[j] = next[j];
+            load(it + 1, next);
+            wait(&acce[b], ((it / C::kAcc) & 1) ^ 1, 64);  // the epilogue is done with sbuf[b]
+#pragma unroll
+            for (int j = 0; j < kPer; ++j)
+                if (32 * j + lane < (uint32_t)NTOK) sbuf[b * NTOK + 32 * j + lane] = cur[j];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&scal[b]);
+        }
     } else if (kFused && warp == 2) {
         // ------------------------------------------------------------ quantiser
         // 16 lanes per token row: lane h = lane & 15 holds elements 8h .. 8h+7
@@ -369,7 +442,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1)
                 const uint32_t addr = sbase + slot * C::kStage + kWBytes + r * 128 +
                                       ((((uint32_t)h >> 1) ^ (r & 7)) << 4) + ((uint32_t)h & 1) * 8;
                 sts64(addr, lo, hi);
-                if (h == 0) sbuf[b * NTOK + r] = r < a.m ? scale : 0.0f;
+                if (h == 0) sbuf[b * NTOK + r] = r < a.m ? scale * tile_sw(kb) : 0.0f;
                 if (blockIdx.x == 0 && r < a.m) {  // tile-0 CTAs also fill the caller's scratch
                     *reinterpret_cast<uint2 *>(a.q_out + (size_t)r * a.k + kb * 128 + 8 * h) = make_uint2(lo, hi);
                     if (h == 0) a.sa_out[(size_t)r * a.kb + kb] = scale;
@@ -390,33 +463,31 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1)
         const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16);
         if (!kFused) grid_dep_wait();  // activation scales come from the previous kernel
         if constexpr (kBlock) {
-            constexpr int kSRegs = (kCpt + 31) / 32;  // scale registers per lane
             for (uint32_t it = 0; it < niter; ++it) {
-                const uint32_t b = it % C::kAcc, kb = kb0 + it;
-                // lane l holds sa[token cgrp*kCpt + 32r + l, kb] * sw; shuffled out below
-                const float sw = tile_row0 < a.n ? __ldg(tile_scale + (size_t)(tile_lrow0 >> 7) * a.kb + kb) : 0.0f;
-                float sreg[kSRegs];
-                if (kFused) wait(&scal[b], (it / C::kAcc) & 1, 32);
-#pragma unroll
-                for (int r = 0; r < kSRegs; ++r) {
-                    const uint32_t tok = cgrp * kCpt + 32 * r + lane;
-                    float sa = 0.0f;
-                    if (32 * r + lane < (uint32_t)kCpt && tok < a.m)
-                        sa = kFused ? sbuf[b * NTOK + tok] : __ldg(a.sa + (size_t)tok * a.kb + kb);
-                    sreg[r] = sa * sw;
-                }
+                const uint32_t b = it % C::kAcc;
+                wait(&scal[b], (it / C::kAcc) & 1, 32);  // sa * sw of this block
                 wait(&accf[b], (it / C::kAcc) & 1, 16);
                 tc_fence_after();
+                // kInFlight columns per wait: several loads in flight hide the
+                // tensor-memory latency
+                constexpr int kF = C::kInFlight;
 #pragma unroll
-                for (int c = 0; c < kCpt / 16; ++c) {
-                    float v[16];
-                    tc_ld16(taddr + b * NTOK + cgrp * kCpt + 16 * c, v);
+                for (int g = 0; g < kCpt / kF; ++g) {
+                    float v[kF];
+                    const uint32_t col = cgrp * kCpt + kF * g;
+#pragma unroll
+                    for (int c = 0; c < kF / 16; ++c)
+                        tc_ld16(taddr + b * NTOK + col + 16 * c, *reinterpret_cast<float(*)[16]>(v + 16 * c));
                     tc_wait_ld();
+                    const float4 *sp = reinterpret_cast<const float4 *>(sbuf + b * NTOK + col);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int j = 16 * c + i;
-                        const float s = __shfl_sync(0xffffffffu, sreg[j >> 5], j & 31);
-                        total[j] = fmaf(v[i], s, total[j]);
+                    for (int q4 = 0; q4 < kF / 4; ++q4) {
+                        const float4 s4 = sp[q4];  // the same address in every lane: a broadcast
+                        float *t = total + kF * g + 4 * q4;
+                        t[0] = fmaf(v[4 * q4 + 0], s4.x, t[0]);
+                        t[1] = fmaf(v[4 * q4 + 1], s4.y, t[1]);
+                        t[2] = fmaf(v[4 * q4 + 2], s4.z, t[2]);
+                        t[3] = fmaf(v[4 * q4 + 3], s4.w, t[3]);
                     }
                 }
                 tc_fence_before();
@@ -504,6 +575,8 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1)
     }
 
     if (split > 1) {
+        // rank r adds rows 128r/split .. 128(r+1)/split - 1 of every rank's
+        // partials, in rank order
         cg::cluster_group cluster = cg::this_cluster();
         cluster.sync();
         const uint32_t r_lo = (kTileRows * sidx) / split, r_hi = (kTileRows * (sidx + 1)) / split;
@@ -522,7 +595,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1)
             for (int rk = 0; rk < 8; ++rk) sum += v[rk];  // rank order; absent ranks add +0
             store(tok, tile_row0 + lr, sum);
         }
-        cluster.sync();
+        cluster.sync();  // no rank leaves while others still read its partials
     }
 
     // ---------------------------------------------------------------- free the tensor memory
@@ -536,6 +609,10 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
+
+// Cluster reduction of one split CTA, in K-block units: its partials grow
+// with the token count (measured: one K block of time per 4 tokens).
+constexpr double tc_reduce_cost(int ntok) { return ntok / 4.0; }
 
 template <int NTOK, bool kBlock, bool kFused>
 const uint32_t *cta_slots_tc() {
@@ -561,7 +638,7 @@ template <int NTOK, bool kBlock, bool kFused>
 cudaError_t launch_tc_variant(const W8A8Args &a, const CUtensorMap (&maps)[7], cudaStream_t s) {
     using C = Tc<NTOK, kBlock, kFused>;
     const uint32_t tiles = (a.n + kTileRows - 1) / kTileRows;
-    const uint32_t split = choose_split_k(tiles, a.kb, cta_slots_tc<NTOK, kBlock, kFused>());
+    const uint32_t split = choose_split_k(tiles, a.kb, cta_slots_tc<NTOK, kBlock, kFused>(), tc_reduce_cost(NTOK));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tiles, split, 1);
     cfg.blockDim = dim3(C::kThreads, 1, 1);
@@ -587,7 +664,7 @@ void plan_tc_variant(const W8A8Args &a, PlanInfo *p) {
     p->kernel = 0;
     p->mma_n = NTOK;
     p->tiles = (a.n + kTileRows - 1) / kTileRows;
-    p->split = choose_split_k(p->tiles, a.kb, slots);
+    p->split = choose_split_k(p->tiles, a.kb, slots, tc_reduce_cost(NTOK));
     p->stages = C::kStages;
     p->threads = C::kThreads;
     p->smem = C::kAlloc;

@@ -338,7 +338,7 @@ const uint32_t *cta_slots() {
 // fill and drain.  slots[s-1] CTAs of clusters of s can be resident at once.
 // Choose s in 1..8 that minimises waves x per-CTA work, with a small charge
 // for the cluster reduction.
-uint32_t choose_split_k(uint32_t tiles, uint32_t kb, const uint32_t *slots) {
+uint32_t choose_split_k(uint32_t tiles, uint32_t kb, const uint32_t *slots, double reduce_cost) {
 #ifdef QDL_TUNE_SPLIT
     if (QDL_TUNE_SPLIT > 0) return QDL_TUNE_SPLIT < kb ? QDL_TUNE_SPLIT : kb;
 #endif
@@ -348,7 +348,8 @@ uint32_t choose_split_k(uint32_t tiles, uint32_t kb, const uint32_t *slots) {
         const uint32_t fit = slots[s - 1] >= s ? slots[s - 1] : s;
         const uint32_t units = tiles * s;
         const uint32_t waves = (units + fit - 1) / fit;
-        const double cost = (double)waves * (((kb + s - 1) / s) + 2.0) * (1.0 + 0.03 * (s - 1));
+        const double cost =
+            (double)waves * (((kb + s - 1) / s) + 2.0 + (s > 1 ? reduce_cost : 0.0)) * (1.0 + 0.03 * (s - 1));
         if (cost < best_cost) {
             best_cost = cost;
             best = s;
@@ -390,7 +391,7 @@ namespace {
 template <int NT, bool kBlock>
 cudaError_t launch_variant(const W8A8Args &a, const CUtensorMap (&maps)[4], cudaStream_t s) {
     const uint32_t tiles = (a.n + kRowsPerCta - 1) / kRowsPerCta;
-    const uint32_t split = choose_split_k(tiles, a.kb, cta_slots<NT, kBlock>());
+    const uint32_t split = choose_split_k(tiles, a.kb, cta_slots<NT, kBlock>(), 0.0);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tiles, split, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -465,7 +466,7 @@ cudaError_t plan_w8a8_gemv_tma(const W8A8Args &a, int format, PlanInfo *p) {
     p->kernel = 1;
     p->mma_n = a.m <= 8 ? 8 : 16;
     p->tiles = (a.n + kRowsPerCta - 1) / kRowsPerCta;
-    p->split = choose_split_k(p->tiles, a.kb, slots);
+    p->split = choose_split_k(p->tiles, a.kb, slots, 0.0);
     p->stages = kStages;
     p->threads = kThreads;
     p->smem = a.m <= 8 ? Layout<1>::kAlloc : Layout<2>::kAlloc;
