@@ -175,13 +175,15 @@ QDL_API qdl_status qdl_w8a8_proj_silu(const qdl_w8a8_weight *w, const void *gate
  *            nq, nkv multiples of 16 enables 8-byte weight loads).
  *   sc[p], zr[p] : device f32 [k/group, n], 16-byte aligned.
  *   out[p] : device f32 [m, n], 4-byte aligned.
- * The kernel multiplies x rounded to f16 with exact nibbles on tensor cores
- * and applies zeros and scales per group in f32 (error within 2^-11 of
- * sum |x w|).  Checks: m >= 1; k >= 1; group > 0, group % 16 == 0,
- * k % group == 0; nq, nkv > 0 and multiples of 8; no NULL pointer;
- * alignments above.  With group 128 and nq, nkv multiples of 32 the
- * tcgen05 kernel streams the weights once per 32 rows; other shapes take an
- * mma.sync kernel, once per 16 rows. */
+ * With nq, nkv multiples of 32, up to 2 rows (up to 4 when group != 128)
+ * take one CUDA-core pass that multiplies f32 x with exact nibbles in f32 and
+ * applies zeros and scales per group.  Otherwise the tensor cores multiply x
+ * rounded to f16 with exact nibbles and apply zeros and scales per group in
+ * f32 (error within 2^-11 of sum |x w|): with group 128 and nq, nkv multiples
+ * of 32 the tcgen05 kernel streams the weights once per 32 rows, other shapes
+ * an mma.sync kernel once per 16 rows.  Checks: m >= 1; k >= 1; group > 0,
+ * group % 16 == 0, k % group == 0; nq, nkv > 0 and multiples of 8; no NULL
+ * pointer; alignments above. */
 QDL_API qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq, uint32_t nkv,
                              uint32_t group, const uint32_t *const *qw, const float *const *sc,
                              const float *const *zr, float *const *out, void *stream);

@@ -457,55 +457,6 @@ __global__ void __launch_bounds__(kThreadsI4, 1)
 
 // ---------------------------------------------------------------- host side
 
-cudaError_t make_tmap_words(CUtensorMap *map, const void *base, uint64_t words, uint64_t rows) {
-    // packed words [rows, words] u32, box 32 words x 64 rows, 128-byte swizzle
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    if (fn == nullptr) return cudaErrorNotSupported;
-    cuuint64_t gdim[2] = {words, rows};
-    cuuint64_t gstride[1] = {words * 4};
-    cuuint32_t box[2] = {32, (cuuint32_t)kStageK};
-    cuuint32_t estride[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), gdim, gstride, box, estride,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-// Resident CTAs for each cluster size (one CTA per SM: the cluster
-// occupancy query accounts for how clusters pack into GPCs).
-cudaError_t make_tmap_f32(CUtensorMap *map, const float *x, uint64_t k, uint64_t rows, uint32_t box_rows) {
-    // x [rows, k] f32, box 32 values x box_rows rows, 128-byte swizzle; rows
-    // past the end read as zero
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    if (fn == nullptr) return cudaErrorNotSupported;
-    cuuint64_t gdim[2] = {k, rows};
-    cuuint64_t gstride[1] = {k * 4};
-    cuuint32_t box[2] = {32, box_rows};
-    cuuint32_t estride[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(x), gdim, gstride, box, estride,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <int NTOK>
 const uint32_t *cluster_fit() {
     static std::mutex mu;
@@ -546,6 +497,55 @@ cudaError_t launch_i4(const Int4Args &a, const CUtensorMap (&maps)[4], cudaStrea
 
 }  // namespace
 
+cudaError_t make_tmap_words(CUtensorMap *map, const void *base, uint64_t words, uint64_t rows, uint32_t box_rows) {
+    // packed words [rows, words] u32, box 32 words x box_rows rows, 128-byte swizzle
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (fn == nullptr) return cudaErrorNotSupported;
+    cuuint64_t gdim[2] = {words, rows};
+    cuuint64_t gstride[1] = {words * 4};
+    cuuint32_t box[2] = {32, box_rows};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), gdim, gstride, box, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_tmap_f32(CUtensorMap *map, const float *x, uint64_t k, uint64_t rows, uint32_t box_rows) {
+    // x [rows, k] f32, box 32 values x box_rows rows, 128-byte swizzle; rows
+    // past the end read as zero
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (fn == nullptr) return cudaErrorNotSupported;
+    cuuint64_t gdim[2] = {k, rows};
+    cuuint64_t gstride[1] = {k * 4};
+    cuuint32_t box[2] = {32, box_rows};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(x), gdim, gstride, box, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+
+
 bool int4_tc_supported(uint32_t nq, uint32_t nkv, uint32_t group) {
     return group == (uint32_t)kGroupK && nq % 32 == 0 && nkv % 32 == 0;
 }
@@ -556,7 +556,7 @@ cudaError_t launch_int4_qkv_tc(const Int4Args &a, cudaStream_t s) {
     const uint32_t ns[3] = {a.nq, a.nkv, a.nkv};
     const uint32_t *qw[3] = {a.qw0, a.qw1, a.qw2};
     for (int p = 0; p < 3; ++p) {
-        cudaError_t e = make_tmap_words(&maps[p], qw[p], ns[p] / 8, a.k);
+        cudaError_t e = make_tmap_words(&maps[p], qw[p], ns[p] / 8, a.k, kStageK);
         if (e != cudaSuccess) return e;
     }
     const uint32_t ntok = a.m <= 16 ? 16 : 32;

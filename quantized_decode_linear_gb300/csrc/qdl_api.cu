@@ -341,8 +341,20 @@ qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq
     a.tiles_kv = (nkv + 127) / 128;
     a.vec2 = vec2;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // tensor-core path (group 128, widths multiples of 32): 32 rows per pass;
-    // otherwise the mma.sync kernel, 16 rows per pass
+    // widths multiples of 32: the CUDA-core kernel for up to 2 rows, and for
+    // 3-4 rows where the tcgen05 kernel does not apply; more rows: the tcgen05
+    // kernel (group 128, widths multiples of 32), 32 rows per pass, otherwise
+    // the mma.sync kernel, 16 rows per pass
+    if (int4_cc_supported(nq, nkv) && (m <= 2 || (m <= 4 && !int4_tc_supported(nq, nkv, group)))) {
+        a.x = x;
+        a.out0 = out[0];
+        a.out1 = out[1];
+        a.out2 = out[2];
+        a.m = m;
+        cudaError_t e = launch_int4_qkv_cc(a, s);
+        if (e != cudaSuccess) return cuda_fail(who, e);
+        return ok();
+    }
     const bool tc = int4_tc_supported(nq, nkv, group);
     const uint32_t chunk = tc ? 32 : 16;
     for (uint32_t done = 0; done < m; done += chunk) {
@@ -455,6 +467,8 @@ qdl_status qdl_check_device_fault(void *stream) {
     if ((e = read_and_clear_tc_fault(&word_tc)) != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
     word |= word_tc;
     if ((e = read_and_clear_int4_fault(&word_tc)) != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
+    word |= word_tc;
+    if ((e = read_and_clear_int4cc_fault(&word_tc)) != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
     word |= word_tc;
     if (word != 0)
         return fail(QDL_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up (fault word 0x%x: 1 = producer, 2/8 = consumer or MMA, 4/16/32 = accumulator)",

@@ -94,6 +94,9 @@ cudaError_t launch_int4_qkv(const Int4Args &a, cudaStream_t s);
 bool int4_tc_supported(uint32_t nq, uint32_t nkv, uint32_t group);
 cudaError_t launch_int4_qkv_tc(const Int4Args &a, cudaStream_t s);  // up to 32 token rows
 cudaError_t read_and_clear_int4_fault(uint32_t *value);
+bool int4_cc_supported(uint32_t nq, uint32_t nkv);                  // widths multiples of 32
+cudaError_t launch_int4_qkv_cc(const Int4Args &a, cudaStream_t s);  // 1..4 token rows, CUDA cores
+cudaError_t read_and_clear_int4cc_fault(uint32_t *value);
 
 int device_sm_count();  // of the current device, cached
 

@@ -15,6 +15,10 @@ namespace qdl {
 // swizzle (box_cols must be 128).  Returns cudaSuccess or an error.
 cudaError_t make_tmap_u8(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t stride,
                          uint32_t box_cols, uint32_t box_rows);
+// packed AWQ words [rows, words] u32, box 32 words x box_rows rows, 128-byte swizzle
+cudaError_t make_tmap_words(CUtensorMap *map, const void *base, uint64_t words, uint64_t rows, uint32_t box_rows);
+// x [rows, k] f32, box 32 values x box_rows rows, 128-byte swizzle; rows past the end read as zero
+cudaError_t make_tmap_f32(CUtensorMap *map, const float *x, uint64_t k, uint64_t rows, uint32_t box_rows);
 
 // CTAs of a kernel that can be resident on one SM at once.
 int resident_ctas(const void *func, int threads, size_t smem, int tmem_cols);

@@ -37,14 +37,31 @@ def test_int4_small(m, k, nq, nkv, group):
         check_close(outs[p], ref[p], bound[p], what=f"proj {p}")
 
 
-@pytest.mark.parametrize("m", [1, 3, 16, 17, 32, 33, 70])
+@pytest.mark.parametrize("m", [9, 16, 17, 32, 33, 70])
 @pytest.mark.parametrize("k,nq,nkv", [(128, 96, 32), (256, 128, 128), (2048, 640, 160), (1024, 4096, 1024)])
 def test_int4_tensor_core_path(m, k, nq, nkv):
-    """group 128 and widths multiple of 32: the tcgen05 kernel (ragged last
-    tiles, several passes of 32 rows)"""
+    """more than 8 rows, group 128 and widths multiple of 32: the tcgen05
+    kernel (ragged last tiles, several passes of 32 rows)"""
     group = 128
     x = syn.normal_f32((m, k), seed=2 * m + k)
     ws = [syn.int4_awq(k, n, group, seed=p + 3 * nq) for p, n in enumerate((nq, nkv, nkv))]
+    outs = _run(x, nq, nkv, group, ws)
+    ref, bound = oracle.int4_qkv(x, nq, nkv, group, [w[0] for w in ws], [w[1] for w in ws],
+                                 [w[2] for w in ws])
+    for p in range(3):
+        check_close(outs[p], ref[p], bound[p], what=f"proj {p}")
+
+
+@pytest.mark.parametrize("m", [1, 2, 3, 4])
+@pytest.mark.parametrize("k,nq,nkv,group", [(128, 32, 32, 128), (1040, 96, 32, 16), (512, 288, 64, 32),
+                                            (4096, 512, 256, 64), (2048, 640, 160, 128), (8192, 32, 64, 128)])
+def test_int4_cuda_core_path(m, k, nq, nkv, group):
+    """widths multiple of 32 with 1-2 rows (1-4 rows for group != 128): the
+    CUDA-core kernel (ragged 256-column tiles, K not a multiple of its 64-row
+    stage, groups 16..128, split-K clusters up to 8); the other cases here
+    cover the tcgen05 kernel's small-row passes"""
+    x = syn.normal_f32((m, k), seed=5 * m + k)
+    ws = [syn.int4_awq(k, n, group, seed=p + 7 * nq) for p, n in enumerate((nq, nkv, nkv))]
     outs = _run(x, nq, nkv, group, ws)
     ref, bound = oracle.int4_qkv(x, nq, nkv, group, [w[0] for w in ws], [w[1] for w in ws],
                                  [w[2] for w in ws])
