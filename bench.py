@@ -36,7 +36,9 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic per launch of the dominant kernel from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and rows;
 # valid only while the kernel source hash matches.  Source: profiles/.
-TRAFFIC = {}
+TRAFFIC = {
+    "w8a8_block128_qkv_m8_k4096_n4096+1024+1024@8": {"bytes": 25239296 + 0, "src": "751436846faf577d"},
+}
 
 
 def _rank_world():
@@ -92,8 +94,10 @@ class W8A8Case:
         self.step_bytes = n * K + w_scales + x_bytes + rows * n * 4
         # of one GEMV launch: weights + scales + e4m3 activations + act scales + output
         self.gemv_bytes = n * K + w_scales + rows * K + self.s.numel() * 4 + rows * n * 4
-        self.gemv_launches = math.ceil(rows / 16)
-        self.launches_per_step = 1 + self.gemv_launches
+        self.gemv_launches = 1  # one tcgen05 launch covers up to 256 rows
+        self.launches_per_step = 1 + self.gemv_launches  # activation quantiser + GEMV
+        self.kernel = "w8a8_gemm_tc_kernel"
+        self.kernel_src = ["w8a8_gemm_tc.cu"]
 
     def step(self, i):
         w = self.weights[i % self.copies]
@@ -142,7 +146,13 @@ class Int4Case:
         n_tot = wl.nq + 2 * wl.nkv
         self.step_bytes = self.weight_bytes + x.nbytes + rows * n_tot * 4
         self.gemv_bytes = self.step_bytes
-        self.gemv_launches = math.ceil(rows / 16)
+        # the library's dispatch for widths multiple of 32 and group 128: the
+        # CUDA-core kernel for up to 2 rows, else tcgen05 passes of 32 rows
+        if rows <= 2:
+            self.gemv_launches, self.kernel, self.kernel_src = 1, "int4_qkv_cc_kernel", ["int4_qkv_cc.cu"]
+        else:
+            self.gemv_launches = math.ceil(rows / 32)
+            self.kernel, self.kernel_src = "int4_qkv_tc_kernel", ["int4_qkv_tc.cu"]
         self.launches_per_step = self.gemv_launches
 
     def step(self, i):
@@ -403,14 +413,31 @@ def run_gpu(args, rank, world, local_rank):
         if dist:
             dist.barrier()
 
-    # end to end through the public API with host buffers (no graphs)
-    e2e_steps = min(steps, 2000)
+    # end to end through the public API with host buffers: every step copies
+    # its inputs from pinned host memory, makes the library call and copies
+    # the result back; replayed from graphs like the device-only steps, and
+    # also timed eagerly (one Python call per step) for reference
+    e2e_graphs = graphs_for(case.e2e_step)
+    for g in e2e_graphs[0] + ([e2e_graphs[1]] if e2e_graphs[1] is not None else []):
+        g.replay()
+    torch.cuda.synchronize()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    replay(e2e_graphs)
+    x1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = x0.elapsed_time(x1) / 1e3
+    if dist:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    eager_steps = min(steps, 2000)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for i in range(e2e_steps):
+    for i in range(eager_steps):
         case.e2e_step(i)
     torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t0
+    eager_s = time.perf_counter() - t0
     h2d, d2h = case.e2e_bytes()
 
     peak, peak_kind = _peaks()
@@ -418,9 +445,8 @@ def run_gpu(args, rank, world, local_rank):
     dom_launch_s = dom_ms / 1e3 / (steps * case.gemv_launches)
     achieved = case.gemv_bytes / case.gemv_launches / dom_launch_s / 1e9
     key = f"{wl.name}@{rows}"
-    src = ["w8a8_gemv_mma.cu"] if Case is W8A8Case else ["int4_qkv.cu"]
     tr = TRAFFIC.get(key)
-    traffic = tr["bytes"] if tr and tr.get("src") == _src_hash(src) else None
+    traffic = tr["bytes"] if tr and tr.get("src") == _src_hash(case.kernel_src) else None
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": warm, "ms_per_step": ms / steps, "us_per_call": ms / steps * 1e3,
@@ -429,12 +455,13 @@ def run_gpu(args, rank, world, local_rank):
         "config": dict(case.describe(), parallelism="replicas" if world > 1 else "single"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "w8a8_gemv_mma_kernel" if Case is W8A8Case else "int4_qkv_kernel",
+                     "kernel": case.kernel,
                      "peak_source": f"{peak_kind} hbm_gbs", "kernel_us": dom_launch_s * 1e6},
         "hbm_frac_step": value / world / peak,
-        "e2e": {"value": case.step_bytes * e2e_steps / e2e_s / 1e9, "unit": "GB/s",
+        "e2e": {"value": case.step_bytes * steps * world / e2e_s / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "us_per_call": e2e_s / e2e_steps * 1e6},
+                "us_per_call": e2e_s / steps * 1e6, "method": "graphs of copy-in, call, copy-out",
+                "eager_us_per_call": eager_s / eager_steps * 1e6},
         "gpu_launches": steps * case.launches_per_step,
         "clocks": clk,
     }
