@@ -12,12 +12,16 @@
 // Two kernels:
 //   - per 128-group (Block128): one warp per group, 4 elements per lane,
 //     absmax by warp shuffles; the grid covers rows x k/128 groups.
-//   - per token row (PerRow): one CTA per row, each thread keeps its
-//     elements in registers (UPT 16-byte units of 8 values), absmax by warp
-//     shuffles plus a shared-memory step, then quantises from registers.
+//   - per token row (PerRow): each row is split over a cluster of up to 8
+//     CTAs; each thread keeps its elements in registers (UPT 16-byte units of
+//     8 values), absmax by warp shuffles, shared memory and then distributed
+//     shared memory across the cluster, then quantises from registers.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include "qdl_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace qdl {
 namespace {
@@ -79,12 +83,21 @@ __global__ void __launch_bounds__(256) act_quant_g128_kernel(ActQuantArgs a) {
 
 // ---------------------------------------------------------------- PerRow
 
+// One row is split over a cluster of C CTAs (blockIdx.x = rank): each CTA
+// keeps its part of the row in registers (UPT 16-byte units of 8 values per
+// thread), reduces its absmax by warp shuffles and shared memory, and the
+// cluster combines the C partial maxima through distributed shared memory
+// (max is exact and order-free, so every rank gets the same absmax).
 template <bool kSilu, int UPT>
 __global__ void __launch_bounds__(1024) act_quant_row_kernel(ActQuantArgs a) {
     __shared__ float warp_max[32];
+    __shared__ float cta_max;
     dependent_launch_prologue();
-    const uint32_t row = blockIdx.x;
+    const uint32_t row = blockIdx.y;
+    const uint32_t nrank = gridDim.x, rank = blockIdx.x;
     const uint32_t units = a.k / 8;
+    const uint32_t per = (units + nrank - 1) / nrank;
+    const uint32_t u0 = rank * per, u1 = u0 + per < units ? u0 + per : units;
     const uint16_t *xa = a.a + (size_t)row * a.lda;
     const uint16_t *xb = kSilu ? a.b + (size_t)row * a.ldb : nullptr;
 
@@ -92,8 +105,8 @@ __global__ void __launch_bounds__(1024) act_quant_row_kernel(ActQuantArgs a) {
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < UPT; ++i) {
-        const uint32_t u = threadIdx.x + i * blockDim.x;
-        if (u < units) {
+        const uint32_t u = u0 + threadIdx.x + i * blockDim.x;
+        if (u < u1) {
             const uint4 pa = *reinterpret_cast<const uint4 *>(xa + u * 8);
             uint4 pb = make_uint4(0, 0, 0, 0);
             if constexpr (kSilu) pb = *reinterpret_cast<const uint4 *>(xb + u * 8);
@@ -114,16 +127,34 @@ __global__ void __launch_bounds__(1024) act_quant_row_kernel(ActQuantArgs a) {
     const uint32_t nwarps = blockDim.x >> 5;
     if (lane == 0) warp_max[warp] = amax;
     __syncthreads();
-    amax = lane < nwarps ? warp_max[lane] : 0.0f;
+    if (warp == 0) {
+        amax = lane < nwarps ? warp_max[lane] : 0.0f;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const float scale = __fdiv_rn(amax, 448.0f);
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if (lane == 0) cta_max = amax;
+    }
+    if (nrank > 1) {
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();  // every rank's cta_max is written
+        if (warp == 0) {
+            float m = lane < nrank ? *cluster.map_shared_rank(&cta_max, lane) : 0.0f;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            if (lane == 0) warp_max[0] = m;
+        }
+        cluster.sync();  // no rank leaves or overwrites while others still read its cta_max
+    } else {
+        __syncthreads();
+        if (threadIdx.x == 0) warp_max[0] = cta_max;
+    }
+    __syncthreads();
+    const float scale = __fdiv_rn(warp_max[0], 448.0f);
 
     uint8_t *qrow = a.q + (size_t)row * a.k;
 #pragma unroll
     for (int i = 0; i < UPT; ++i) {
-        const uint32_t u = threadIdx.x + i * blockDim.x;
-        if (u < units) {
+        const uint32_t u = u0 + threadIdx.x + i * blockDim.x;
+        if (u < u1) {
             uint32_t w[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -133,33 +164,54 @@ __global__ void __launch_bounds__(1024) act_quant_row_kernel(ActQuantArgs a) {
                 make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
         }
     }
-    if (threadIdx.x == 0) a.s[row] = scale;
+    if (rank == 0 && threadIdx.x == 0) a.s[row] = scale;
 }
 
 template <typename Kernel>
-cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, cudaStream_t s, const ActQuantArgs &a) {
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, cudaStream_t s, const ActQuantArgs &a,
+                       uint32_t cluster_x = 1) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (QDL_TUNE_PDL) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = QDL_TUNE_PDL ? 1 : 0;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
+// Ranks per row: enough CTAs to cover the SMs about twice (up to 8, the
+// portable cluster size), but at least 256 units of 8 values per rank; short
+// rows stay in one CTA, where the cluster barriers would cost more than the
+// split saves.
 template <bool kSilu>
 cudaError_t launch_row(const ActQuantArgs &a, cudaStream_t s) {
     const uint32_t units = a.k / 8;
-    uint32_t threads = units < 1024 ? ((units + 31) / 32) * 32 : 1024;
-    const uint32_t upt = (units + threads - 1) / threads;
-    dim3 grid(a.rows), block(threads);
-    if (upt <= 1) return launch_pdl(act_quant_row_kernel<kSilu, 1>, grid, block, s, a);
-    if (upt <= 2) return launch_pdl(act_quant_row_kernel<kSilu, 2>, grid, block, s, a);
-    if (upt <= 4) return launch_pdl(act_quant_row_kernel<kSilu, 4>, grid, block, s, a);
-    return launch_pdl(act_quant_row_kernel<kSilu, 8>, grid, block, s, a);
+    const uint32_t want = (2u * (uint32_t)device_sm_count() + a.rows - 1) / a.rows;
+    uint32_t ranks = want < 1 ? 1 : want > 8 ? 8 : want;
+    while (ranks > 1 && units / ranks < 256) --ranks;
+    const uint32_t per = (units + ranks - 1) / ranks;
+    uint32_t threads = per < 1024 ? ((per + 31) / 32) * 32 : 1024;
+    if (threads < 64) threads = 64;
+    const uint32_t upt = (per + threads - 1) / threads;
+    dim3 grid(ranks, a.rows), block(threads);
+    if (upt <= 1) return launch_pdl(act_quant_row_kernel<kSilu, 1>, grid, block, s, a, ranks);
+    if (upt <= 2) return launch_pdl(act_quant_row_kernel<kSilu, 2>, grid, block, s, a, ranks);
+    if (upt <= 4) return launch_pdl(act_quant_row_kernel<kSilu, 4>, grid, block, s, a, ranks);
+    return launch_pdl(act_quant_row_kernel<kSilu, 8>, grid, block, s, a, ranks);
 }
 
 template <bool kSilu>
