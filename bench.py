@@ -95,7 +95,10 @@ class W8A8Case:
         # of one GEMV launch: weights + scales + e4m3 activations + act scales + output
         self.gemv_bytes = n * K + w_scales + rows * K + self.s.numel() * 4 + rows * n * 4
         self.gemv_launches = 1  # one tcgen05 launch covers up to 256 rows
-        self.launches_per_step = 1 + self.gemv_launches  # activation quantiser + GEMV
+        # the library's plan: 1 when the GEMV quantises its own activations,
+        # else the quantiser + the GEMV (always for the SiLU variant)
+        plan = qdl.w8a8_plan(self.weights[0], rows)
+        self.launches_per_step = 2 if wl.silu else plan["proj_launches"]
         self.kernel = "w8a8_gemm_tc_kernel"
         self.kernel_src = ["w8a8_gemm_tc.cu"]
 

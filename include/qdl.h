@@ -230,6 +230,9 @@ typedef struct {
     uint32_t threads;    /* threads per CTA */
     uint32_t smem_bytes; /* dynamic shared memory per CTA */
     int32_t resident_clusters; /* clusters of split_k CTAs that fit the device at once */
+    uint32_t proj_launches; /* kernels one qdl_w8a8_proj call makes for these rows: 1 when
+                               the GEMV quantises its own activations (Block128, rows <= 16,
+                               every split-K rank's K blocks fit its ring), else 2 */
 } qdl_plan;
 
 QDL_API qdl_status qdl_w8a8_plan(const qdl_w8a8_weight *w, uint32_t rows, qdl_plan *plan);

@@ -142,6 +142,14 @@ qdl_status launch_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *
     return ok();
 }
 
+// qdl_w8a8_proj makes one launch (the GEMV quantises its own activation
+// blocks) for Block128, up to 16 rows, when every split-K rank's K blocks fit
+// the fused kernel's ring; otherwise the quantiser and the GEMV.
+bool proj_is_fused(const qdl_w8a8_weight *w, uint32_t rows) {
+    return QDL_TUNE_FUSED && w->format == QDL_SCALE_BLOCK128 && rows <= 16 && kMmaMaxRows == 0 &&
+           w8a8_fused_fits(w->n, w->k / kKUnit);
+}
+
 }  // namespace
 
 int device_sm_count() {
@@ -283,7 +291,7 @@ qdl_status qdl_w8a8_proj(const qdl_w8a8_weight *w, const void *x, uint32_t ldx, 
     qdl_status st = check_gemv(who, w, q, q_scale, q_bytes, scale_bytes, rows, out, out_dtype, ldc);
     if (st != QDL_OK) return st;
     if ((st = check_input(who, "x", x, ldx, w->k)) != QDL_OK) return st;
-    if (QDL_TUNE_FUSED && w->format == QDL_SCALE_BLOCK128 && rows <= 16 && kMmaMaxRows == 0) {
+    if (proj_is_fused(w, rows)) {
         // one launch: the GEMV quantises its own activation blocks
         return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, static_cast<cudaStream_t>(stream), ~0u,
                            kWaitLimitNs, x, ldx);
@@ -456,6 +464,7 @@ qdl_status qdl_w8a8_plan(const qdl_w8a8_weight *w, uint32_t rows, qdl_plan *plan
     plan->threads = p.threads;
     plan->smem_bytes = p.smem;
     plan->resident_clusters = p.clusters;
+    plan->proj_launches = proj_is_fused(w, rows) ? 1u : 2u;
     return ok();
 }
 

@@ -10,7 +10,12 @@
 namespace qdl {
 
 #ifndef QDL_TUNE_FUSED
-#define QDL_TUNE_FUSED 0  // quantise Block128 activations inside the GEMV (rows <= 16)
+// 1: qdl_w8a8_proj quantises Block128 activations inside the GEMV (rows <= 16,
+// short K ranges) in one launch.  Off: measured slower than the quantiser +
+// GEMV pair overlapped by programmatic launch (11.3 vs 9.45 us per call on
+// the M=8, K=4096 QKV projection), since every column tile re-quantises its
+// K range on the critical path.
+#define QDL_TUNE_FUSED 0
 #endif
 #ifndef QDL_TUNE_PDL
 #define QDL_TUNE_PDL 1  // programmatic dependent launch between the library's kernels
@@ -83,6 +88,8 @@ cudaError_t launch_w8a8_gemm_tc(const W8A8Args &a, int format, const uint8_t *co
                                 const uint32_t seg_n[3], cudaStream_t s);
 cudaError_t read_and_clear_tc_fault(uint32_t *value);
 uint32_t tc_bucket(uint32_t m);  // MMA N of the tensor-core kernel for m token rows
+// true when every split-K rank's K blocks fit the fused variant's ring (rows <= 16)
+bool w8a8_fused_fits(uint32_t n, uint32_t kb);
 cudaError_t launch_w8a8_proj_fused(const W8A8Args &a, const uint8_t *const seg_w[3], const uint32_t seg_n[3],
                                    cudaStream_t s);
 // Split-K factor minimising waves x (K blocks per CTA + fixed cost), where a

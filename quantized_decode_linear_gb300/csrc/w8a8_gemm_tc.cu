@@ -18,12 +18,15 @@
 //                      mbarrier.
 //   warp 2 (Block128): stages sa[m, kb] * sw[kb] for each K block in shared
 //                      memory for the epilogue (one buffer per accumulator).
-//   warp 2 (fused)   : instead quantises the bf16 activations of each K block
+//   fused variant    : when the CTA's whole K range fits the ring, a prologue
+//                      replaces the activation TMA and the scale warp: one lane
+//                      requests every weight block at once while warps 1..
+//                      quantise the bf16 activations of the CTA's K blocks
 //                      (absmax/448 per token and 128-group, RNE satfinite E4M3,
 //                      the arithmetic of the act-quant kernel) straight into
-//                      the stage's swizzled operand and the block's scales into
-//                      shared memory; the CTAs of tile 0 also write the codes
-//                      and scales to the caller's scratch.
+//                      the swizzled operands and the block scales into shared
+//                      memory; the CTAs of tile 0 also write the codes and
+//                      scales to the caller's scratch.  One launch per call.
 //   other warps      : epilogue, reading the f32 accumulators with tcgen05.ld.
 //
 // Scales.  PerRow: the accumulator sums the CTA's whole K range; the epilogue
@@ -127,7 +130,7 @@ struct Tc {
     static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
     static_assert(kTileRows * NTOK * 4 <= kBarOff, "split-K partials must fit in the stage ring");
     static_assert(kTmemCols <= 512, "tensor memory");
-    static_assert((3 * kStages + 3 * kAcc + 1) * 8 + 8 <= 512, "barrier area");
+    static_assert((2 * kStages + 3 * kAcc + 1) * 8 + 8 <= 512, "barrier area");
     static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
     static_assert(!kFused || (kBlock && NTOK == 16), "fused quantisation: Block128, up to 16 rows");
     static_assert(kInFlight % 16 == 0 && kCpt % kInFlight == 0, "epilogue load groups");
@@ -209,8 +212,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
     uint64_t *empty = full + C::kStages;
-    uint64_t *qfull = empty + C::kStages;  // fused: activation operand written
-    uint64_t *accf = qfull + C::kStages;   // [kAcc] accumulator buffer ready
+    uint64_t *accf = empty + C::kStages;  // [kAcc] accumulator buffer ready
     uint64_t *acce = accf + C::kAcc;      // [kAcc] accumulator buffer drained
     uint64_t *scal = acce + C::kAcc;      // [kAcc] fused: block scales written
     uint64_t *done = scal + C::kAcc;      // all MMAs complete
@@ -229,7 +231,6 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&qfull[s], 1);
         }
         for (int b = 0; b < C::kAcc; ++b) {
             mbar_init(&accf[b], 1);
@@ -277,41 +278,122 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
     auto tile_sw = [&](uint32_t kb) -> float {
         return tile_row0 < a.n ? __ldg(tile_scale + (size_t)(tile_lrow0 >> 7) * a.kb + kb) : 0.0f;
     };
+    // TMA of one K block of this tile's weights into stage `st`
+    const uint64_t pol_w = policy_evict_first();
+    auto load_weights = [&](uint32_t it, uint8_t *st, uint64_t *bar) {
+        const int32_t kk = (int32_t)((kb0 + it) * 128);
+        if (QDL_TC_BIGBOX && tile_single) {  // the whole tile lies in one segment: one box
+            tma_load_2d(st, tile_big, kk, (int32_t)tile_lrow0, bar, pol_w);
+            return;
+        }
+#pragma unroll 1
+        for (int b = 0; b < kTileRows / 16; ++b) {
+            const uint32_t r0 = tile_row0 + 16 * b;
+            const CUtensorMap *m;
+            uint32_t lr;
+            if (r0 < a.n1) {
+                m = &tm_w0; lr = r0;
+            } else if (r0 < a.n2) {
+                m = &tm_w1; lr = r0 - a.n1;
+            } else {
+                m = &tm_w2; lr = r0 - a.n2;
+            }
+            tma_load_2d(st + b * kWBox, m, kk, (int32_t)lr, bar, pol_w);
+        }
+    };
     uint32_t issued = 0;
     constexpr int kCpt = C::kCpt;
     float total[kBlock ? kCpt : 1];
 #pragma unroll
     for (int j = 0; j < (kBlock ? kCpt : 1); ++j) total[j] = 0.0f;
 
+    if constexpr (kFused) {
+        // ------------------------------------------------------------ fused prologue
+        // The CTA's whole K range fits the ring (the host only takes this
+        // variant when niter <= kStages and niter <= kAcc): one lane requests
+        // the weights of every block at once, and meanwhile warps 1.. quantise
+        // the CTA's activation blocks (16 lanes per 128-value group of a token
+        // row, rows >= m as zeros) straight into the B operands, and the block
+        // scales sa * sw into sbuf.
+        if (warp == 0) {
+            if (lane == 0) {
+                prefetch_tmap(tile_big);
+                for (uint32_t it = 0; it < niter; ++it) {
+                    mbar_arrive_expect_tx(&full[it], kWBytes);
+                    issued = it + 1;
+                    if (it == a.debug_skip_iter) continue;  // self-test: this stage never lands
+                    load_weights(it, smem + it * C::kStage, &full[it]);
+                }
+            }
+        } else {
+            grid_dep_wait();  // x comes from the previous kernel; the scratch may still be read by it
+            const int h = lane & 15, half = lane >> 4;
+            const uint32_t sbase = smem_u32(smem);
+            const uint16_t *x = reinterpret_cast<const uint16_t *>(a.x);
+            const uint32_t ngroups = NTOK * niter;
+            constexpr uint32_t kQWarps = C::kThreads / 32 - 1;
+            constexpr int kPasses = (NTOK * C::kStages + 2 * kQWarps - 1) / (2 * kQWarps);
+            // every load of this warp first (independent), then the arithmetic
+            uint4 raw[kPasses];
+#pragma unroll
+            for (int ps = 0; ps < kPasses; ++ps) {
+                const uint32_t gi = 2 * (warp - 1) + 2 * kQWarps * ps + half;
+                const uint32_t it = gi / NTOK, r = gi % NTOK;
+                raw[ps] = gi < ngroups && r < a.m
+                              ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)r * a.ldx + (kb0 + it) * 128 + 8 * h))
+                              : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int ps = 0; ps < kPasses; ++ps) {
+                const uint32_t gi = 2 * (warp - 1) + 2 * kQWarps * ps + half;
+                const bool valid = gi < ngroups;
+                const uint32_t it = gi / NTOK, r = gi % NTOK, kb = kb0 + it;
+                const uint32_t w[4] = {raw[ps].x, raw[ps].y, raw[ps].z, raw[ps].w};
+                float v[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    v[2 * j] = bf16_bits_to_f32(w[j] & 0xFFFFu);
+                    v[2 * j + 1] = bf16_bits_to_f32(w[j] >> 16);
+                }
+                float amax = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+                const float scale = __fdiv_rn(amax, 448.0f);
+                uint32_t lo = 0, hi = 0;  // token rows >= m: zero codes, nothing to divide
+                if (r < a.m) {
+                    uint32_t c[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        c[j] = cvt_e4m3x2(quant_operand(v[2 * j], scale), quant_operand(v[2 * j + 1], scale));
+                    lo = c[0] | (c[1] << 16);
+                    hi = c[2] | (c[3] << 16);
+                }
+                if (valid) {
+                    // row r, bytes 8h .. 8h+7: 16-byte chunk h/2 (swizzled by r & 7), half h & 1
+                    const uint32_t addr = sbase + it * C::kStage + kWBytes + r * 128 +
+                                          ((((uint32_t)h >> 1) ^ (r & 7)) << 4) + ((uint32_t)h & 1) * 8;
+                    sts64(addr, lo, hi);
+                    if (h == 0) sbuf[it * NTOK + r] = r < a.m ? scale * tile_sw(kb) : 0.0f;
+                    if (blockIdx.x == 0 && r < a.m) {  // tile-0 CTAs also fill the caller's scratch
+                        *reinterpret_cast<uint2 *>(a.q_out + (size_t)r * a.k + kb * 128 + 8 * h) = make_uint2(lo, hi);
+                        if (h == 0) a.sa_out[(size_t)r * a.kb + kb] = scale;
+                    }
+                }
+            }
+            fence_proxy_async_smem();  // the B operands are read by the tensor core
+        }
+        __syncthreads();
+    }
+
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
+        if (lane == 0 && !kFused) {
             prefetch_tmap(tile_big);
-            if (!kFused) prefetch_tmap(&tm_a);
-            const uint64_t pol_w = policy_evict_first();
+            prefetch_tmap(&tm_a);
             const uint64_t pol_a = policy_evict_last();
-            auto load_weights = [&](uint32_t it, uint8_t *st, uint64_t *bar) {
-                const int32_t kk = (int32_t)((kb0 + it) * 128);
-                if (QDL_TC_BIGBOX && tile_single) {  // the whole tile lies in one segment: one box
-                    tma_load_2d(st, tile_big, kk, (int32_t)tile_lrow0, bar, pol_w);
-                    return;
-                }
-#pragma unroll 1
-                for (int b = 0; b < kTileRows / 16; ++b) {
-                    const uint32_t r0 = tile_row0 + 16 * b;
-                    const CUtensorMap *m;
-                    uint32_t lr;
-                    if (r0 < a.n1) {
-                        m = &tm_w0; lr = r0;
-                    } else if (r0 < a.n2) {
-                        m = &tm_w1; lr = r0 - a.n1;
-                    } else {
-                        m = &tm_w2; lr = r0 - a.n2;
-                    }
-                    tma_load_2d(st + b * kWBox, m, kk, (int32_t)lr, bar, pol_w);
-                }
-            };
-            constexpr uint32_t kTx = kFused ? kWBytes : C::kStage;
+            constexpr uint32_t kTx = C::kStage;
             // weights of the first stages before waiting for the previous kernel
             const uint32_t head = niter < (uint32_t)C::kStages ? niter : (uint32_t)C::kStages;
             for (uint32_t it = 0; it < head; ++it) {
@@ -320,13 +402,11 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
                 if (it == a.debug_skip_iter) continue;  // self-test: this stage never lands
                 load_weights(it, smem + it * C::kStage, &full[it]);
             }
-            if (!kFused) {
-                grid_dep_wait();  // activations are written by the previous kernel
-                for (uint32_t it = 0; it < head; ++it)
-                    if (it != a.debug_skip_iter)
-                        tma_load_2d(smem + it * C::kStage + kWBytes, &tm_a, (int32_t)((kb0 + it) * 128), 0, &full[it],
-                                    pol_a);
-            }
+            grid_dep_wait();  // activations are written by the previous kernel
+            for (uint32_t it = 0; it < head; ++it)
+                if (it != a.debug_skip_iter)
+                    tma_load_2d(smem + it * C::kStage + kWBytes, &tm_a, (int32_t)((kb0 + it) * 128), 0, &full[it],
+                                pol_a);
             for (uint32_t it = head; it < niter; ++it) {
                 const uint32_t slot = it % C::kStages, ph = (it / C::kStages) & 1;
                 wait(&empty[slot], ph ^ 1, 1);
@@ -336,7 +416,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
                 if (it == a.debug_skip_iter) continue;
                 uint8_t *st = smem + slot * C::kStage;
                 load_weights(it, st, &full[slot]);
-                if (!kFused) tma_load_2d(st + kWBytes, &tm_a, (int32_t)((kb0 + it) * 128), 0, &full[slot], pol_a);
+                tma_load_2d(st + kWBytes, &tm_a, (int32_t)((kb0 + it) * 128), 0, &full[slot], pol_a);
             }
         }
     } else if (warp == 1) {
@@ -349,7 +429,6 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
                 const uint32_t b = kBlock ? it % C::kAcc : 0;
                 if (kBlock) wait(&acce[b], ((it / C::kAcc) & 1) ^ 1, 4);
                 wait(&full[slot], ph, 8);
-                if (kFused) wait(&qfull[slot], ph, 8);
                 if (*abort_flag) break;
                 tc_fence_after();
                 const uint64_t ad = sw128_desc(sbase + slot * C::kStage);
@@ -397,64 +476,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
             if (lane == 0) mbar_arrive(&scal[b]);
         }
     } else if (kFused && warp == 2) {
-        // ------------------------------------------------------------ quantiser
-        // 16 lanes per token row: lane h = lane & 15 holds elements 8h .. 8h+7
-        // of the row's 128-group; two rows per pass.
-        grid_dep_wait();
-        const int h = lane & 15, half = lane >> 4;
-        const uint32_t sbase = smem_u32(smem);
-        const uint16_t *x = reinterpret_cast<const uint16_t *>(a.x);
-        for (uint32_t it = 0; it < niter; ++it) {
-            const uint32_t slot = it % C::kStages, ph = (it / C::kStages) & 1;
-            const uint32_t b = it % C::kAcc, kb = kb0 + it;
-            // load this block of x for every row first (independent loads)
-            uint4 raw[NTOK / 2];
-#pragma unroll
-            for (int p = 0; p < NTOK / 2; ++p) {
-                const uint32_t r = 2 * p + half;
-                raw[p] = r < a.m ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)r * a.ldx + kb * 128 + 8 * h))
-                                 : make_uint4(0, 0, 0, 0);
-            }
-            wait(&empty[slot], ph ^ 1, 64);                // operand slot free
-            wait(&acce[b], ((it / C::kAcc) & 1) ^ 1, 64);  // scale buffer free
-#pragma unroll
-            for (int p = 0; p < NTOK / 2; ++p) {
-                const uint32_t r = 2 * p + half;
-                const uint32_t w[4] = {raw[p].x, raw[p].y, raw[p].z, raw[p].w};
-                float v[8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    v[2 * j] = bf16_bits_to_f32(w[j] & 0xFFFFu);
-                    v[2 * j + 1] = bf16_bits_to_f32(w[j] >> 16);
-                }
-                float amax = 0.0f;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
-#pragma unroll
-                for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-                const float scale = __fdiv_rn(amax, 448.0f);
-                uint32_t c[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    c[j] = cvt_e4m3x2(quant_operand(v[2 * j], scale), quant_operand(v[2 * j + 1], scale));
-                const uint32_t lo = c[0] | (c[1] << 16), hi = c[2] | (c[3] << 16);
-                // row r, bytes 8h..8h+7: 16-byte chunk h>>1 (swizzled by r & 7), half h&1
-                const uint32_t addr = sbase + slot * C::kStage + kWBytes + r * 128 +
-                                      ((((uint32_t)h >> 1) ^ (r & 7)) << 4) + ((uint32_t)h & 1) * 8;
-                sts64(addr, lo, hi);
-                if (h == 0) sbuf[b * NTOK + r] = r < a.m ? scale * tile_sw(kb) : 0.0f;
-                if (blockIdx.x == 0 && r < a.m) {  // tile-0 CTAs also fill the caller's scratch
-                    *reinterpret_cast<uint2 *>(a.q_out + (size_t)r * a.k + kb * 128 + 8 * h) = make_uint2(lo, hi);
-                    if (h == 0) a.sa_out[(size_t)r * a.kb + kb] = scale;
-                }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&qfull[slot]);
-                mbar_arrive(&scal[b]);
-            }
-        }
+        // fused: the prologue already wrote every operand and block scale
     } else {
         // ------------------------------------------------------------ epilogue
         const int e = warp - C::kEpiBase;
@@ -465,7 +487,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
         if constexpr (kBlock) {
             for (uint32_t it = 0; it < niter; ++it) {
                 const uint32_t b = it % C::kAcc;
-                wait(&scal[b], (it / C::kAcc) & 1, 32);  // sa * sw of this block
+                if (!kFused) wait(&scal[b], (it / C::kAcc) & 1, 32);  // sa * sw of this block
                 wait(&accf[b], (it / C::kAcc) & 1, 16);
                 tc_fence_after();
                 // kInFlight columns per wait: several loads in flight hide the
@@ -726,6 +748,14 @@ cudaError_t launch_w8a8_gemm_tc(const W8A8Args &a, int format, const uint8_t *co
 
 // Block128 projection with the activation quantisation fused in (rows <= 16):
 // a.x is the bf16 input, a.q / a.sa the caller's scratch that tile-0 CTAs fill.
+bool w8a8_fused_fits(uint32_t n, uint32_t kb) {
+    using C = Tc<16, true, true>;
+    const uint32_t tiles = (n + kTileRows - 1) / kTileRows;
+    const uint32_t split = choose_split_k(tiles, kb, cta_slots_tc<16, true, true>(), tc_reduce_cost(16));
+    const uint32_t niter = (kb + split - 1) / split;  // the largest rank's K blocks
+    return niter <= (uint32_t)C::kStages && niter <= (uint32_t)C::kAcc;
+}
+
 cudaError_t launch_w8a8_proj_fused(const W8A8Args &a, const uint8_t *const seg_w[3], const uint32_t seg_n[3],
                                    cudaStream_t s) {
     CUtensorMap maps[7];
