@@ -99,6 +99,9 @@ class W8A8Case:
         # else the quantiser + the GEMV (always for the SiLU variant)
         plan = qdl.w8a8_plan(self.weights[0], rows)
         self.launches_per_step = 2 if wl.silu else plan["proj_launches"]
+        # the GEMV as the projection runs it: with split K it adds into the
+        # zeroed f32 output
+        self.dom_dtype = qdl.OUT_F32_ADD if plan["split_k"] > 1 else qdl.OUT_F32
         self.kernel = "w8a8_gemm_tc_kernel"
         self.kernel_src = ["w8a8_gemm_tc.cu"]
 
@@ -112,7 +115,8 @@ class W8A8Case:
             qdl.w8a8_proj(w, self.x, self.rows, self.out, self.q, self.s)
 
     def dominant(self, i):
-        self.qdl.w8a8_gemv(self.weights[i % self.copies], self.q, self.s, self.rows, self.out)
+        self.qdl.w8a8_gemv(self.weights[i % self.copies], self.q, self.s, self.rows, self.out,
+                           out_dtype=self.dom_dtype)
 
     def e2e_step(self, i):
         self.x.copy_(self.x_host, non_blocking=True)

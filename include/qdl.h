@@ -58,8 +58,11 @@ typedef enum {
  *             token row and 128-wide K group, stored [rows, K/128]. */
 typedef enum { QDL_SCALE_PER_ROW = 0, QDL_SCALE_BLOCK128 = 1 } qdl_scale;
 
-/* Output element type of the W8A8 GEMV. */
-typedef enum { QDL_OUT_F32 = 0, QDL_OUT_BF16 = 1 } qdl_dtype;
+/* Output element type of the W8A8 GEMV.  QDL_OUT_F32_ADD (qdl_w8a8_gemv
+ * only) adds y to the f32 values already in out; split-K partial sums are
+ * then added with f32 atomics, so their order, and the last bits of the
+ * result, may vary from run to run. */
+typedef enum { QDL_OUT_F32 = 0, QDL_OUT_BF16 = 1, QDL_OUT_F32_ADD = 2 } qdl_dtype;
 
 #define QDL_MAX_ROWS 256  /* w8a8_decode.rs W8A8_MAX_ROWS */
 #define QDL_K_UNIT 128    /* w8a8_decode.rs W8A8_K_UNIT   */
@@ -141,7 +144,10 @@ QDL_API qdl_status qdl_act_quant_silu(int32_t format, const void *gate, const vo
  *   q, q_scale : device, as written by qdl_act_quant (capacities q_bytes,
  *                scale_bytes are checked like the activation scratch).
  *   out        : device [rows, ldc] of out_dtype (f32, or bf16 rounded to
- *                nearest even); columns N..ldc-1 are not written.
+ *                nearest even, or f32 accumulated: out += y); columns
+ *                N..ldc-1 are not written.
+ * With F32 and BF16 output, the partial sums of CTAs that split K are added
+ * in a fixed order, so results are reproducible bit for bit.
  * Checks: weight initialised; 1 <= rows <= 256; capacities; ldc >= N;
  * out aligned to its element size; out_dtype valid. */
 QDL_API qdl_status qdl_w8a8_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *q_scale,
@@ -150,14 +156,20 @@ QDL_API qdl_status qdl_w8a8_gemv(const qdl_w8a8_weight *w, const uint8_t *q, con
 
 /* Decode projection (w8a8_decode.rs fn w8a8_proj): qdl_act_quant with the
  * weight's format and K, then qdl_w8a8_gemv, on one stream.  q and q_scale
- * are the caller's activation scratch (sizes from qdl_scratch_bytes). */
+ * are the caller's activation scratch (sizes from qdl_scratch_bytes).
+ * With f32 output, when the GEMV splits K over several CTAs, the quantiser
+ * first sets out[0..rows)[0..N) to zero and the GEMV adds into it
+ * (QDL_OUT_F32_ADD): the order of the split-K additions varies, so results
+ * may differ in the last bits from run to run (always within the GEMV's
+ * error bound).  bf16 output takes the fixed-order reduction.  out_dtype is
+ * QDL_OUT_F32 or QDL_OUT_BF16. */
 QDL_API qdl_status qdl_w8a8_proj(const qdl_w8a8_weight *w, const void *x, uint32_t ldx, uint32_t rows,
                          void *out, int32_t out_dtype, uint32_t ldc, uint8_t *q, float *q_scale,
                          size_t q_bytes, size_t scale_bytes, void *stream);
 
 /* MLP down projection: qdl_act_quant_silu with the weight's format and K,
  * then qdl_w8a8_gemv (the composition w8a8_decode.rs uses for gate/up
- * inputs). */
+ * inputs).  f32 output is accumulated as in qdl_w8a8_proj. */
 QDL_API qdl_status qdl_w8a8_proj_silu(const qdl_w8a8_weight *w, const void *gate, const void *up,
                               uint32_t ld_gate, uint32_t ld_up, uint32_t rows, void *out,
                               int32_t out_dtype, uint32_t ldc, uint8_t *q, float *q_scale,

@@ -17,6 +17,7 @@ PER_ROW = 0
 BLOCK128 = 1
 OUT_F32 = 0
 OUT_BF16 = 1
+OUT_F32_ADD = 2  # qdl_w8a8_gemv only: out += y
 MAX_ROWS = 256
 K_UNIT = 128
 

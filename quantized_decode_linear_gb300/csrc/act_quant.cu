@@ -53,6 +53,11 @@ __device__ __forceinline__ void dependent_launch_prologue() {
 template <bool kSilu>
 __global__ void __launch_bounds__(256) act_quant_g128_kernel(ActQuantArgs a) {
     dependent_launch_prologue();
+    if (a.zout != nullptr) {  // the whole grid zeroes the output rows
+        const uint32_t total = a.rows * a.zn, stride = gridDim.x * blockDim.x;
+        for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += stride)
+            a.zout[(size_t)(e / a.zn) * a.zldc + e % a.zn] = 0.0f;
+    }
     const uint32_t groups_per_row = a.k / kKUnit;
     const uint32_t gid = blockIdx.x * 8 + (threadIdx.x >> 5);
     const uint32_t lane = threadIdx.x & 31;
@@ -94,6 +99,11 @@ __global__ void __launch_bounds__(1024) act_quant_row_kernel(ActQuantArgs a) {
     __shared__ float cta_max;
     dependent_launch_prologue();
     const uint32_t row = blockIdx.y;
+    if (a.zout != nullptr) {  // the row's ranks zero its output row
+        const uint32_t stride = gridDim.x * blockDim.x;
+        for (uint32_t c = blockIdx.x * blockDim.x + threadIdx.x; c < a.zn; c += stride)
+            a.zout[(size_t)row * a.zldc + c] = 0.0f;
+    }
     const uint32_t nrank = gridDim.x, rank = blockIdx.x;
     const uint32_t units = a.k / 8;
     const uint32_t per = (units + nrank - 1) / nrank;

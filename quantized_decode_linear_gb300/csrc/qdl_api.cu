@@ -89,7 +89,8 @@ qdl_status check_weight(const char *who, const qdl_w8a8_weight *w) {
 
 qdl_status launch_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *q_scale, uint32_t rows, void *out,
                        int32_t out_dtype, uint32_t ldc, cudaStream_t stream, uint32_t debug_skip_iter = ~0u,
-                       uint64_t wait_limit_ns = kWaitLimitNs, const void *fused_x = nullptr, uint32_t fused_ldx = 0) {
+                       uint64_t wait_limit_ns = kWaitLimitNs, const void *fused_x = nullptr, uint32_t fused_ldx = 0,
+                       bool accumulate = false) {
     const size_t spr = scales_per_row(w->format, w->k);
     const size_t elt = out_dtype == QDL_OUT_BF16 ? 2 : 4;
     W8A8Args a = {};
@@ -111,6 +112,7 @@ qdl_status launch_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *
     a.kb = w->k / kKUnit;
     a.debug_skip_iter = debug_skip_iter;
     a.wait_limit_ns = wait_limit_ns;
+    a.accumulate = out_dtype == QDL_OUT_F32_ADD || (accumulate && out_dtype == QDL_OUT_F32);
     // Token rows up to QDL_MMA_MAX_ROWS go to the mma.sync streaming kernel;
     // all others take one pass of the tcgen05 kernel (rows <= 256).
     if (rows > kMmaMaxRows) {
@@ -140,6 +142,30 @@ qdl_status launch_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *
     cudaError_t e = launch_w8a8_gemv_tma(a, w->format, seg_w, seg_n, stream);
     if (e != cudaSuccess) return cuda_fail("qdl_w8a8_gemv", e);
     return ok();
+}
+
+// split-K factor the tcgen05 GEMV takes for this weight and row count
+uint32_t gemv_split(const qdl_w8a8_weight *w, uint32_t rows) {
+    if (rows <= kMmaMaxRows) return 1;
+    W8A8Args a = {};
+    a.n = w->n;
+    a.k = w->k;
+    a.kb = w->k / kKUnit;
+    a.m = rows;
+    PlanInfo p = {};
+    return plan_w8a8_gemm_tc(a, w->format, &p) == cudaSuccess ? p.split : 1;
+}
+
+// The projection entry points with f32 output let the quantiser zero the
+// output first, so that the GEMV's split-K ranks add into it atomically
+// instead of meeting in a cluster reduction.
+bool zero_f32_output(ActQuantArgs &a, const qdl_w8a8_weight *w, uint32_t rows, void *out, int32_t out_dtype,
+                     uint32_t ldc, uint32_t n) {
+    if (out_dtype != QDL_OUT_F32 || gemv_split(w, rows) < 2) return false;  // nothing to add up
+    a.zout = static_cast<float *>(out);
+    a.zldc = ldc;
+    a.zn = n;
+    return true;
 }
 
 // qdl_w8a8_proj makes one launch (the GEMV quantises its own activation
@@ -261,7 +287,7 @@ qdl_status qdl_act_quant_silu(int32_t format, const void *gate, const void *up, 
 }
 
 static qdl_status check_gemv(const char *who, const qdl_w8a8_weight *w, const uint8_t *q, const float *q_scale, size_t q_bytes,
-                             size_t scale_bytes, uint32_t rows, const void *out, int32_t out_dtype, uint32_t ldc) {
+                             size_t scale_bytes, uint32_t rows, const void *out, int32_t out_dtype, uint32_t ldc, bool allow_add = false) {
     qdl_status st = check_weight(who, w);
     if (st != QDL_OK) return st;
     // w8a8_decode_available
@@ -271,8 +297,9 @@ static qdl_status check_gemv(const char *who, const qdl_w8a8_weight *w, const ui
     if (!aligned(q, 16) || !aligned(q_scale, 4))
         return fail(QDL_ERR_INVALID_ARG, "%s: q must be 16-byte and q_scale 4-byte aligned", who);
     if (ldc < w->n) return fail(QDL_ERR_INVALID_ARG, "%s: ldc=%u < N=%u", who, ldc, w->n);
-    if (out_dtype != QDL_OUT_F32 && out_dtype != QDL_OUT_BF16)
-        return fail(QDL_ERR_INVALID_ARG, "%s: output dtype %d is not F32 or BF16", who, (int)out_dtype);
+    if (out_dtype != QDL_OUT_F32 && out_dtype != QDL_OUT_BF16 && !(allow_add && out_dtype == QDL_OUT_F32_ADD))
+        return fail(QDL_ERR_INVALID_ARG, "%s: output dtype %d is not %s", who, (int)out_dtype,
+                    allow_add ? "F32, BF16 or F32_ADD" : "F32 or BF16");
     if (out == nullptr || !aligned(out, out_dtype == QDL_OUT_BF16 ? 2 : 4))
         return fail(QDL_ERR_INVALID_ARG, "%s: output is NULL or misaligned", who);
     return QDL_OK;
@@ -280,7 +307,7 @@ static qdl_status check_gemv(const char *who, const qdl_w8a8_weight *w, const ui
 
 qdl_status qdl_w8a8_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *q_scale, size_t q_bytes, size_t scale_bytes,
                          uint32_t rows, void *out, int32_t out_dtype, uint32_t ldc, void *stream) {
-    qdl_status st = check_gemv("w8a8_gemv", w, q, q_scale, q_bytes, scale_bytes, rows, out, out_dtype, ldc);
+    qdl_status st = check_gemv("w8a8_gemv", w, q, q_scale, q_bytes, scale_bytes, rows, out, out_dtype, ldc, true);
     if (st != QDL_OK) return st;
     return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, static_cast<cudaStream_t>(stream));
 }
@@ -297,9 +324,11 @@ qdl_status qdl_w8a8_proj(const qdl_w8a8_weight *w, const void *x, uint32_t ldx, 
                            kWaitLimitNs, x, ldx);
     }
     ActQuantArgs a = {static_cast<const uint16_t *>(x), nullptr, ldx, 0, rows, w->k, q, q_scale};
+    const bool acc = zero_f32_output(a, w, rows, out, out_dtype, ldc, w->n);
     cudaError_t e = launch_act_quant(a, w->format, false, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(who, e);
-    return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, static_cast<cudaStream_t>(stream));
+    return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, static_cast<cudaStream_t>(stream), ~0u, kWaitLimitNs,
+                       nullptr, 0, acc);
 }
 
 qdl_status qdl_w8a8_proj_silu(const qdl_w8a8_weight *w, const void *gate, const void *up, uint32_t ld_gate, uint32_t ld_up,
@@ -311,9 +340,11 @@ qdl_status qdl_w8a8_proj_silu(const qdl_w8a8_weight *w, const void *gate, const 
     if ((st = check_input(who, "gate", gate, ld_gate, w->k)) != QDL_OK) return st;
     if ((st = check_input(who, "up", up, ld_up, w->k)) != QDL_OK) return st;
     ActQuantArgs a = {static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up), ld_gate, ld_up, rows, w->k, q, q_scale};
+    const bool acc = zero_f32_output(a, w, rows, out, out_dtype, ldc, w->n);
     cudaError_t e = launch_act_quant(a, w->format, true, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(who, e);
-    return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, static_cast<cudaStream_t>(stream));
+    return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, static_cast<cudaStream_t>(stream), ~0u, kWaitLimitNs,
+                       nullptr, 0, acc);
 }
 
 qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq, uint32_t nkv, uint32_t group,

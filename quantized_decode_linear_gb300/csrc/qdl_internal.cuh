@@ -33,6 +33,10 @@ struct ActQuantArgs {
     uint32_t rows, k;
     uint8_t *q;         // [rows, k]
     float *s;           // [rows] or [rows, k/128]
+    // optional: f32 output [rows, zn] (row stride zldc) to set to zero after
+    // the dependency wait, for a following GEMV that accumulates into it
+    float *zout;
+    uint32_t zldc, zn;
 };
 
 struct W8A8Args {
@@ -49,6 +53,7 @@ struct W8A8Args {
     uint32_t kb;        // k / 128
     uint32_t debug_skip_iter;  // self-test only: pipeline stage never loaded (else ~0u)
     uint64_t wait_limit_ns;    // limit of every device-side wait
+    uint32_t accumulate;       // f32 output is zero: split-K ranks add their partials atomically
     // fused projection only: bf16 input [m, ldx] and the scratch it fills
     const void *x;
     uint32_t ldx;

@@ -41,7 +41,9 @@
 // after griddepcontrol.wait.
 //
 // Split-K CTAs of one cluster reduce their partials through distributed shared
-// memory in rank order (deterministic).  Every wait is bounded; after a
+// memory in rank order (deterministic), or, when the caller has zeroed an f32
+// output (the projection entry points), add them into it with f32 atomics
+// (no cluster barrier; the order of the additions varies from run to run).  Every wait is bounded; after a
 // timeout the CTA records a fault word, waits (bounded) for its copies and
 // MMAs in flight, frees its tensor memory and returns.
 #include <cooperative_groups.h>
@@ -537,10 +539,18 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
     }
     grid_dep_wait();  // outputs may be read or written by earlier kernels
 
-    auto store = [&](uint32_t tok, uint32_t r, float v) {
+    // split-K ranks add into the zeroed f32 output (red.global.add.f32)
+    // instead of meeting in the cluster reduction
+    const bool add_out = a.accumulate && split > 1;
+    auto add = [&](uint32_t tok, uint32_t r, float v) {
+        if (tok < a.m && r < a.n) atomicAdd(reinterpret_cast<float *>(a.out) + (size_t)tok * a.ldc + r, v);
+    };
+    auto store = [&](uint32_t tok, uint32_t r, float v) {  // the single writer of (tok, r)
         if (tok < a.m && r < a.n) {
             if (a.out_bf16)
                 reinterpret_cast<__nv_bfloat16 *>(a.out)[(size_t)tok * a.ldc + r] = __float2bfloat16_rn(v);
+            else if (a.accumulate)
+                reinterpret_cast<float *>(a.out)[(size_t)tok * a.ldc + r] += v;
             else
                 reinterpret_cast<float *>(a.out)[(size_t)tok * a.ldc + r] = v;
         }
@@ -561,6 +571,8 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
                 const uint32_t tok = cgrp * kCpt + j;
                 if (split == 1)
                     store(tok, row, total[j]);
+                else if (add_out)
+                    add(tok, row, total[j]);
                 else
                     red[tok * kTileRows + lrow] = total[j];
             }
@@ -587,6 +599,8 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
                     const float s = tok < a.m ? __ldg(a.sa + tok) * swr : 0.0f;
                     if (split == 1)
                         store(tok, row, v[i] * s);
+                    else if (add_out)
+                        add(tok, row, v[i] * s);
                     else
                         red[tok * kTileRows + lrow] = v[i] * s;
                 }
@@ -596,7 +610,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
         }
     }
 
-    if (split > 1) {
+    if (split > 1 && !add_out) {
         // rank r adds rows 128r/split .. 128(r+1)/split - 1 of every rank's
         // partials, in rank order
         cg::cluster_group cluster = cg::this_cluster();

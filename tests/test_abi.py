@@ -217,6 +217,17 @@ def test_proj_checks_input(lib):
     assert st == INVALID and "x stride=4095" in lib.qdl_last_error().decode()
 
 
+def test_accumulating_output_is_gemv_only(lib):
+    """QDL_OUT_F32_ADD (out += y) is accepted by qdl_w8a8_gemv's checks but
+    not by the projections, which pick accumulation themselves"""
+    d = _weight(lib)
+    st = lib.qdl_w8a8_proj(ctypes.byref(d), DEV, 4096, 8, DEV + 0x4000000, qdl.OUT_F32_ADD, 6144,
+                           DEV + 0x1000000, DEV + 0x2000000, 1 << 24, 1 << 20, None)
+    assert st == INVALID and "output dtype 2 is not F32 or BF16" in lib.qdl_last_error().decode()
+    st, err = _gemv(lib, d, dtype=qdl.OUT_F32_ADD, ldc=6143)  # fails on ldc, after the dtype check passed
+    assert st == INVALID and "ldc=6143" in err, err
+
+
 # ---------------------------------------------------------------- INT4
 
 def _int4(lib, x=DEV, m=1, k=4096, nq=4096, nkv=1024, group=128, qw=None, sc=None, zr=None, out=None):

@@ -70,6 +70,26 @@ def test_proj_segments_and_ragged_n(fmt, sizes, k, rows):
 
 
 @pytest.mark.parametrize("fmt", [qdl.PER_ROW, qdl.BLOCK128])
+@pytest.mark.parametrize("n,k,rows", [(384, 384, 3), (256, 8192, 8), (6144, 4096, 8), (1024, 14336, 64)])
+def test_gemv_accumulating_output(fmt, n, k, rows):
+    """QDL_OUT_F32_ADD adds y to the values already in out, with the split-K
+    partial sums added atomically (shapes cover unsplit and split plans)"""
+    segs = _segments(fmt, k, [n], seed=n + rows)
+    x = syn.bf16_normal((rows, k), seed=7 + rows)
+    qo, so = oracle.act_quant(fmt, x, k)
+    yo, bo = oracle.w8a8_gemv(fmt, qo, so, segs)
+    w, _keep = upload_weight(segs, fmt)
+    base = np.random.default_rng(n).normal(0.0, 1.0, (rows, n)).astype(np.float32)
+    out = dev(base)
+    qdl.w8a8_gemv(w, dev(qo), dev(so if fmt == qdl.BLOCK128 else so[:, None]), rows, out,
+                  out_dtype=qdl.OUT_F32_ADD)
+    torch.cuda.synchronize()
+    # the additions into out each round once more (at most split + 1 of them)
+    check_close(host(out), base.astype(np.float64) + yo, bo + 2 ** -18 * np.abs(base) / 2e-3,
+                what=f"fmt={fmt} split={qdl.w8a8_plan(w, rows)['split_k']}")
+
+
+@pytest.mark.parametrize("fmt", [qdl.PER_ROW, qdl.BLOCK128])
 def test_bf16_output(fmt):
     rows, k = 9, 512
     segs = _segments(fmt, k, [256, 128], seed=3)
