@@ -101,8 +101,8 @@ class W8A8Case:
         self.launches_per_step = 2 if wl.silu else plan["proj_launches"]
         # the GEMV as the projection runs it: with split K it adds into the
         # zeroed f32 output
-        self.dom_dtype = qdl.OUT_F32_ADD if plan["split_k"] > 1 else qdl.OUT_F32
-        self.kernel = "w8a8_gemm_tc_kernel"
+        self.dom_dtype = qdl.OUT_F32_ADD if plan["proj_accumulates"] else qdl.OUT_F32
+        self.kernel = "w8a8_streamk_kernel" if plan["proj_streamk"] else "w8a8_gemm_tc_kernel"
         self.kernel_src = ["w8a8_gemm_tc.cu"]
 
     def step(self, i):

@@ -229,7 +229,7 @@ QDL_API qdl_status qdl_w8a8_proj_static(const qdl_w8a8_weight *w, const void *x,
                                         uint32_t rows, void *out, int32_t out_dtype, uint32_t ldc,
                                         void *stream);
 
-/* Launch plan of qdl_w8a8_gemv for `rows` token rows on the current device:
+/* Launch plan of qdl_w8a8_gemv (QDL_OUT_F32) for `rows` token rows on the current device:
  * which kernel runs and how the work is cut (no counterpart on the pages;
  * for tuning and tests).  Queries the device's occupancy tables; launches
  * nothing. */
@@ -245,6 +245,11 @@ typedef struct {
     uint32_t proj_launches; /* kernels one qdl_w8a8_proj call makes for these rows: 1 when
                                the GEMV quantises its own activations (Block128, rows <= 16,
                                every split-K rank's K blocks fit its ring), else 2 */
+    uint32_t proj_accumulates; /* 1 when qdl_w8a8_proj with f32 output zeroes out and runs the
+                                  GEMV as QDL_OUT_F32_ADD (split K, or the stream-K kernel
+                                  that Block128 takes for 17..128 rows), else 0 */
+    uint32_t proj_streamk;     /* 1 when that accumulating GEMV is the stream-K kernel (one
+                                  contiguous range of (tile, K block) units per CTA), else 0 */
 } qdl_plan;
 
 QDL_API qdl_status qdl_w8a8_plan(const qdl_w8a8_weight *w, uint32_t rows, qdl_plan *plan);

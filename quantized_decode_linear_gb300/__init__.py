@@ -50,7 +50,8 @@ class Plan(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("mma_n", ctypes.c_uint32), ("tiles", ctypes.c_uint32),
                 ("split_k", ctypes.c_uint32), ("stages", ctypes.c_uint32), ("threads", ctypes.c_uint32),
                 ("smem_bytes", ctypes.c_uint32), ("resident_clusters", ctypes.c_int32),
-                ("proj_launches", ctypes.c_uint32)]
+                ("proj_launches", ctypes.c_uint32), ("proj_accumulates", ctypes.c_uint32),
+                ("proj_streamk", ctypes.c_uint32)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

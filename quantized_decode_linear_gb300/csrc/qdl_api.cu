@@ -159,9 +159,13 @@ uint32_t gemv_split(const qdl_w8a8_weight *w, uint32_t rows) {
 // The projection entry points with f32 output let the quantiser zero the
 // output first, so that the GEMV's split-K ranks add into it atomically
 // instead of meeting in a cluster reduction.
+bool proj_accumulates(const qdl_w8a8_weight *w, uint32_t rows) {
+    return gemv_split(w, rows) >= 2 || w8a8_streamk_applies(w->format, rows);
+}
+
 bool zero_f32_output(ActQuantArgs &a, const qdl_w8a8_weight *w, uint32_t rows, void *out, int32_t out_dtype,
                      uint32_t ldc, uint32_t n) {
-    if (out_dtype != QDL_OUT_F32 || gemv_split(w, rows) < 2) return false;  // nothing to add up
+    if (out_dtype != QDL_OUT_F32 || !proj_accumulates(w, rows)) return false;
     a.zout = static_cast<float *>(out);
     a.zldc = ldc;
     a.zn = n;
@@ -496,6 +500,8 @@ qdl_status qdl_w8a8_plan(const qdl_w8a8_weight *w, uint32_t rows, qdl_plan *plan
     plan->smem_bytes = p.smem;
     plan->resident_clusters = p.clusters;
     plan->proj_launches = proj_is_fused(w, rows) ? 1u : 2u;
+    plan->proj_accumulates = !proj_is_fused(w, rows) && proj_accumulates(w, rows) ? 1u : 0u;
+    plan->proj_streamk = plan->proj_accumulates && w8a8_streamk_applies(w->format, rows) ? 1u : 0u;
     return ok();
 }
 

@@ -93,6 +93,9 @@ cudaError_t launch_w8a8_gemm_tc(const W8A8Args &a, int format, const uint8_t *co
                                 const uint32_t seg_n[3], cudaStream_t s);
 cudaError_t read_and_clear_tc_fault(uint32_t *value);
 uint32_t tc_bucket(uint32_t m);  // MMA N of the tensor-core kernel for m token rows
+// true when the accumulating Block128 GEMV for these rows runs stream-K
+// (one range of (tile, K block) units per CTA; it needs a zeroed f32 output)
+bool w8a8_streamk_applies(int format, uint32_t rows);
 // true when every split-K rank's K blocks fit the fused variant's ring (rows <= 16)
 bool w8a8_fused_fits(uint32_t n, uint32_t kb);
 cudaError_t launch_w8a8_proj_fused(const W8A8Args &a, const uint8_t *const seg_w[3], const uint32_t seg_n[3],

@@ -63,6 +63,14 @@ namespace cg = cooperative_groups;
 #ifndef QDL_TC_STAGE_BYTES_BIG
 #define QDL_TC_STAGE_BYTES_BIG (72 * 1024)
 #endif
+// token buckets in which the accumulating Block128 GEMV runs stream-K (at 256
+// tokens the f32 atomics of the shared tiles cost more than the balance wins)
+#ifndef QDL_STREAMK_MIN_NTOK
+#define QDL_STREAMK_MIN_NTOK 32
+#endif
+#ifndef QDL_STREAMK_MAX_NTOK
+#define QDL_STREAMK_MAX_NTOK 128
+#endif
 #ifndef QDL_TC_BIG_NTOK
 #define QDL_TC_BIG_NTOK 128
 #endif
@@ -644,6 +652,292 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
     }
 }
 
+// ---------------------------------------------------------------- stream-K variant
+//
+// Block128, f32 output that the caller has zeroed (accumulate mode).  The work
+// is the sequence of (tile, K block) units, tile-major; CTA c of P takes units
+// [c U / P, (c+1) U / P) and streams them through one ring without stopping at
+// tile boundaries, so every CTA moves the same number of weight bytes and no
+// CTA waits for a second wave.  The epilogue keeps register totals for the
+// current tile; when the CTA's range leaves that tile it stores them if the
+// CTA covered the whole tile, and otherwise adds them into the output with f32
+// atomics (a tile shared by two or more CTAs).  Roles, barriers and bounded waits are those
+// of w8a8_gemm_tc_kernel<NTOK, true, false>.
+template <int NTOK>
+__global__ void __launch_bounds__(Tc<NTOK, true, false>::kThreads, 1) __maxnreg__((Tc<NTOK, true, false>::kMaxRegs))
+    w8a8_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
+                        const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_b0,
+                        const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_b2,
+                        const __grid_constant__ CUtensorMap tm_a, const W8A8Args a) {
+    using C = Tc<NTOK, true, false>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+    uint64_t *empty = full + C::kStages;
+    uint64_t *accf = empty + C::kStages;
+    uint64_t *acce = accf + C::kAcc;
+    uint64_t *scal = acce + C::kAcc;
+    uint64_t *done = scal + C::kAcc;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+    float *sbuf = reinterpret_cast<float *>(smem + C::kScaleOff);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t tiles = (a.n + kTileRows - 1) / kTileRows;
+    const uint64_t units = (uint64_t)tiles * a.kb;
+    const uint32_t u0 = (uint32_t)(units * blockIdx.x / gridDim.x);
+    const uint32_t u1 = (uint32_t)(units * (blockIdx.x + 1) / gridDim.x);
+    const uint32_t niter = u1 - u0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < C::kAcc; ++b) {
+            mbar_init(&accf[b], 1);
+            mbar_init(&acce[b], C::kEpi);
+            mbar_init(&scal[b], 1);
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(C::kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto fault = [&](uint32_t code) {
+        *abort_flag = 1;
+        atomicOr(&g_tc_fault, code);
+    };
+    auto wait = [&](uint64_t *bar, uint32_t parity, uint32_t code) {
+        if (!*abort_flag && !mbar_wait(bar, parity, a.wait_limit_ns)) fault(code);
+    };
+    // segment of a tile (Block128 tiles never straddle segments)
+    struct TileSeg {
+        const float *scale;
+        const CUtensorMap *big;
+        uint32_t lrow0;
+        bool single;
+    };
+    auto tile_seg = [&](uint32_t tile) {
+        const uint32_t r0 = tile * kTileRows;
+        TileSeg t;
+        uint32_t seg_end;
+        if (r0 < a.n1) {
+            t.scale = a.sw0; t.lrow0 = r0; t.big = &tm_b0; seg_end = a.n1;
+        } else if (r0 < a.n2) {
+            t.scale = a.sw1; t.lrow0 = r0 - a.n1; t.big = &tm_b1; seg_end = a.n2;
+        } else {
+            t.scale = a.sw2; t.lrow0 = r0 - a.n2; t.big = &tm_b2; seg_end = a.n;
+        }
+        t.single = r0 + kTileRows <= seg_end || seg_end == a.n;
+        return t;
+    };
+
+    uint32_t issued = 0;
+    constexpr int kCpt = C::kCpt;
+    float total[kCpt];
+#pragma unroll
+    for (int j = 0; j < kCpt; ++j) total[j] = 0.0f;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_a);
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_a = policy_evict_last();
+            auto load_weights = [&](uint32_t u, uint8_t *st, uint64_t *bar) {
+                const uint32_t tile = u / a.kb, kb = u % a.kb;
+                const TileSeg t = tile_seg(tile);
+                const int32_t kk = (int32_t)(kb * 128);
+                if (QDL_TC_BIGBOX && t.single) {
+                    tma_load_2d(st, t.big, kk, (int32_t)t.lrow0, bar, pol_w);
+                    return;
+                }
+#pragma unroll 1
+                for (int b = 0; b < kTileRows / 16; ++b) {
+                    const uint32_t r0 = tile * kTileRows + 16 * b;
+                    const CUtensorMap *m;
+                    uint32_t lr;
+                    if (r0 < a.n1) {
+                        m = &tm_w0; lr = r0;
+                    } else if (r0 < a.n2) {
+                        m = &tm_w1; lr = r0 - a.n1;
+                    } else {
+                        m = &tm_w2; lr = r0 - a.n2;
+                    }
+                    tma_load_2d(st + b * kWBox, m, kk, (int32_t)lr, bar, pol_w);
+                }
+            };
+            constexpr uint32_t kTx = C::kStage;
+            const uint32_t head = niter < (uint32_t)C::kStages ? niter : (uint32_t)C::kStages;
+            for (uint32_t it = 0; it < head; ++it) {
+                mbar_arrive_expect_tx(&full[it], kTx);
+                issued = it + 1;
+                load_weights(u0 + it, smem + it * C::kStage, &full[it]);
+            }
+            grid_dep_wait();  // activations are written by the previous kernel
+            for (uint32_t it = 0; it < head; ++it)
+                tma_load_2d(smem + it * C::kStage + kWBytes, &tm_a, (int32_t)(((u0 + it) % a.kb) * 128), 0, &full[it],
+                            pol_a);
+            for (uint32_t it = head; it < niter; ++it) {
+                const uint32_t slot = it % C::kStages, ph = (it / C::kStages) & 1;
+                wait(&empty[slot], ph ^ 1, 1);
+                if (*abort_flag) break;
+                mbar_arrive_expect_tx(&full[slot], kTx);
+                issued = it + 1;
+                uint8_t *st = smem + slot * C::kStage;
+                load_weights(u0 + it, st, &full[slot]);
+                tma_load_2d(st + kWBytes, &tm_a, (int32_t)(((u0 + it) % a.kb) * 128), 0, &full[slot], pol_a);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f8<NTOK>();
+            const uint32_t sbase = smem_u32(smem);
+            for (uint32_t it = 0; it < niter; ++it) {
+                const uint32_t slot = it % C::kStages, ph = (it / C::kStages) & 1;
+                const uint32_t b = it % C::kAcc;
+                wait(&acce[b], ((it / C::kAcc) & 1) ^ 1, 4);
+                wait(&full[slot], ph, 8);
+                if (*abort_flag) break;
+                tc_fence_after();
+                const uint64_t ad = sw128_desc(sbase + slot * C::kStage);
+                const uint64_t bd = sw128_desc(sbase + slot * C::kStage + kWBytes);
+                const uint32_t d = tmem + b * NTOK;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) tc_mma(d, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+                tc_commit(&empty[slot]);
+                tc_commit(&accf[b]);
+            }
+            tc_commit(done);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ scale warp
+        constexpr int kPer = (NTOK + 31) / 32;
+        grid_dep_wait();
+        auto load = [&](uint32_t it, float (&v)[kPer]) {
+            const uint32_t u = u0 + it, tile = u / a.kb, kb = u % a.kb;
+            float sw = 0.0f;
+            if (it < niter) {
+                const TileSeg t = tile_seg(tile);
+                sw = __ldg(t.scale + (size_t)(t.lrow0 >> 7) * a.kb + kb);
+            }
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const uint32_t tok = 32 * j + lane;
+                v[j] = (it < niter && tok < a.m && tok < (uint32_t)NTOK) ? __ldg(a.sa + (size_t)tok * a.kb + kb) * sw
+                                                                      : 0.0f;
+            }
+        };
+        float next[kPer];
+        load(0, next);
+        for (uint32_t it = 0; it < niter; ++it) {
+            const uint32_t b = it % C::kAcc;
+            float cur[kPer];
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) cur[j] = next[j];
+            load(it + 1, next);
+            wait(&acce[b], ((it / C::kAcc) & 1) ^ 1, 64);
+#pragma unroll
+            for (int j = 0; j < kPer; ++j)
+                if (32 * j + lane < (uint32_t)NTOK) sbuf[b * NTOK + 32 * j + lane] = cur[j];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&scal[b]);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int e = warp - C::kEpiBase;
+        const int quad = warp & 3;
+        const int cgrp = e >> 2;
+        const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16);
+        const uint32_t lrow = 32 * quad + lane;
+        grid_dep_wait();  // scales come from, and the output is shared with, earlier kernels
+        for (uint32_t it = 0; it < niter; ++it) {
+            const uint32_t b = it % C::kAcc;
+            wait(&scal[b], (it / C::kAcc) & 1, 32);
+            wait(&accf[b], (it / C::kAcc) & 1, 16);
+            tc_fence_after();
+            constexpr int kF = C::kInFlight;
+#pragma unroll
+            for (int g = 0; g < kCpt / kF; ++g) {
+                float v[kF];
+                const uint32_t col = cgrp * kCpt + kF * g;
+#pragma unroll
+                for (int c = 0; c < kF / 16; ++c)
+                    tc_ld16(taddr + b * NTOK + col + 16 * c, *reinterpret_cast<float(*)[16]>(v + 16 * c));
+                tc_wait_ld();
+                const float4 *sp = reinterpret_cast<const float4 *>(sbuf + b * NTOK + col);
+#pragma unroll
+                for (int q4 = 0; q4 < kF / 4; ++q4) {
+                    const float4 s4 = sp[q4];
+                    float *t = total + kF * g + 4 * q4;
+                    t[0] = fmaf(v[4 * q4 + 0], s4.x, t[0]);
+                    t[1] = fmaf(v[4 * q4 + 1], s4.y, t[1]);
+                    t[2] = fmaf(v[4 * q4 + 2], s4.z, t[2]);
+                    t[3] = fmaf(v[4 * q4 + 3], s4.w, t[3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[b]);
+            // the range leaves this tile: a tile this CTA covers whole is
+            // stored, the part of a tile shared with a neighbour is added
+            const uint32_t u = u0 + it;
+            if (it + 1 == niter || (u + 1) % a.kb == 0) {
+                const uint32_t tile = u / a.kb;
+                const bool whole = tile * a.kb >= u0 && (tile + 1) * a.kb <= u1;
+                const uint32_t row = tile * kTileRows + lrow;
+                if (row < a.n && !*abort_flag) {
+                    float *orow = reinterpret_cast<float *>(a.out) + row + (size_t)(cgrp * kCpt) * a.ldc;
+                    const uint32_t nt = a.m > (uint32_t)(cgrp * kCpt) ? a.m - cgrp * kCpt : 0u;  // valid tokens here
+                    if (whole) {
+#pragma unroll
+                        for (int j = 0; j < kCpt; ++j)
+                            if ((uint32_t)j < nt) orow[(size_t)j * a.ldc] = total[j];
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < kCpt; ++j)
+                            if ((uint32_t)j < nt) atomicAdd(orow + (size_t)j * a.ldc, total[j]);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kCpt; ++j) total[j] = 0.0f;
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- drain after a timeout
+    __syncthreads();
+    grid_dep_launch();
+    if (*abort_flag) {
+        if (warp == 0 && lane == 0) {
+            const uint32_t first = issued > (uint32_t)C::kStages ? issued - C::kStages : 0;
+            for (uint32_t it = first; it < issued; ++it)
+                mbar_wait(&full[it % C::kStages], (it / C::kStages) & 1, a.wait_limit_ns);
+        }
+        if (warp == 1 && lane == 0) mbar_wait(done, 0, a.wait_limit_ns);
+        __syncthreads();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols)
+                     : "memory");
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 // Cluster reduction of one split CTA, in K-block units: its partials grow
@@ -729,6 +1023,51 @@ cudaError_t launch_tc_rows(const W8A8Args &a, const CUtensorMap (&maps)[7], uint
     }
 }
 
+// Stream-K: one CTA per resident slot (the same shared memory and threads as
+// the split-K Block128 variant, no cluster), at most one unit each.
+template <int NTOK>
+cudaError_t launch_streamk_variant(const W8A8Args &a, const CUtensorMap (&maps)[7], cudaStream_t s) {
+    using C = Tc<NTOK, true, false>;
+    static std::mutex mu;
+    static std::vector<uint32_t> slots;  // per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    uint32_t p;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if ((int)slots.size() <= dev) slots.resize(dev + 1, 0);
+        if (slots[dev] == 0) {
+            const void *f = (const void *)w8a8_streamk_kernel<NTOK>;
+            cudaFuncSetAttribute(w8a8_streamk_kernel<NTOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kAlloc);
+            slots[dev] = (uint32_t)(resident_ctas(f, C::kThreads, C::kAlloc, C::kTmemCols) * device_sm_count());
+        }
+        p = slots[dev];
+    }
+    const uint64_t units = (uint64_t)((a.n + kTileRows - 1) / kTileRows) * a.kb;
+    if (units < p) p = (uint32_t)units;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p, 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kAlloc;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = QDL_TUNE_PDL ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, w8a8_streamk_kernel<NTOK>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+                              maps[6], a);
+}
+
+cudaError_t launch_streamk_rows(const W8A8Args &a, const CUtensorMap (&maps)[7], uint32_t ntok, cudaStream_t s) {
+    static_assert(QDL_STREAMK_MIN_NTOK >= 32 && QDL_STREAMK_MAX_NTOK <= 128, "stream-K is instantiated for 32..128");
+    switch (ntok) {
+        case 32: return launch_streamk_variant<32>(a, maps, s);
+        case 64: return launch_streamk_variant<64>(a, maps, s);
+        default: return launch_streamk_variant<128>(a, maps, s);
+    }
+}
+
 cudaError_t weight_maps(const W8A8Args &a, const uint8_t *const seg_w[3], const uint32_t seg_n[3],
                         CUtensorMap (&maps)[7]) {
     for (int i = 0; i < 3; ++i) {  // 16-row boxes x3, 128-row boxes x3
@@ -757,7 +1096,13 @@ cudaError_t launch_w8a8_gemm_tc(const W8A8Args &a, int format, const uint8_t *co
     const uint32_t ntok = tc_bucket(a.m);
     e = make_tmap_u8(&maps[6], a.q, a.k, a.m, a.k, 128, ntok);
     if (e != cudaSuccess) return e;
+    if (a.accumulate && w8a8_streamk_applies(format, a.m)) return launch_streamk_rows(a, maps, ntok, s);
     return format == QDL_SCALE_BLOCK128 ? launch_tc_rows<true>(a, maps, ntok, s) : launch_tc_rows<false>(a, maps, ntok, s);
+}
+
+bool w8a8_streamk_applies(int format, uint32_t rows) {
+    const uint32_t ntok = tc_bucket(rows);
+    return format == QDL_SCALE_BLOCK128 && ntok >= QDL_STREAMK_MIN_NTOK && ntok <= QDL_STREAMK_MAX_NTOK;
 }
 
 // Block128 projection with the activation quantisation fused in (rows <= 16):

@@ -70,7 +70,8 @@ def test_chain_of_gemvs_writing_one_output():
 
 
 @pytest.mark.parametrize("fmt,n,k,rows", [(qdl.BLOCK128, 6144, 4096, 8), (qdl.PER_ROW, 1024, 1024, 1),
-                                          (qdl.BLOCK128, 28672, 8192, 256), (qdl.PER_ROW, 4096, 14336, 64)])
+                                          (qdl.BLOCK128, 28672, 8192, 256), (qdl.PER_ROW, 4096, 14336, 64),
+                                          (qdl.BLOCK128, 28672, 8192, 64), (qdl.BLOCK128, 6144, 4096, 20)])
 def test_plan_is_consistent(fmt, n, k, rows):
     codes = torch.zeros((n, k), dtype=torch.uint8, device="cuda")
     scale = torch.ones(((n + 127) // 128 * (k // 128)) if fmt == qdl.BLOCK128 else n, device="cuda")
@@ -85,3 +86,7 @@ def test_plan_is_consistent(fmt, n, k, rows):
     assert p["proj_launches"] in (1, 2)
     if fmt == qdl.PER_ROW or rows > 16:
         assert p["proj_launches"] == 2
+    # the f32 projection accumulates when K is split or Block128 runs stream-K
+    streamk = fmt == qdl.BLOCK128 and 16 < rows <= 128
+    assert p["proj_accumulates"] == (1 if p["split_k"] > 1 or streamk else 0)
+    assert p["proj_streamk"] == (1 if streamk else 0)

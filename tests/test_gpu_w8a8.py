@@ -70,10 +70,14 @@ def test_proj_segments_and_ragged_n(fmt, sizes, k, rows):
 
 
 @pytest.mark.parametrize("fmt", [qdl.PER_ROW, qdl.BLOCK128])
-@pytest.mark.parametrize("n,k,rows", [(384, 384, 3), (256, 8192, 8), (6144, 4096, 8), (1024, 14336, 64)])
+@pytest.mark.parametrize("n,k,rows", [(384, 384, 3), (256, 8192, 8), (6144, 4096, 8), (1024, 14336, 64),
+                                      (2048, 4096, 100), (640, 1024, 256), (1000, 2048, 33), (128, 8192, 128),
+                                      (768, 2048, 20)])
 def test_gemv_accumulating_output(fmt, n, k, rows):
     """QDL_OUT_F32_ADD adds y to the values already in out, with the split-K
-    partial sums added atomically (shapes cover unsplit and split plans)"""
+    partial sums added atomically (shapes cover unsplit and split plans, and,
+    for Block128 with 17 to 128 rows, the stream-K kernel with tiles shared
+    by two CTAs and ragged N)"""
     segs = _segments(fmt, k, [n], seed=n + rows)
     x = syn.bf16_normal((rows, k), seed=7 + rows)
     qo, so = oracle.act_quant(fmt, x, k)
