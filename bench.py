@@ -153,14 +153,11 @@ class Int4Case:
         n_tot = wl.nq + 2 * wl.nkv
         self.step_bytes = self.weight_bytes + x.nbytes + rows * n_tot * 4
         self.gemv_bytes = self.step_bytes
-        # the library's dispatch for widths multiple of 32 and group 128: the
-        # CUDA-core kernel for up to 2 rows, else tcgen05 passes of 32 rows
-        if rows <= 2:
-            self.gemv_launches, self.kernel, self.kernel_src = 1, "int4_qkv_cc_kernel", ["int4_qkv_cc.cu"]
-        else:
-            self.gemv_launches = math.ceil(rows / 32)
-            self.kernel, self.kernel_src = "int4_qkv_tc_kernel", ["int4_qkv_tc.cu"]
-        self.launches_per_step = self.gemv_launches
+        # the library's dispatch for widths multiple of 32 and group 128:
+        # tcgen05 passes of 32 rows, each an output-zeroing launch and the GEMV
+        self.gemv_launches = math.ceil(rows / 32)
+        self.kernel, self.kernel_src = "int4_qkv_tc_kernel", ["int4_qkv_tc.cu"]
+        self.launches_per_step = 2 * self.gemv_launches
 
     def step(self, i):
         s = self.sets[i % self.copies]

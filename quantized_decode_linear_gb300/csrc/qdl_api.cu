@@ -364,12 +364,14 @@ qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq
         return fail(QDL_ERR_INVALID_ARG, "%s: nq=%u, nkv=%u (want positive multiples of 8)", who, nq, nkv);
     if (!aligned(x, 16)) return fail(QDL_ERR_INVALID_ARG, "%s: x must be 16-byte aligned", who);
     bool vec2 = nq % 16 == 0 && nkv % 16 == 0;
+    bool qw16 = true;  // the TMA kernels stream codes from 16-byte aligned bases
     for (int p = 0; p < 3; ++p) {
         if (qw[p] == nullptr || sc[p] == nullptr || zr[p] == nullptr || out[p] == nullptr)
             return fail(QDL_ERR_INVALID_ARG, "%s: projection %d has a NULL pointer", who, p);
         if (!aligned(qw[p], 4) || !aligned(sc[p], 16) || !aligned(zr[p], 16) || !aligned(out[p], 4))
             return fail(QDL_ERR_INVALID_ARG, "%s: projection %d misaligned (qw 4, sc/zr 16, out 4 bytes)", who, p);
         vec2 = vec2 && aligned(qw[p], 8);
+        qw16 = qw16 && aligned(qw[p], 16);
     }
     Int4Args a = {};
     a.qw0 = qw[0]; a.qw1 = qw[1]; a.qw2 = qw[2];
@@ -384,11 +386,11 @@ qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq
     a.tiles_kv = (nkv + 127) / 128;
     a.vec2 = vec2;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // widths multiples of 32: the CUDA-core kernel for up to 2 rows, and for
-    // 3-4 rows where the tcgen05 kernel does not apply; more rows: the tcgen05
-    // kernel (group 128, widths multiples of 32), 32 rows per pass, otherwise
-    // the mma.sync kernel, 16 rows per pass
-    if (int4_cc_supported(nq, nkv) && (m <= 2 || (m <= 4 && !int4_tc_supported(nq, nkv, group)))) {
+    // group 128 and widths multiples of 32: the tcgen05 kernel, 32 rows per
+    // pass; other widths multiples of 32: the CUDA-core kernel for up to 4
+    // rows; otherwise the mma.sync kernel, 16 rows per pass
+    const bool tc = qw16 && int4_tc_supported(nq, nkv, group);
+    if (qw16 && int4_cc_supported(nq, nkv) && (m <= QDL_INT4_CC_MAX_ROWS || (m <= 4 && !tc))) {
         a.x = x;
         a.out0 = out[0];
         a.out1 = out[1];
@@ -398,7 +400,6 @@ qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq
         if (e != cudaSuccess) return cuda_fail(who, e);
         return ok();
     }
-    const bool tc = int4_tc_supported(nq, nkv, group);
     const uint32_t chunk = tc ? 32 : 16;
     for (uint32_t done = 0; done < m; done += chunk) {
         const uint32_t mm = m - done < chunk ? m - done : chunk;

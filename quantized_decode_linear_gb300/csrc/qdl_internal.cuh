@@ -17,6 +17,11 @@ namespace qdl {
 // K range on the critical path.
 #define QDL_TUNE_FUSED 0
 #endif
+#ifndef QDL_INT4_CC_MAX_ROWS
+// token rows up to which the AWQ projection takes the CUDA-core kernel even
+// where the tcgen05 kernel applies (0: never)
+#define QDL_INT4_CC_MAX_ROWS 0
+#endif
 #ifndef QDL_TUNE_PDL
 #define QDL_TUNE_PDL 1  // programmatic dependent launch between the library's kernels
 #endif

@@ -37,11 +37,13 @@ def test_int4_small(m, k, nq, nkv, group):
         check_close(outs[p], ref[p], bound[p], what=f"proj {p}")
 
 
-@pytest.mark.parametrize("m", [9, 16, 17, 32, 33, 70])
-@pytest.mark.parametrize("k,nq,nkv", [(128, 96, 32), (256, 128, 128), (2048, 640, 160), (1024, 4096, 1024)])
+@pytest.mark.parametrize("m", [1, 2, 9, 16, 17, 32, 33, 70])
+@pytest.mark.parametrize("k,nq,nkv", [(128, 96, 32), (256, 128, 128), (2048, 640, 160), (1024, 4096, 1024),
+                                      (16384, 128, 32)])
 def test_int4_tensor_core_path(m, k, nq, nkv):
-    """more than 8 rows, group 128 and widths multiple of 32: the tcgen05
-    kernel (ragged last tiles, several passes of 32 rows)"""
+    """group 128 and widths multiple of 32: the tcgen05 kernel (ragged last
+    128-column tiles, K ranges from one 64-row unit to more units per CTA than
+    its code ring holds, several passes of 32 rows)"""
     group = 128
     x = syn.normal_f32((m, k), seed=2 * m + k)
     ws = [syn.int4_awq(k, n, group, seed=p + 3 * nq) for p, n in enumerate((nq, nkv, nkv))]
@@ -56,10 +58,10 @@ def test_int4_tensor_core_path(m, k, nq, nkv):
 @pytest.mark.parametrize("k,nq,nkv,group", [(128, 32, 32, 128), (1040, 96, 32, 16), (512, 288, 64, 32),
                                             (4096, 512, 256, 64), (2048, 640, 160, 128), (8192, 32, 64, 128)])
 def test_int4_cuda_core_path(m, k, nq, nkv, group):
-    """widths multiple of 32 with 1-2 rows (1-4 rows for group != 128): the
-    CUDA-core kernel (ragged 256-column tiles, K not a multiple of its 64-row
-    stage, groups 16..128, split-K clusters up to 8); the other cases here
-    cover the tcgen05 kernel's small-row passes"""
+    """widths multiple of 32 with 1-4 rows and group != 128: the CUDA-core
+    kernel (ragged 256-column tiles, K not a multiple of its 64-row stage,
+    groups 16..64, split-K clusters up to 8); the group-128 cases here cover
+    the tcgen05 kernel's small-row passes"""
     x = syn.normal_f32((m, k), seed=5 * m + k)
     ws = [syn.int4_awq(k, n, group, seed=p + 7 * nq) for p, n in enumerate((nq, nkv, nkv))]
     outs = _run(x, nq, nkv, group, ws)
