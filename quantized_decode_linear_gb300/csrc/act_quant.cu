@@ -42,12 +42,20 @@ __device__ __forceinline__ float quant_operand(float v, float scale) {
 
 // ---------------------------------------------------------------- Block128
 
-// Programmatic launch overlap: the input comes from the previous kernel and
-// the scratch written here may still be read by it, so wait for it first;
-// then let the next kernel (the GEMV) start streaming its weights at once.
+// Programmatic launch overlap: let the next kernel (the GEMV) launch at once,
+// so that its CTAs take SMs as the previous kernel's CTAs leave and start
+// streaming their weights; then wait for the previous kernel, since the input
+// comes from it and the scratch written here may still be read by it.  (The
+// GEMV reads this kernel's output only after its own dependency wait, which
+// returns when this grid has completed.)
 __device__ __forceinline__ void dependent_launch_prologue() {
+#if QDL_TUNE_EARLY_TRIGGER
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#else
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
 }
 
 template <bool kSilu>

@@ -22,6 +22,12 @@ namespace qdl {
 // where the tcgen05 kernel applies (0: never)
 #define QDL_INT4_CC_MAX_ROWS 0
 #endif
+#ifndef QDL_TUNE_EARLY_TRIGGER
+// 1: the activation quantiser releases the GEMV before its own dependency
+// wait, so consecutive calls overlap (the next GEMV streams weights while the
+// previous one finishes)
+#define QDL_TUNE_EARLY_TRIGGER 1
+#endif
 #ifndef QDL_TUNE_PDL
 #define QDL_TUNE_PDL 1  // programmatic dependent launch between the library's kernels
 #endif
@@ -59,6 +65,7 @@ struct W8A8Args {
     uint32_t debug_skip_iter;  // self-test only: pipeline stage never loaded (else ~0u)
     uint64_t wait_limit_ns;    // limit of every device-side wait
     uint32_t accumulate;       // f32 output is zero: split-K ranks add their partials atomically
+    uint32_t early_trigger;    // set by the launcher: release dependent kernels at the start
     // fused projection only: bf16 input [m, ldx] and the scratch it fills
     const void *x;
     uint32_t ldx;
