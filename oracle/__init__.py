@@ -17,6 +17,10 @@ Functions and what they follow (the C source restates each in a comment):
   1..3 segments (``W8a8Weight::boundaries``), dequantise-then-dot in double.
 * ``int4_qkv`` -- fused_int4_qkv.rs, ``fused_int4_qkv_{q,k,v}`` with
   ``unpack_awq_qkv`` and the shift table ``QKV_AWQ_SHIFTS``.
+* ``kv_quant_int8`` / ``kv_dequant_int8`` / ``kv_quant_int4`` /
+  ``kv_dequant_int4`` -- kv_cache_quant.wgsl: per-token symmetric int8 (the
+  page's "FP8" and INT8 per-token kernels) and per-group asymmetric INT4 with
+  two codes per byte.
 """
 from __future__ import annotations
 
@@ -74,6 +78,10 @@ def _load():
             lib.orc_w8a8_gemv.argtypes = [I, P, P, I, I, I, P, P, P, P, P]
             lib.orc_w8a8_gemv_sampled.argtypes = [I, P, P, I, I, I, P, P, P, P, P, I, P, P]
             lib.orc_int4_qkv.argtypes = [P, I, I, I, I, I, P, P, P, P, P]
+            lib.orc_kv_quant_int8.argtypes = [P, I, I, P, P]
+            lib.orc_kv_dequant_int8.argtypes = [P, P, I, I, P]
+            lib.orc_kv_quant_int4.argtypes = [P, S, I, P, P, P]
+            lib.orc_kv_dequant_int4.argtypes = [P, P, P, S, I, P]
             lib.orc_num_threads.restype = I
             _lib = lib
     return _lib
@@ -205,3 +213,44 @@ def int4_qkv(x, nq: int, nkv: int, group: int, qw, sc, zr):
     _load().orc_int4_qkv(_ptr(x), m, k, nq, nkv, group, arr(qw), arr(sc), arr(zr),
                          arr(outs), arr(bounds))
     return outs, bounds
+
+
+def kv_quant_int8(x):
+    """x f32 [tokens, dim] -> (codes int8 [tokens, dim], scales f32 [tokens])."""
+    x = _c(x, np.float32)
+    t, d = x.shape
+    q = np.empty((t, d), np.int8)
+    s = np.empty((t,), np.float32)
+    _load().orc_kv_quant_int8(_ptr(x), t, d, _ptr(q), _ptr(s))
+    return q, s
+
+
+def kv_dequant_int8(q, s):
+    q = _c(q, np.int8)
+    s = _c(s, np.float32)
+    t, d = q.shape
+    out = np.empty((t, d), np.float32)
+    _load().orc_kv_dequant_int8(_ptr(q), _ptr(s), t, d, _ptr(out))
+    return out
+
+
+def kv_quant_int4(x, group: int):
+    """x f32 (any shape, flattened) -> (packed uint8 [n/2], scale f32 [n/group],
+    zero f32 [n/group])."""
+    x = _c(x, np.float32).reshape(-1)
+    n = x.size
+    assert group > 0 and group % 2 == 0 and n % group == 0
+    packed = np.empty((n // 2,), np.uint8)
+    sc = np.empty((n // group,), np.float32)
+    zr = np.empty((n // group,), np.float32)
+    _load().orc_kv_quant_int4(_ptr(x), n, group, _ptr(packed), _ptr(sc), _ptr(zr))
+    return packed, sc, zr
+
+
+def kv_dequant_int4(packed, scale, zero, n: int, group: int):
+    packed = _c(packed, np.uint8).reshape(-1)
+    scale = _c(scale, np.float32)
+    zero = _c(zero, np.float32)
+    out = np.empty((n,), np.float32)
+    _load().orc_kv_dequant_int4(_ptr(packed), _ptr(scale), _ptr(zero), n, group, _ptr(out))
+    return out

@@ -352,3 +352,106 @@ void orc_int4_qkv(const float *x, int m, int k, int nq, int nkv, int group,
         }
     }
 }
+
+/* ---------------------------------------------------------------------
+ * KV-cache quantisation (kv_cache_quant.wgsl).
+ *
+ * Per-token symmetric int8 (the page's quantize_kv_fp8_per_token_f32 and
+ * quantize_kv_int8_f32 compute the same thing; the "FP8" name does not match
+ * its arithmetic, which scales to 127 and rounds to integers): per token row,
+ *   s = max(absmax / 127, 1e-8),  q = clamp(round(v / s), -128, 127)
+ * with WGSL round() (nearest integer, halves to even); dequantisation is
+ * q * s.  The page stores each code in its own u32 word; here codes are int8
+ * bytes, the same values.
+ *
+ * Per-group asymmetric INT4 (quantize_kv_int4_f32 / dequantize_kv_int4_f32):
+ * groups are consecutive runs of `group` values of the flattened
+ * [tokens, head_dim] array;
+ *   scale = (max - min) / 15,  zero = -min / max(scale, 1e-8),
+ *   q = clamp(round((v - min) / max(scale, 1e-8)), 0, 15),
+ *   dequantised v = q * scale - zero * scale.
+ * Two codes per byte: flattened element e sits in byte e / 2, the low nibble
+ * for even e.  The page writes zeros at scales[num_tokens + group], which
+ * overlaps the scales once there are more groups than tokens; here zeros
+ * have an array of their own.
+ *
+ * Every step is one binary32 operation rounded to nearest (the file is
+ * built without contraction), so codes and dequantised values are exact.
+ * ------------------------------------------------------------------- */
+
+/* WGSL round(): nearest integer, halves to even, for any finite float */
+static double round_wgsl(float v) {
+    double a = fabs((double)v);
+    double r = round_half_even(a);
+    return v < 0 ? -r : r;
+}
+
+void orc_kv_quant_int8(const float *x, int tokens, int dim, int8_t *q, float *s) {
+    for (int t = 0; t < tokens; ++t) {
+        const float *row = x + (size_t)t * dim;
+        float mx = 0.0f;
+        for (int d = 0; d < dim; ++d) {
+            float a = fabsf(row[d]);
+            if (a > mx) mx = a;
+        }
+        float sc = mx / 127.0f;
+        if (!(sc > 1e-8f)) sc = 1e-8f;
+        s[t] = sc;
+        for (int d = 0; d < dim; ++d) {
+            float r = row[d] / sc;
+            double qi = round_wgsl(r);
+            if (qi < -128.0) qi = -128.0;
+            if (qi > 127.0) qi = 127.0;
+            q[(size_t)t * dim + d] = (int8_t)qi;
+        }
+    }
+}
+
+void orc_kv_dequant_int8(const int8_t *q, const float *s, int tokens, int dim, float *out) {
+    for (int t = 0; t < tokens; ++t)
+        for (int d = 0; d < dim; ++d) {
+            size_t i = (size_t)t * dim + d;
+            out[i] = (float)q[i] * s[t];
+        }
+}
+
+void orc_kv_quant_int4(const float *x, size_t n, int group, uint8_t *packed, float *scale, float *zero) {
+    size_t groups = n / (size_t)group;
+    memset(packed, 0, n / 2);
+    for (size_t g = 0; g < groups; ++g) {
+        const float *v = x + g * (size_t)group;
+        float mn = v[0], mx = v[0];
+        for (int i = 0; i < group; ++i) {
+            if (v[i] < mn) mn = v[i];
+            if (v[i] > mx) mx = v[i];
+        }
+        float sc = (mx - mn) / 15.0f;
+        float den = sc > 1e-8f ? sc : 1e-8f;
+        float z = -mn / den;
+        scale[g] = sc;
+        zero[g] = z;
+        for (int i = 0; i < group; ++i) {
+            float r = (v[i] - mn) / den;
+            double qi = round_wgsl(r);
+            if (qi < 0.0) qi = 0.0;
+            if (qi > 15.0) qi = 15.0;
+            size_t e = g * (size_t)group + (size_t)i;
+            if (e % 2 == 0)
+                packed[e / 2] = (uint8_t)((packed[e / 2] & 0xF0) | (uint8_t)qi);
+            else
+                packed[e / 2] = (uint8_t)((packed[e / 2] & 0x0F) | ((uint8_t)qi << 4));
+        }
+    }
+}
+
+void orc_kv_dequant_int4(const uint8_t *packed, const float *scale, const float *zero, size_t n, int group,
+                         float *out) {
+    for (size_t e = 0; e < n; ++e) {
+        size_t g = e / (size_t)group;
+        uint8_t b = packed[e / 2];
+        int qi = (e % 2) ? (b >> 4) & 0xF : b & 0xF;
+        float a = (float)qi * scale[g];
+        float c = zero[g] * scale[g];
+        out[e] = a - c;
+    }
+}

@@ -21,6 +21,9 @@
  *   - The AWQ INT4 fused-QKV GEMV of fused_int4_qkv.rs (QKV_AWQ_SHIFTS,
  *     unpack_awq_qkv, fused_int4_qkv_q/_k/_v): f32 dequantisation exactly as
  *     the shader writes it, dot product accumulated in double.
+ *   - The KV-cache quantisers of kv_cache_quant.wgsl: per-token symmetric
+ *     int8 and per-group asymmetric INT4 with two codes per byte, and their
+ *     dequantisers, step for step in binary32.
  *
  * Parity pins: every function is checked against values fixed by the pages
  * and the mathematics in tests/test_oracle_*.py (hand-computed nibble and
@@ -78,6 +81,17 @@ void orc_int4_qkv(const float *x, int m, int k, int nq, int nkv, int group,
                   const uint32_t *const *qw, const float *const *sc,
                   const float *const *zr, double *const *out,
                   double *const *bound);
+
+/* KV-cache quantisation (kv_cache_quant.wgsl): per-token symmetric int8,
+ * x [tokens, dim] -> q int8 [tokens, dim], s [tokens]; per-group asymmetric
+ * INT4 over the flattened x [n] (n % group == 0, group even) -> packed
+ * [n / 2] (two codes per byte, even element in the low nibble), scale and
+ * zero [n / group]. */
+void orc_kv_quant_int8(const float *x, int tokens, int dim, int8_t *q, float *s);
+void orc_kv_dequant_int8(const int8_t *q, const float *s, int tokens, int dim, float *out);
+void orc_kv_quant_int4(const float *x, size_t n, int group, uint8_t *packed, float *scale, float *zero);
+void orc_kv_dequant_int4(const uint8_t *packed, const float *scale, const float *zero, size_t n, int group,
+                         float *out);
 
 int orc_num_threads(void);
 
