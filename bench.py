@@ -184,6 +184,86 @@ class Int4Case:
                       f"({self.copies * self.weight_bytes / 1e6:.0f} MB)"}
 
 
+class KvCase:
+    """KV-cache quantiser workload: a step quantises one block of rows and
+    dequantises another (long untouched) block; blocks rotate over enough
+    copies that every step streams from HBM."""
+
+    def __init__(self, wl, rows, torch, qdl, syn, l2_bytes):
+        self.wl, self.rows, self.qdl = wl, rows, qdl
+        n = rows * wl.head_dim
+        self.n = n
+        x = syn.kv_values(wl, rows)
+        self.int4 = wl.group > 0
+        code_bytes = n // 2 if self.int4 else n
+        side = (n // wl.group) * 8 if self.int4 else rows * 4  # scales (+ zeros)
+        per_copy = 4 * n + code_bytes + side + 4 * n
+        self.copies = max(2, math.ceil(4 * l2_bytes / per_copy))
+        dev = torch.from_numpy(x).cuda()
+        self.x = [dev] + [dev.clone() for _ in range(self.copies - 1)]
+        self.out = [torch.empty_like(dev) for _ in range(self.copies)]
+        if self.int4:
+            self.q = [torch.empty((n // 2,), dtype=torch.uint8, device="cuda") for _ in range(self.copies)]
+            self.s = [torch.empty((n // wl.group,), dtype=torch.float32, device="cuda") for _ in range(self.copies)]
+            self.z = [torch.empty((n // wl.group,), dtype=torch.float32, device="cuda") for _ in range(self.copies)]
+        else:
+            self.q = [torch.empty((rows, wl.head_dim), dtype=torch.int8, device="cuda") for _ in range(self.copies)]
+            self.s = [torch.empty((rows,), dtype=torch.float32, device="cuda") for _ in range(self.copies)]
+            self.z = [None] * self.copies
+        for i in range(self.copies):  # every block holds valid codes before the first dequantisation
+            self._quant(i)
+        self.x_host = torch.from_numpy(x).pin_memory()
+        self.out_host = torch.empty(x.shape, dtype=torch.float32).pin_memory()
+        self.weight_bytes = 0
+        # algorithmic bytes: quantise (read x, write codes + side data) and
+        # dequantise (read codes + side data, write values)
+        self.gemv_bytes = 4 * n + code_bytes + side
+        self.step_bytes = self.gemv_bytes + code_bytes + side + 4 * n
+        self.gemv_launches, self.launches_per_step = 1, 2
+        self.kernel = "kv_quant_int4_kernel" if self.int4 else "kv_quant_int8_kernel"
+        self.kernel_src = ["kv_quant.cu"]
+        self.dtype = "u4" if self.int4 else "int8"
+
+    def _quant(self, i):
+        wl, r, d = self.wl, self.rows, self.wl.head_dim
+        if self.int4:
+            self.qdl.kv_quant_int4(self.x[i], r, d, wl.group, self.q[i], self.s[i], self.z[i])
+        else:
+            self.qdl.kv_quant_int8(self.x[i], r, d, self.q[i], self.s[i])
+
+    def _dequant(self, i):
+        wl, r, d = self.wl, self.rows, self.wl.head_dim
+        if self.int4:
+            self.qdl.kv_dequant_int4(self.q[i], self.s[i], self.z[i], r, d, wl.group, self.out[i])
+        else:
+            self.qdl.kv_dequant_int8(self.q[i], self.s[i], r, d, self.out[i])
+
+    def step(self, i):
+        self._quant(i % self.copies)
+        self._dequant((i + self.copies // 2) % self.copies)
+
+    def dominant(self, i):
+        self._quant(i % self.copies)
+
+    def e2e_step(self, i):
+        c = i % self.copies
+        self.x[c].copy_(self.x_host, non_blocking=True)
+        self._quant(c)
+        self._dequant(c)
+        self.out_host.copy_(self.out[c], non_blocking=True)
+
+    def e2e_bytes(self):
+        return self.x_host.numel() * 4, self.out_host.numel() * 4
+
+    def describe(self):
+        wl = self.wl
+        return {"workload": wl.name, "rows": self.rows, "head_dim": wl.head_dim,
+                "codec": f"int4 group {wl.group}" if self.int4 else "int8 per token",
+                "copies": self.copies,
+                "l2": f"inputs larger than L2: blocks rotate over {self.copies} copies "
+                      f"({self.copies * (8 * self.n) / 1e6:.0f} MB of values)"}
+
+
 # ---------------------------------------------------------------- timing helpers
 
 def _graph(torch, fn, start, count):
@@ -253,6 +333,21 @@ def _oracle_step_fn(wl, rows, syn, fraction):
     """returns (fn, bytes_equiv, sample description) for one oracle step on a
     fraction of the workload's output columns"""
     import oracle
+    if hasattr(wl, "head_dim"):
+        take = max(64, int(round(rows * fraction)))
+        x = syn.kv_values(wl, take)
+        n = take * wl.head_dim
+
+        def fn():
+            if wl.group:
+                p, sc, zr = oracle.kv_quant_int4(x, wl.group)
+                oracle.kv_dequant_int4(p, sc, zr, n, wl.group)
+            else:
+                q, s = oracle.kv_quant_int8(x)
+                oracle.kv_dequant_int8(q, s)
+        code = n // 2 if wl.group else n
+        side = (n // wl.group) * 8 if wl.group else take * 4
+        return fn, 8 * n + 2 * (code + side), f"quantise + dequantise {take} of {rows} rows"
     if hasattr(wl, "fmt"):
         segs = syn.w8a8_weights(wl)
         xb = syn.w8a8_activations(wl, rows)
@@ -332,7 +427,8 @@ def run_reference(args, rank, world):
     value = b * args.steps / dt / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if hasattr(wl, "head_dim") else "f64",
             "data": "synthetic",
             "config": {"workload": wl.name, "rows": rows, "parallelism": "replicas"},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
@@ -358,7 +454,7 @@ def run_gpu(args, rank, world, local_rank):
 
     wl = syn.WORKLOADS[args.workload]
     rows = args.rows or wl.rows[0]
-    Case = W8A8Case if hasattr(wl, "fmt") else Int4Case
+    Case = W8A8Case if hasattr(wl, "fmt") else KvCase if hasattr(wl, "head_dim") else Int4Case
     case = Case(wl, rows, torch, qdl, syn, l2)
 
     # graphs covering exactly K steps: up to four distinct graphs of c calls
@@ -455,7 +551,7 @@ def run_gpu(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": warm, "ms_per_step": ms / steps, "us_per_call": ms / steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3" if Case is W8A8Case else "f16", "data": "synthetic",
+        "dtype": "e4m3" if Case is W8A8Case else getattr(case, "dtype", "f16"), "data": "synthetic",
         "config": dict(case.describe(), parallelism="replicas" if world > 1 else "single"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,

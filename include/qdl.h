@@ -187,18 +187,60 @@ QDL_API qdl_status qdl_w8a8_proj_silu(const qdl_w8a8_weight *w, const void *gate
  *            nq, nkv multiples of 16 enables 8-byte weight loads).
  *   sc[p], zr[p] : device f32 [k/group, n], 16-byte aligned.
  *   out[p] : device f32 [m, n], 4-byte aligned.
- * With nq, nkv multiples of 32, up to 2 rows (up to 4 when group != 128)
- * take one CUDA-core pass that multiplies f32 x with exact nibbles in f32 and
- * applies zeros and scales per group.  Otherwise the tensor cores multiply x
- * rounded to f16 with exact nibbles and apply zeros and scales per group in
- * f32 (error within 2^-11 of sum |x w|): with group 128 and nq, nkv multiples
- * of 32 the tcgen05 kernel streams the weights once per 32 rows, other shapes
- * an mma.sync kernel once per 16 rows.  Checks: m >= 1; k >= 1; group > 0,
+ * With group 128, nq and nkv multiples of 32 and every qw[p] 16-byte aligned,
+ * the tcgen05 kernel streams the weights once per 32 rows (two launches per
+ * pass: out is zeroed, then the GEMV adds per-tile partial sums into it with
+ * f32 atomics, so the order of those additions varies from run to run); it
+ * multiplies x rounded to f16 with exact nibbles (error within 2^-11 of
+ * sum |x w|) and applies zeros and scales per group in f32.  Other widths
+ * that are multiples of 32 take, for up to 4 rows, one CUDA-core pass in f32;
+ * every other shape an mma.sync kernel (x rounded to f16) once per 16 rows.
+ * Checks: m >= 1; k >= 1; group > 0,
  * group % 16 == 0, k % group == 0; nq, nkv > 0 and multiples of 8; no NULL
  * pointer; alignments above. */
 QDL_API qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq, uint32_t nkv,
                              uint32_t group, const uint32_t *const *qw, const float *const *sc,
                              const float *const *zr, float *const *out, void *stream);
+
+/* ------------------------------------------------------------------
+ * KV-cache quantisers (kv_cache_quant.wgsl: quantize_kv_fp8_per_token_f32,
+ * quantize_kv_int8_f32, quantize_kv_int4_f32 and the dequantize_* kernels).
+ * The page's "FP8" per-token kernel and its INT8 one compute the same thing,
+ * symmetric int8, so one pair of entry points serves both.  Every step is
+ * one binary32 operation rounded to nearest; round() takes halves to even.
+ * Arguments are device pointers; calls are asynchronous on `stream`; on an
+ * invalid argument nothing is launched and qdl_last_error() explains.
+ * Shapes: x and out are [tokens, head_dim] f32 (row-major, 16-byte aligned);
+ * tokens >= 1, head_dim a positive multiple of 4, tokens * head_dim < 2^31.
+ * ------------------------------------------------------------------ */
+
+/* Per token t:  scale[t] = max(absmax_d |x[t,d]| / 127, 1e-8),
+ *               q[t,d] = clamp(round(x[t,d] / scale[t]), -128, 127).
+ * q: int8 [tokens, head_dim] (the page keeps each code in a u32 word; the
+ * values are the same), 4-byte aligned; scale: f32 [tokens]. */
+QDL_API qdl_status qdl_kv_quant_int8(const float *x, uint32_t tokens, uint32_t head_dim, int8_t *q, float *scale,
+                                     void *stream);
+
+/* out[t,d] = q[t,d] * scale[t]. */
+QDL_API qdl_status qdl_kv_dequant_int8(const int8_t *q, const float *scale, uint32_t tokens, uint32_t head_dim,
+                                       float *out, void *stream);
+
+/* Per group g of `group` consecutive values of the flattened x (group a
+ * positive multiple of 8 dividing tokens * head_dim):
+ *   scale[g] = (max - min) / 15,  zero[g] = -min / max(scale[g], 1e-8),
+ *   code = clamp(round((v - min) / max(scale[g], 1e-8)), 0, 15).
+ * packed: [tokens * head_dim / 2] bytes, two codes per byte, value e in byte
+ * e / 2, the low nibble when e is even; 4-byte aligned.  scale, zero: f32
+ * [tokens * head_dim / group], separate arrays (the page stores zeros after
+ * the scales at an offset of num_tokens, which overlaps the scales as soon as
+ * there are more groups than tokens).  A constant group gets scale 0 and
+ * dequantises to 0, as the page's formulas give. */
+QDL_API qdl_status qdl_kv_quant_int4(const float *x, uint32_t tokens, uint32_t head_dim, uint32_t group,
+                                     uint8_t *packed, float *scale, float *zero, void *stream);
+
+/* out[e] = code(e) * scale[g] - zero[g] * scale[g], g = e / group. */
+QDL_API qdl_status qdl_kv_dequant_int4(const uint8_t *packed, const float *scale, const float *zero, uint32_t tokens,
+                                       uint32_t head_dim, uint32_t group, float *out, void *stream);
 
 /* Size of the library's own device array used by qdl_w8a8_proj_static. */
 #define QDL_STATIC_SCRATCH_BYTES (4 << 20)

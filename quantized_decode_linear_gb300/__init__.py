@@ -31,6 +31,7 @@ STATUS_NAMES = {0: "QDL_OK", 1: "QDL_ERR_INVALID_ARG", 2: "QDL_ERR_SCRATCH_TOO_S
 EXPORTS = ("qdl_w8a8_weight_init", "qdl_scratch_bytes", "qdl_act_quant", "qdl_act_quant_silu",
            "qdl_w8a8_gemv", "qdl_w8a8_proj", "qdl_w8a8_proj_silu", "qdl_int4_qkv_gemv",
            "qdl_w8a8_proj_static", "qdl_w8a8_plan", "qdl_check_device_fault", "qdl_selftest_bounded_wait",
+           "qdl_kv_quant_int8", "qdl_kv_dequant_int8", "qdl_kv_quant_int4", "qdl_kv_dequant_int4",
            "qdl_last_error", "qdl_status_string")
 
 
@@ -88,6 +89,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "qdl_w8a8_proj_silu": [P, P, P, U32, U32, U32, P, I32, U32, P, P, SZ, SZ, P],
             "qdl_int4_qkv_gemv": [P, U32, U32, U32, U32, U32, P, P, P, P, P],
             "qdl_w8a8_proj_static": [P, P, U32, U32, P, I32, U32, P],
+            "qdl_kv_quant_int8": [P, U32, U32, P, P, P],
+            "qdl_kv_dequant_int8": [P, P, U32, U32, P, P],
+            "qdl_kv_quant_int4": [P, U32, U32, U32, P, P, P, P],
+            "qdl_kv_dequant_int4": [P, P, P, U32, U32, U32, P, P],
             "qdl_check_device_fault": [P],
             "qdl_w8a8_plan": [P, U32, P],
             "qdl_selftest_bounded_wait": [P, P, P, SZ, SZ, U32, P, U32, P],
@@ -249,6 +254,26 @@ def int4_qkv_gemv(x, m: int, k: int, nq: int, nkv: int, group: int, qw, sc, zr, 
     arr = lambda xs: (ctypes.c_void_p * 3)(*[_ptr(t) for t in xs])
     _check(load().qdl_int4_qkv_gemv(_ptr(x), m, k, nq, nkv, group, arr(qw), arr(sc), arr(zr), arr(out),
                                     _stream(stream)))
+
+
+def kv_quant_int8(x, tokens: int, head_dim: int, q, scale, stream=None):
+    """KV-cache per-token int8: x f32 [tokens, head_dim] -> q int8, scale f32 [tokens]."""
+    _check(load().qdl_kv_quant_int8(_ptr(x), tokens, head_dim, _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def kv_dequant_int8(q, scale, tokens: int, head_dim: int, out, stream=None):
+    _check(load().qdl_kv_dequant_int8(_ptr(q), _ptr(scale), tokens, head_dim, _ptr(out), _stream(stream)))
+
+
+def kv_quant_int4(x, tokens: int, head_dim: int, group: int, packed, scale, zero, stream=None):
+    """KV-cache per-group INT4: packed uint8 [tokens*head_dim/2], scale/zero f32 [tokens*head_dim/group]."""
+    _check(load().qdl_kv_quant_int4(_ptr(x), tokens, head_dim, group, _ptr(packed), _ptr(scale), _ptr(zero),
+                                    _stream(stream)))
+
+
+def kv_dequant_int4(packed, scale, zero, tokens: int, head_dim: int, group: int, out, stream=None):
+    _check(load().qdl_kv_dequant_int4(_ptr(packed), _ptr(scale), _ptr(zero), tokens, head_dim, group, _ptr(out),
+                                      _stream(stream)))
 
 
 def selftest_bounded_wait(w: W8A8Weight, q, q_scale, rows: int, out, limit_us: int = 20000,

@@ -414,6 +414,88 @@ qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq
     return ok();
 }
 
+// ---------------------------------------------------------------- KV-cache quantisers
+//
+// kv_cache_quant.wgsl.  Shapes: x and out [tokens, head_dim] f32; int8 codes
+// [tokens, head_dim] with scales [tokens]; INT4 over the flattened
+// tokens * head_dim values, packed two per byte, scales and zeros
+// [tokens * head_dim / group].
+
+namespace {
+
+qdl_status check_kv_shape(const char *who, uint32_t tokens, uint32_t head_dim) {
+    if (tokens < 1 || head_dim < 1 || head_dim % 4 != 0)
+        return fail(QDL_ERR_INVALID_ARG, "%s: tokens=%u, head_dim=%u (want tokens >= 1, head_dim a positive multiple of 4)",
+                    who, tokens, head_dim);
+    if ((uint64_t)tokens * head_dim >= (1ull << 31))
+        return fail(QDL_ERR_UNSUPPORTED, "%s: tokens * head_dim = %llu exceeds 2^31", who,
+                    (unsigned long long)tokens * head_dim);
+    return QDL_OK;
+}
+
+qdl_status check_kv_int4(const char *who, uint32_t tokens, uint32_t head_dim, uint32_t group) {
+    qdl_status st = check_kv_shape(who, tokens, head_dim);
+    if (st != QDL_OK) return st;
+    if (group == 0 || group % 8 != 0 || ((uint64_t)tokens * head_dim) % group != 0)
+        return fail(QDL_ERR_INVALID_ARG, "%s: group=%u (want a positive multiple of 8 dividing tokens * head_dim = %llu)",
+                    who, group, (unsigned long long)tokens * head_dim);
+    return QDL_OK;
+}
+
+}  // namespace
+
+qdl_status qdl_kv_quant_int8(const float *x, uint32_t tokens, uint32_t head_dim, int8_t *q, float *scale,
+                             void *stream) {
+    const char *who = "quantize_kv_int8";
+    qdl_status st = check_kv_shape(who, tokens, head_dim);
+    if (st != QDL_OK) return st;
+    if (x == nullptr || q == nullptr || scale == nullptr) return fail(QDL_ERR_INVALID_ARG, "%s: NULL pointer argument", who);
+    if (!aligned(x, 16) || !aligned(q, 4) || !aligned(scale, 4))
+        return fail(QDL_ERR_INVALID_ARG, "%s: x must be 16-byte, q and scale 4-byte aligned", who);
+    cudaError_t e = launch_kv_quant_int8(x, tokens, head_dim, q, scale, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(who, e);
+}
+
+qdl_status qdl_kv_dequant_int8(const int8_t *q, const float *scale, uint32_t tokens, uint32_t head_dim, float *out,
+                               void *stream) {
+    const char *who = "dequantize_kv_int8";
+    qdl_status st = check_kv_shape(who, tokens, head_dim);
+    if (st != QDL_OK) return st;
+    if (q == nullptr || scale == nullptr || out == nullptr) return fail(QDL_ERR_INVALID_ARG, "%s: NULL pointer argument", who);
+    if (!aligned(q, 4) || !aligned(scale, 4) || !aligned(out, 16))
+        return fail(QDL_ERR_INVALID_ARG, "%s: q and scale must be 4-byte, out 16-byte aligned", who);
+    cudaError_t e = launch_kv_dequant_int8(q, scale, tokens, head_dim, out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(who, e);
+}
+
+qdl_status qdl_kv_quant_int4(const float *x, uint32_t tokens, uint32_t head_dim, uint32_t group, uint8_t *packed,
+                             float *scale, float *zero, void *stream) {
+    const char *who = "quantize_kv_int4";
+    qdl_status st = check_kv_int4(who, tokens, head_dim, group);
+    if (st != QDL_OK) return st;
+    if (x == nullptr || packed == nullptr || scale == nullptr || zero == nullptr)
+        return fail(QDL_ERR_INVALID_ARG, "%s: NULL pointer argument", who);
+    if (!aligned(x, 16) || !aligned(packed, 4) || !aligned(scale, 4) || !aligned(zero, 4))
+        return fail(QDL_ERR_INVALID_ARG, "%s: x must be 16-byte, packed, scale and zero 4-byte aligned", who);
+    cudaError_t e = launch_kv_quant_int4(x, (size_t)tokens * head_dim, group, packed, scale, zero,
+                                         static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(who, e);
+}
+
+qdl_status qdl_kv_dequant_int4(const uint8_t *packed, const float *scale, const float *zero, uint32_t tokens,
+                               uint32_t head_dim, uint32_t group, float *out, void *stream) {
+    const char *who = "dequantize_kv_int4";
+    qdl_status st = check_kv_int4(who, tokens, head_dim, group);
+    if (st != QDL_OK) return st;
+    if (packed == nullptr || scale == nullptr || zero == nullptr || out == nullptr)
+        return fail(QDL_ERR_INVALID_ARG, "%s: NULL pointer argument", who);
+    if (!aligned(packed, 4) || !aligned(scale, 4) || !aligned(zero, 4) || !aligned(out, 16))
+        return fail(QDL_ERR_INVALID_ARG, "%s: packed, scale and zero must be 4-byte, out 16-byte aligned", who);
+    cudaError_t e = launch_kv_dequant_int4(packed, scale, zero, (size_t)tokens * head_dim, group, out,
+                                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(who, e);
+}
+
 // ---------------------------------------------------------------- no-allocation variant
 //
 // qdl_w8a8_proj_static: the decode projection for callers that cannot

@@ -125,6 +125,15 @@ bool int4_cc_supported(uint32_t nq, uint32_t nkv);                  // widths mu
 cudaError_t launch_int4_qkv_cc(const Int4Args &a, cudaStream_t s);  // 1..4 token rows, CUDA cores
 cudaError_t read_and_clear_int4cc_fault(uint32_t *value);
 
+// KV-cache quantisers (kv_cache_quant.wgsl); arguments checked by the C ABI
+cudaError_t launch_kv_quant_int8(const float *x, uint32_t tokens, uint32_t dim, int8_t *q, float *scale, cudaStream_t s);
+cudaError_t launch_kv_dequant_int8(const int8_t *q, const float *scale, uint32_t tokens, uint32_t dim, float *out,
+                                   cudaStream_t s);
+cudaError_t launch_kv_quant_int4(const float *x, size_t n, uint32_t group, uint8_t *packed, float *scale, float *zero,
+                                 cudaStream_t s);
+cudaError_t launch_kv_dequant_int4(const uint8_t *packed, const float *scale, const float *zero, size_t n,
+                                   uint32_t group, float *out, cudaStream_t s);
+
 int device_sm_count();  // of the current device, cached
 
 // ---------------------------------------------------------------- device helpers

@@ -15,7 +15,8 @@ Recipe (LLM-shaped decode workloads):
   and scales as inputs);
 * AWQ INT4: packed words of uniform random bits (so every nibble is uniform on
   0..15), scales U(0.001, 0.02), zeros uniform on 0..15 (integers by default,
-  continuous U(0, 15) on request).
+  continuous U(0, 15) on request);
+* KV-cache blocks: float32 N(0, 1) rows of head_dim values.
 """
 from __future__ import annotations
 
@@ -133,6 +134,17 @@ class Int4Workload:
     seed: int = 0
 
 
+@dataclasses.dataclass(frozen=True)
+class KvWorkload:
+    """A block of KV-cache rows (token x head) of head_dim values; group 0
+    means per-token int8, otherwise per-group INT4."""
+    name: str
+    head_dim: int
+    group: int
+    rows: tuple
+    seed: int = 0
+
+
 WORKLOADS = {
     "w8a8_perrow_m1_k1024_n1024": W8A8Workload(
         "w8a8_perrow_m1_k1024_n1024", PER_ROW, 1024, (1024,), (1,), 0.02),
@@ -147,6 +159,8 @@ WORKLOADS = {
     "w8a8_block128_gateup_k8192_n14336+14336": W8A8Workload(
         "w8a8_block128_gateup_k8192_n14336+14336", BLOCK128, 8192, (14336, 14336),
         (1, 2, 4, 8, 16, 32, 64, 128, 256), 0.015),
+    "kv_int8_t32768_d128": KvWorkload("kv_int8_t32768_d128", 128, 0, (32768,)),
+    "kv_int4_t32768_d128_g128": KvWorkload("kv_int4_t32768_d128_g128", 128, 128, (32768,)),
 }
 
 HEADLINE = "w8a8_block128_qkv_m8_k4096_n4096+1024+1024"
@@ -172,3 +186,8 @@ def int4_weights(wl: Int4Workload, integer_zeros: bool = True):
 
 def int4_activations(wl: Int4Workload, rows: int) -> np.ndarray:
     return normal_f32((rows, wl.k), wl.seed)
+
+
+def kv_values(wl: KvWorkload, rows: int, copy: int = 0) -> np.ndarray:
+    """K or V rows ~ N(0, 1), float32 [rows, head_dim]"""
+    return normal_f32((rows, wl.head_dim), wl.seed + 100 + copy)

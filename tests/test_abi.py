@@ -252,3 +252,45 @@ def _int4(lib, x=DEV, m=1, k=4096, nq=4096, nkv=1024, group=128, qw=None, sc=Non
 def test_int4_rejects(lib, kw, msg):
     st, err = _int4(lib, **kw)
     assert st == INVALID and msg in err, (st, err)
+
+
+# ---------------------------------------------------------------- KV-cache quantisers
+
+def _kv(lib, fn, **kw):
+    a = dict(x=DEV, tokens=64, dim=128, group=64, q=DEV + 0x1000000, s=DEV + 0x2000000, z=DEV + 0x3000000,
+             out=DEV + 0x4000000)
+    a.update(kw)
+    if fn == "q8":
+        st = lib.qdl_kv_quant_int8(a["x"], a["tokens"], a["dim"], a["q"], a["s"], None)
+    elif fn == "d8":
+        st = lib.qdl_kv_dequant_int8(a["q"], a["s"], a["tokens"], a["dim"], a["out"], None)
+    elif fn == "q4":
+        st = lib.qdl_kv_quant_int4(a["x"], a["tokens"], a["dim"], a["group"], a["q"], a["s"], a["z"], None)
+    else:
+        st = lib.qdl_kv_dequant_int4(a["q"], a["s"], a["z"], a["tokens"], a["dim"], a["group"], a["out"], None)
+    return st, lib.qdl_last_error().decode()
+
+
+@pytest.mark.parametrize("fn,kw,msg", [
+    ("q8", dict(tokens=0), "tokens=0"),
+    ("q8", dict(dim=130), "head_dim=130"),
+    ("q8", dict(x=0), "NULL"),
+    ("q8", dict(x=DEV + 4), "x must be 16-byte"),
+    ("q8", dict(q=DEV + 2), "4-byte aligned"),
+    ("d8", dict(out=DEV + 8), "out 16-byte aligned"),
+    ("d8", dict(s=0), "NULL"),
+    ("q4", dict(group=0), "group=0"),
+    ("q4", dict(group=12), "group=12"),
+    ("q4", dict(tokens=3, dim=4, group=8), "group=8"),
+    ("q4", dict(z=0), "NULL"),
+    ("d4", dict(dim=2), "head_dim=2"),
+    ("d4", dict(q=DEV + 1), "4-byte"),
+])
+def test_kv_rejects(lib, fn, kw, msg):
+    st, err = _kv(lib, fn, **kw)
+    assert st == INVALID and msg in err, (st, err)
+
+
+def test_kv_rejects_oversized(lib):
+    st, err = _kv(lib, "q8", tokens=1 << 20, dim=4096)
+    assert st == UNSUPPORTED and "exceeds 2^31" in err, (st, err)
