@@ -28,7 +28,21 @@ namespace {
 
 constexpr int kKvThreads = 256;
 constexpr int kKvWarps = kKvThreads / 32;
-constexpr int kTokensPerWarp = 4;  // int8 quantiser: tokens whose loads one warp keeps in flight
+#ifndef QDL_KV_TOKENS_PER_WARP
+#define QDL_KV_TOKENS_PER_WARP 2
+#endif
+#ifndef QDL_KV_ROUNDS
+#define QDL_KV_ROUNDS 1
+#endif
+constexpr int kTokensPerWarp = QDL_KV_TOKENS_PER_WARP;  // int8 quantiser: tokens whose loads one warp keeps in flight
+
+// Programmatic launch: release the next kernel at once, then wait for the
+// previous one (the input may come from it, and it may still read the
+// buffers written here).
+__device__ __forceinline__ void kv_dependency_prologue() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 __device__ __forceinline__ float kv_scale_int8(float absmax) {
     const float s = __fdiv_rn(absmax, 127.0f);
@@ -46,6 +60,7 @@ template <int CH>
 __global__ void __launch_bounds__(kKvThreads) kv_quant_int8_kernel(const float *__restrict__ x, uint32_t tokens,
                                                                     uint32_t dim, uint32_t *__restrict__ q,
                                                                     float *__restrict__ scale) {
+    kv_dependency_prologue();
     const uint32_t warp = (blockIdx.x * kKvWarps + (threadIdx.x >> 5)), lane = threadIdx.x & 31;
     const uint32_t t0 = warp * kTokensPerWarp;
     const uint32_t chunks = dim / 4;
@@ -84,6 +99,7 @@ __global__ void __launch_bounds__(kKvThreads) kv_quant_int8_kernel(const float *
 __global__ void __launch_bounds__(kKvThreads) kv_quant_int8_wide_kernel(const float *__restrict__ x, uint32_t tokens,
                                                                          uint32_t dim, uint32_t *__restrict__ q,
                                                                          float *__restrict__ scale) {
+    kv_dependency_prologue();
     const uint32_t t = blockIdx.x * kKvWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (t >= tokens) return;
     const uint32_t chunks = dim / 4;
@@ -107,6 +123,7 @@ __global__ void __launch_bounds__(kKvThreads) kv_quant_int8_wide_kernel(const fl
 __global__ void __launch_bounds__(kKvThreads) kv_dequant_int8_kernel(const uint32_t *__restrict__ q,
                                                                       const float *__restrict__ scale, uint32_t tokens,
                                                                       uint32_t dim, float4 *__restrict__ out) {
+    kv_dependency_prologue();
     const size_t words = (size_t)tokens * dim / 4;
     const uint32_t wpt = dim / 4;  // words per token
     const size_t stride = (size_t)gridDim.x * blockDim.x;
@@ -155,12 +172,13 @@ __device__ __forceinline__ void minmax8(const float4 &a, const float4 &b, float 
 // group = 8 L with L a power of two <= 32: L lanes per group, one 8-value
 // chunk per lane, 32 / L groups per warp and kRounds batches per warp with
 // every load issued first
-constexpr int kRounds = 2;
+constexpr int kRounds = QDL_KV_ROUNDS;
 
 template <int L>
 __global__ void __launch_bounds__(kKvThreads) kv_quant_int4_kernel(const float *__restrict__ x, uint32_t groups,
                                                                     uint32_t *__restrict__ packed,
                                                                     float *__restrict__ scale, float *__restrict__ zero) {
+    kv_dependency_prologue();
     constexpr uint32_t kGpw = 32 / L, kGroup = 8 * L;
     const uint32_t warp = blockIdx.x * kKvWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     const uint32_t chunk = lane % L;
@@ -198,6 +216,7 @@ __global__ void __launch_bounds__(kKvThreads) kv_quant_int4_wide_kernel(const fl
                                                                          uint32_t group, uint32_t *__restrict__ packed,
                                                                          float *__restrict__ scale,
                                                                          float *__restrict__ zero) {
+    kv_dependency_prologue();
     const uint32_t g = blockIdx.x * kKvWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (g >= groups) return;
     const uint32_t chunks = group / 8;
@@ -228,6 +247,7 @@ __global__ void __launch_bounds__(kKvThreads) kv_dequant_int4_kernel(const uint3
                                                                       const float *__restrict__ scale,
                                                                       const float *__restrict__ zero, size_t words,
                                                                       uint32_t group, float4 *__restrict__ out) {
+    kv_dependency_prologue();
     const uint32_t wpg = group / 8;  // words per group
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < words; i += stride) {
@@ -240,6 +260,20 @@ __global__ void __launch_bounds__(kKvThreads) kv_dequant_int4_kernel(const uint3
         out[2 * i] = make_float4(o[0], o[1], o[2], o[3]);
         out[2 * i + 1] = make_float4(o[4], o[5], o[6], o[7]);
     }
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kv(void (*kernel)(KArgs...), uint32_t grid, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kKvThreads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = QDL_TUNE_PDL ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 uint32_t grid_for(size_t work_items, uint32_t per_block) {
@@ -258,57 +292,45 @@ uint32_t stream_grid(size_t items) {
 
 cudaError_t launch_kv_quant_int8(const float *x, uint32_t tokens, uint32_t dim, int8_t *q, float *scale, cudaStream_t s) {
     uint32_t *qw = reinterpret_cast<uint32_t *>(q);
-    const uint32_t per_block = kKvWarps * kTokensPerWarp;
-    if (dim <= 128)
-        kv_quant_int8_kernel<1><<<grid_for(tokens, per_block), kKvThreads, 0, s>>>(x, tokens, dim, qw, scale);
-    else if (dim <= 256)
-        kv_quant_int8_kernel<2><<<grid_for(tokens, per_block), kKvThreads, 0, s>>>(x, tokens, dim, qw, scale);
-    else if (dim <= 512)
-        kv_quant_int8_kernel<4><<<grid_for(tokens, per_block), kKvThreads, 0, s>>>(x, tokens, dim, qw, scale);
-    else
-        kv_quant_int8_wide_kernel<<<grid_for(tokens, kKvWarps), kKvThreads, 0, s>>>(x, tokens, dim, qw, scale);
-    return cudaGetLastError();
+    const uint32_t grid = grid_for(tokens, kKvWarps * kTokensPerWarp);
+    if (dim <= 128) return launch_kv(kv_quant_int8_kernel<1>, grid, s, x, tokens, dim, qw, scale);
+    if (dim <= 256) return launch_kv(kv_quant_int8_kernel<2>, grid, s, x, tokens, dim, qw, scale);
+    if (dim <= 512) return launch_kv(kv_quant_int8_kernel<4>, grid, s, x, tokens, dim, qw, scale);
+    return launch_kv(kv_quant_int8_wide_kernel, grid_for(tokens, kKvWarps), s, x, tokens, dim, qw, scale);
 }
 
 cudaError_t launch_kv_dequant_int8(const int8_t *q, const float *scale, uint32_t tokens, uint32_t dim, float *out,
                                    cudaStream_t s) {
     const size_t words = (size_t)tokens * dim / 4;
-    kv_dequant_int8_kernel<<<stream_grid(words), kKvThreads, 0, s>>>(reinterpret_cast<const uint32_t *>(q), scale,
-                                                                       tokens, dim, reinterpret_cast<float4 *>(out));
-    return cudaGetLastError();
+    return launch_kv(kv_dequant_int8_kernel, stream_grid(words), s, reinterpret_cast<const uint32_t *>(q), scale,
+                     tokens, dim, reinterpret_cast<float4 *>(out));
 }
 
 cudaError_t launch_kv_quant_int4(const float *x, size_t n, uint32_t group, uint8_t *packed, float *scale, float *zero,
                                  cudaStream_t s) {
-    const size_t groups = n / group;
+    const uint32_t groups = (uint32_t)(n / group);
     uint32_t *pw = reinterpret_cast<uint32_t *>(packed);
-    const uint32_t lanes = group / 8;
     auto launch = [&](auto tag) {
         constexpr int L = decltype(tag)::value;
-        const uint32_t per_block = kKvWarps * kRounds * (32 / L);
-        kv_quant_int4_kernel<L><<<grid_for(groups, per_block), kKvThreads, 0, s>>>(x, (uint32_t)groups, pw, scale, zero);
+        return launch_kv(kv_quant_int4_kernel<L>, grid_for(groups, kKvWarps * kRounds * (32 / L)), s, x, groups, pw,
+                         scale, zero);
     };
-    switch (lanes) {
-        case 1: launch(std::integral_constant<int, 1>()); break;
-        case 2: launch(std::integral_constant<int, 2>()); break;
-        case 4: launch(std::integral_constant<int, 4>()); break;
-        case 8: launch(std::integral_constant<int, 8>()); break;
-        case 16: launch(std::integral_constant<int, 16>()); break;
-        case 32: launch(std::integral_constant<int, 32>()); break;
-        default:
-            kv_quant_int4_wide_kernel<<<grid_for(groups, kKvWarps), kKvThreads, 0, s>>>(x, (uint32_t)groups, group, pw,
-                                                                                      scale, zero);
+    switch (group / 8) {  // lanes per group
+        case 1: return launch(std::integral_constant<int, 1>());
+        case 2: return launch(std::integral_constant<int, 2>());
+        case 4: return launch(std::integral_constant<int, 4>());
+        case 8: return launch(std::integral_constant<int, 8>());
+        case 16: return launch(std::integral_constant<int, 16>());
+        case 32: return launch(std::integral_constant<int, 32>());
+        default: return launch_kv(kv_quant_int4_wide_kernel, grid_for(groups, kKvWarps), s, x, groups, group, pw, scale, zero);
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_kv_dequant_int4(const uint8_t *packed, const float *scale, const float *zero, size_t n,
                                    uint32_t group, float *out, cudaStream_t s) {
     const size_t words = n / 8;
-    kv_dequant_int4_kernel<<<stream_grid(words), kKvThreads, 0, s>>>(reinterpret_cast<const uint32_t *>(packed), scale,
-                                                                       zero, words, group,
-                                                                       reinterpret_cast<float4 *>(out));
-    return cudaGetLastError();
+    return launch_kv(kv_dequant_int4_kernel, stream_grid(words), s, reinterpret_cast<const uint32_t *>(packed), scale,
+                     zero, words, group, reinterpret_cast<float4 *>(out));
 }
 
 }  // namespace qdl
