@@ -82,6 +82,8 @@ def _load():
             lib.orc_kv_dequant_int8.argtypes = [P, P, I, I, P]
             lib.orc_kv_quant_int4.argtypes = [P, S, I, P, P, P]
             lib.orc_kv_dequant_int4.argtypes = [P, P, P, S, I, P]
+            lib.orc_fp8_weight_quant.argtypes = [I, P, S, I, I, P, P]
+            lib.orc_awq_pack.argtypes = [P, I, I, P]
             lib.orc_num_threads.restype = I
             _lib = lib
     return _lib
@@ -254,3 +256,26 @@ def kv_dequant_int4(packed, scale, zero, n: int, group: int):
     out = np.empty((n,), np.float32)
     _load().orc_kv_dequant_int4(_ptr(packed), _ptr(scale), _ptr(zero), n, group, _ptr(out))
     return out
+
+
+def fp8_weight_quant(fmt: int, w):
+    """w f32 [n, k] (k % 128 == 0) -> (codes uint8 [n, k], scales f32 [n] for
+    PER_ROW or [ceil(n/128), k/128] for BLOCK128)."""
+    w = _c(w, np.float32)
+    n, k = w.shape
+    assert k % 128 == 0
+    codes = np.empty((n, k), np.uint8)
+    scales = np.empty((n,) if fmt == 0 else ((n + 127) // 128, k // 128), np.float32)
+    _load().orc_fp8_weight_quant(fmt, _ptr(w), k, n, k, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def awq_pack(nib):
+    """nib uint8 [k, n] (codes 0..15, n % 8 == 0) -> uint32 [k, n/8] in the
+    AWQ shift order."""
+    nib = _c(nib, np.uint8)
+    k, n = nib.shape
+    assert n % 8 == 0
+    qw = np.empty((k, n // 8), np.uint32)
+    _load().orc_awq_pack(_ptr(nib), k, n, _ptr(qw))
+    return qw

@@ -354,6 +354,65 @@ void orc_int4_qkv(const float *x, int m, int k, int nq, int nkv, int group,
 }
 
 /* ---------------------------------------------------------------------
+ * FP8 weight quantisation: the weight side of w8a8_decode.rs's scale
+ * layouts (enum W8a8Scale: one f32 scale per output row, or one per 128x128
+ * block of the [n, K] weight stored [ceil(n/128), K/128]), with the scale
+ * the workloads state for weights, absmax / 448:
+ *   s    = absmax over the row or block / 448      (binary32 division)
+ *   code = e4m3(w / s)                             (binary32 division, RNE satfinite)
+ * A row or block whose absmax is 0 stores s = 0 and the codes of its +-0
+ * values (the rule the activation quantiser follows).  A ragged last block
+ * row covers the remaining n % 128 rows.
+ * ------------------------------------------------------------------- */
+
+static void quant_region(const float *w, size_t ldw, int r0, int r1, int c0, int c1, uint8_t *codes, int k,
+                         float *s_out) {
+    float amax = 0.0f;
+    for (int r = r0; r < r1; ++r)
+        for (int c = c0; c < c1; ++c) {
+            float v = fabsf(w[(size_t)r * ldw + c]);
+            if (v > amax) amax = v;
+        }
+    float scale = amax / 448.0f;
+    *s_out = scale;
+    for (int r = r0; r < r1; ++r)
+        for (int c = c0; c < c1; ++c) {
+            float v = w[(size_t)r * ldw + c];
+            codes[(size_t)r * k + c] = (scale == 0.0f) ? orc_e4m3_encode(v) : orc_e4m3_encode(v / scale);
+        }
+}
+
+void orc_fp8_weight_quant(int fmt, const float *w, size_t ldw, int n, int k, uint8_t *codes, float *scales) {
+    if (fmt == ORC_PER_ROW) {
+#pragma omp parallel for schedule(static)
+        for (int r = 0; r < n; ++r) quant_region(w, ldw, r, r + 1, 0, k, codes, k, scales + r);
+    } else {
+        int nb = (n + 127) / 128, kb = k / 128;
+#pragma omp parallel for schedule(static)
+        for (int b = 0; b < nb * kb; ++b) {
+            int br = b / kb, bc = b % kb;
+            int r1 = (br + 1) * 128 < n ? (br + 1) * 128 : n;
+            quant_region(w, ldw, br * 128, r1, bc * 128, bc * 128 + 128, codes, k, scales + b);
+        }
+    }
+}
+
+/* AWQ packing, the inverse of the unpacking in fused_int4_qkv.rs
+ * (QKV_AWQ_SHIFTS, unpack_awq_qkv): word j of row kk holds the code of
+ * column 8j + i at bits SHIFT[i] .. SHIFT[i] + 3.  Codes are 0..15, one per
+ * byte of nib [k, n]; qw is [k, n/8]. */
+void orc_awq_pack(const uint8_t *nib, int k, int n, uint32_t *qw) {
+    int words = n / 8;
+    for (int kk = 0; kk < k; ++kk)
+        for (int j = 0; j < words; ++j) {
+            uint32_t word = 0;
+            for (int i = 0; i < 8; ++i)
+                word |= (uint32_t)(nib[(size_t)kk * n + 8 * j + i] & 0xFu) << orc_awq_shift[i];
+            qw[(size_t)kk * words + j] = word;
+        }
+}
+
+/* ---------------------------------------------------------------------
  * KV-cache quantisation (kv_cache_quant.wgsl).
  *
  * Per-token symmetric int8 (the page's quantize_kv_fp8_per_token_f32 and

@@ -21,6 +21,10 @@
  *   - The AWQ INT4 fused-QKV GEMV of fused_int4_qkv.rs (QKV_AWQ_SHIFTS,
  *     unpack_awq_qkv, fused_int4_qkv_q/_k/_v): f32 dequantisation exactly as
  *     the shader writes it, dot product accumulated in double.
+ *   - FP8 weight quantisation per output row or 128x128 block with scale
+ *     absmax / 448 (the weight recipe of the workloads, in the scale layouts
+ *     of w8a8_decode.rs), and AWQ packing of 4-bit codes in the shift order
+ *     of fused_int4_qkv.rs (the inverse of its unpacking).
  *   - The KV-cache quantisers of kv_cache_quant.wgsl: per-token symmetric
  *     int8 and per-group asymmetric INT4 with two codes per byte, and their
  *     dequantisers, step for step in binary32.
@@ -81,6 +85,15 @@ void orc_int4_qkv(const float *x, int m, int k, int nq, int nkv, int group,
                   const uint32_t *const *qw, const float *const *sc,
                   const float *const *zr, double *const *out,
                   double *const *bound);
+
+/* FP8 weight quantisation per output row or per 128x128 block (scale =
+ * absmax / 448): w f32 [n, ldw] (first k columns), k % 128 == 0;
+ * codes [n, k]; scales [n] (PER_ROW) or [ceil(n/128), k/128] (BLOCK128). */
+void orc_fp8_weight_quant(int fmt, const float *w, size_t ldw, int n, int k, uint8_t *codes, float *scales);
+
+/* AWQ packing in the shift order of fused_int4_qkv.rs: nib u8 [k, n] (codes
+ * 0..15, n % 8 == 0) -> qw u32 [k, n/8]. */
+void orc_awq_pack(const uint8_t *nib, int k, int n, uint32_t *qw);
 
 /* KV-cache quantisation (kv_cache_quant.wgsl): per-token symmetric int8,
  * x [tokens, dim] -> q int8 [tokens, dim], s [tokens]; per-group asymmetric
