@@ -92,17 +92,20 @@ class W8A8Case:
         x_bytes = rows * (2 * K if wl.silu else K) * 2
         # algorithmic bytes of one fused call: weights + weight scales + bf16 input + f32 output
         self.step_bytes = n * K + w_scales + x_bytes + rows * n * 4
-        # of one GEMV launch: weights + scales + e4m3 activations + act scales + output
-        self.gemv_bytes = n * K + w_scales + rows * K + self.s.numel() * 4 + rows * n * 4
-        self.gemv_launches = 1  # one tcgen05 launch covers up to 256 rows
-        # the library's plan: 1 when the GEMV quantises its own activations,
-        # else the quantiser + the GEMV (always for the SiLU variant)
-        plan = qdl.w8a8_plan(self.weights[0], rows)
-        self.launches_per_step = 2 if wl.silu else plan["proj_launches"]
+        # one tcgen05 GEMV launch covers up to 256 rows; a projection of more
+        # rows runs in passes of 256, each streaming the weights again
+        self.passes = [(d, min(256, rows - d)) for d in range(0, rows, 256)]
+        # of the GEMV launches: weights + scales + e4m3 activations + act scales + output
+        self.gemv_bytes = sum(n * K + w_scales + p * K + p * spr * 4 + p * n * 4 for _, p in self.passes)
+        self.gemv_launches = len(self.passes)
+        # the library's plan per pass: 1 launch when the GEMV quantises its own
+        # activations, else the quantiser + the GEMV (always for the SiLU variant)
+        plans = [qdl.w8a8_plan(self.weights[0], p) for _, p in self.passes]
+        self.launches_per_step = sum(2 if wl.silu else pl["proj_launches"] for pl in plans)
         # the GEMV as the projection runs it: with split K it adds into the
         # zeroed f32 output
-        self.dom_dtype = qdl.OUT_F32_ADD if plan["proj_accumulates"] else qdl.OUT_F32
-        self.kernel = "w8a8_streamk_kernel" if plan["proj_streamk"] else "w8a8_gemm_tc_kernel"
+        self.dom_dtypes = [qdl.OUT_F32_ADD if pl["proj_accumulates"] else qdl.OUT_F32 for pl in plans]
+        self.kernel = "w8a8_streamk_kernel" if plans[0]["proj_streamk"] else "w8a8_gemm_tc_kernel"
         self.kernel_src = ["w8a8_gemm_tc.cu"]
 
     def step(self, i):
@@ -115,8 +118,9 @@ class W8A8Case:
             qdl.w8a8_proj(w, self.x, self.rows, self.out, self.q, self.s)
 
     def dominant(self, i):
-        self.qdl.w8a8_gemv(self.weights[i % self.copies], self.q, self.s, self.rows, self.out,
-                           out_dtype=self.dom_dtype)
+        w = self.weights[i % self.copies]
+        for (d, p), dt in zip(self.passes, self.dom_dtypes):
+            self.qdl.w8a8_gemv(w, self.q[:p], self.s[:p], p, self.out[d:d + p], out_dtype=dt)
 
     def e2e_step(self, i):
         self.x.copy_(self.x_host, non_blocking=True)
@@ -153,10 +157,16 @@ class Int4Case:
         n_tot = wl.nq + 2 * wl.nkv
         self.step_bytes = self.weight_bytes + x.nbytes + rows * n_tot * 4
         self.gemv_bytes = self.step_bytes
-        # the library's dispatch for widths multiple of 32 and group 128:
-        # tcgen05 passes of 32 rows, each an output-zeroing launch and the GEMV
-        self.gemv_launches = math.ceil(rows / 32)
-        self.kernel, self.kernel_src = "int4_qkv_tc_kernel", ["int4_qkv_tc.cu"]
+        # the library's dispatch for widths multiple of 32: up to 4 rows the
+        # CUDA-core stream-K kernel (f32 products), else (group 128) tcgen05
+        # passes of 32 rows (f16 operands); each is an output-zeroing launch
+        # and the GEMV
+        if rows <= 4:
+            self.gemv_launches = 1
+            self.kernel, self.kernel_src, self.dtype = "int4_qkv_sk_kernel", ["int4_qkv_cc.cu"], "f32"
+        else:
+            self.gemv_launches = math.ceil(rows / 32)
+            self.kernel, self.kernel_src, self.dtype = "int4_qkv_tc_kernel", ["int4_qkv_tc.cu"], "f16"
         self.launches_per_step = 2 * self.gemv_launches
 
     def step(self, i):
@@ -264,6 +274,76 @@ class KvCase:
                       f"({self.copies * (8 * self.n) / 1e6:.0f} MB of values)"}
 
 
+class PrepCase:
+    """Weight preparation workload: one step quantises a bf16 weight to FP8
+    (fp8) or packs 4-bit codes into AWQ words (awq); buffers rotate over
+    enough copies that every step streams from HBM."""
+
+    def __init__(self, wl, rows, torch, qdl, syn, l2_bytes):
+        self.wl, self.rows, self.qdl = wl, rows, qdl
+        self.fp8 = wl.prep == "fp8"
+        if self.fp8:
+            src = syn.prep_weight_bf16(wl)
+            in_bytes = src.nbytes
+            nsc = wl.n if wl.scale_format == 0 else ((wl.n + 127) // 128) * (wl.k // 128)
+            out_bytes = wl.n * wl.k + 4 * nsc
+            dev = torch.from_numpy(src.view(np.int16)).cuda().view(torch.bfloat16)
+            self.host_in = torch.from_numpy(src.view(np.int16)).view(torch.bfloat16).pin_memory()
+        else:
+            src = syn.prep_codes(wl)
+            in_bytes = src.nbytes
+            out_bytes = wl.k * wl.n // 2
+            dev = torch.from_numpy(src).cuda()
+            self.host_in = torch.from_numpy(src).pin_memory()
+        self.copies = max(1, math.ceil(4 * l2_bytes / (in_bytes + out_bytes))) if in_bytes + out_bytes < 4 * l2_bytes else 1
+        self.src = [dev] + [dev.clone() for _ in range(self.copies - 1)]
+        if self.fp8:
+            shape = (wl.n,) if wl.scale_format == 0 else ((wl.n + 127) // 128, wl.k // 128)
+            self.codes = [torch.empty((wl.n, wl.k), dtype=torch.uint8, device="cuda") for _ in range(self.copies)]
+            self.scales = [torch.empty(shape, dtype=torch.float32, device="cuda") for _ in range(self.copies)]
+            self.host_out = torch.empty((wl.n, wl.k), dtype=torch.uint8).pin_memory()
+        else:
+            self.codes = [torch.empty((wl.k, wl.n // 8), dtype=torch.int32, device="cuda") for _ in range(self.copies)]
+            self.host_out = torch.empty((wl.k, wl.n // 8), dtype=torch.int32).pin_memory()
+        self.weight_bytes = in_bytes
+        self.gemv_bytes = self.step_bytes = in_bytes + out_bytes
+        self.gemv_launches, self.launches_per_step = 1, 1
+        self.kernel = "fp8_weight_quant_kernel" if self.fp8 else "awq_pack_kernel"
+        self.kernel_src = ["weight_quant.cu"]
+        self.dtype = "e4m3" if self.fp8 else "u4"
+
+    def _call(self, c):
+        wl = self.wl
+        if self.fp8:
+            self.qdl.fp8_weight_quant(wl.scale_format, self.src[c], self.qdl.IN_BF16, wl.k, wl.n, wl.k,
+                                      self.codes[c], self.scales[c])
+        else:
+            self.qdl.awq_pack(self.src[c], wl.k, wl.n, self.codes[c])
+
+    def step(self, i):
+        self._call(i % self.copies)
+
+    dominant = step
+
+    def e2e_step(self, i):
+        c = i % self.copies
+        self.src[c].copy_(self.host_in, non_blocking=True)
+        self._call(c)
+        self.host_out.copy_(self.codes[c], non_blocking=True)
+
+    def e2e_bytes(self):
+        return self.host_in.numel() * self.host_in.element_size(), self.host_out.numel() * self.host_out.element_size()
+
+    def describe(self):
+        wl = self.wl
+        d = {"workload": wl.name, "n": wl.n, "k": wl.k, "copies": self.copies,
+             "l2": f"inputs larger than L2: {self.copies} cop{'y' if self.copies == 1 else 'ies'} of "
+                   f"{self.step_bytes / 1e6:.0f} MB moved per step"}
+        if self.fp8:
+            d.update(input="bf16", scale_format="per_row" if wl.scale_format == 0 else "block128")
+        return d
+
+
 # ---------------------------------------------------------------- timing helpers
 
 def _graph(torch, fn, start, count):
@@ -333,6 +413,22 @@ def _oracle_step_fn(wl, rows, syn, fraction):
     """returns (fn, bytes_equiv, sample description) for one oracle step on a
     fraction of the workload's output columns"""
     import oracle
+    if hasattr(wl, "prep"):
+        if wl.prep == "fp8":
+            take = max(128, int(round(wl.n * fraction / 128)) * 128)
+            w = syn.prep_weight_bf16(wl, take)
+            w32 = (w.astype(np.uint32) << 16).view(np.float32)
+            nsc = take if wl.scale_format == 0 else (take // 128) * (wl.k // 128)
+
+            def fn():
+                oracle.fp8_weight_quant(wl.scale_format, w32)
+            return fn, take * wl.k * 3 + 4 * nsc, f"quantise {take} of {wl.n} rows"
+        take = max(1, int(round(wl.k * fraction)))
+        nib = syn.prep_codes(wl, take)
+
+        def fn():
+            oracle.awq_pack(nib)
+        return fn, take * wl.n * 3 // 2, f"pack {take} of {wl.k} rows"
     if hasattr(wl, "head_dim"):
         take = max(64, int(round(rows * fraction)))
         x = syn.kv_values(wl, take)
@@ -454,7 +550,8 @@ def run_gpu(args, rank, world, local_rank):
 
     wl = syn.WORKLOADS[args.workload]
     rows = args.rows or wl.rows[0]
-    Case = W8A8Case if hasattr(wl, "fmt") else KvCase if hasattr(wl, "head_dim") else Int4Case
+    Case = (PrepCase if hasattr(wl, "prep") else W8A8Case if hasattr(wl, "fmt") else
+            KvCase if hasattr(wl, "head_dim") else Int4Case)
     case = Case(wl, rows, torch, qdl, syn, l2)
 
     # graphs covering exactly K steps: up to four distinct graphs of c calls

@@ -67,6 +67,7 @@ typedef enum { QDL_OUT_F32 = 0, QDL_OUT_BF16 = 1, QDL_OUT_F32_ADD = 2 } qdl_dtyp
 #define QDL_MAX_ROWS 256  /* w8a8_decode.rs W8A8_MAX_ROWS */
 #define QDL_K_UNIT 128    /* w8a8_decode.rs W8A8_K_UNIT   */
 #define QDL_MAX_K 65536   /* library limit on K for the activation quantiser */
+#define QDL_MAX_PROJ_ROWS 65536 /* library limit on rows of one qdl_w8a8_proj call */
 
 /* One FP8 weight segment (the fields w8a8_decode.rs reads from Fp8Weight).
  *   weight : device, e4m3 codes [n, k], row-major (K contiguous), 16-byte
@@ -157,6 +158,11 @@ QDL_API qdl_status qdl_w8a8_gemv(const qdl_w8a8_weight *w, const uint8_t *q, con
 /* Decode projection (w8a8_decode.rs fn w8a8_proj): qdl_act_quant with the
  * weight's format and K, then qdl_w8a8_gemv, on one stream.  q and q_scale
  * are the caller's activation scratch (sizes from qdl_scratch_bytes).
+ * rows may exceed 256 (a prefill-shaped call; the page stops at
+ * W8A8_MAX_ROWS = 256), up to QDL_MAX_PROJ_ROWS: the call then runs in
+ * passes of 256 rows, in order on the stream, each quantising into the same
+ * 256-row scratch and streaming the weights once more; pass p covers rows
+ * 256p.. of x and out. The scratch needs to hold min(rows, 256) rows.
  * With f32 output, when the GEMV splits K over several CTAs, the quantiser
  * first sets out[0..rows)[0..N) to zero and the GEMV adds into it
  * (QDL_OUT_F32_ADD): the order of the split-K additions varies, so results
@@ -169,7 +175,8 @@ QDL_API qdl_status qdl_w8a8_proj(const qdl_w8a8_weight *w, const void *x, uint32
 
 /* MLP down projection: qdl_act_quant_silu with the weight's format and K,
  * then qdl_w8a8_gemv (the composition w8a8_decode.rs uses for gate/up
- * inputs).  f32 output is accumulated as in qdl_w8a8_proj. */
+ * inputs).  f32 output is accumulated, and rows beyond 256 run in passes,
+ * as in qdl_w8a8_proj. */
 QDL_API qdl_status qdl_w8a8_proj_silu(const qdl_w8a8_weight *w, const void *gate, const void *up,
                               uint32_t ld_gate, uint32_t ld_up, uint32_t rows, void *out,
                               int32_t out_dtype, uint32_t ldc, uint8_t *q, float *q_scale,
@@ -187,14 +194,16 @@ QDL_API qdl_status qdl_w8a8_proj_silu(const qdl_w8a8_weight *w, const void *gate
  *            nq, nkv multiples of 16 enables 8-byte weight loads).
  *   sc[p], zr[p] : device f32 [k/group, n], 16-byte aligned.
  *   out[p] : device f32 [m, n], 4-byte aligned.
- * With group 128, nq and nkv multiples of 32 and every qw[p] 16-byte aligned,
- * the tcgen05 kernel streams the weights once per 32 rows (two launches per
- * pass: out is zeroed, then the GEMV adds per-tile partial sums into it with
- * f32 atomics, so the order of those additions varies from run to run); it
+ * With nq and nkv multiples of 32 and every qw[p] 16-byte aligned, up to 4
+ * rows (up to 8 with group != 128) take one CUDA-core pass in f32 (x
+ * unrounded, exact nibbles), and more rows with group 128 take the tcgen05
+ * kernel once per 32 rows, which
  * multiplies x rounded to f16 with exact nibbles (error within 2^-11 of
- * sum |x w|) and applies zeros and scales per group in f32.  Other widths
- * that are multiples of 32 take, for up to 4 rows, one CUDA-core pass in f32;
- * every other shape an mma.sync kernel (x rounded to f16) once per 16 rows.
+ * sum |x w|) and applies zeros and scales per group in f32.  Both make two
+ * launches: out is zeroed, then the GEMV adds per-tile partial sums into it
+ * with f32 atomics, so the order of those additions, and the last bits of
+ * the result, vary from run to run.  Every other shape takes an mma.sync
+ * kernel (x rounded to f16) once per 16 rows.
  * Checks: m >= 1; k >= 1; group > 0,
  * group % 16 == 0, k % group == 0; nq, nkv > 0 and multiples of 8; no NULL
  * pointer; alignments above. */
@@ -241,6 +250,45 @@ QDL_API qdl_status qdl_kv_quant_int4(const float *x, uint32_t tokens, uint32_t h
 /* out[e] = code(e) * scale[g] - zero[g] * scale[g], g = e / group. */
 QDL_API qdl_status qdl_kv_dequant_int4(const uint8_t *packed, const float *scale, const float *zero, uint32_t tokens,
                                        uint32_t head_dim, uint32_t group, float *out, void *stream);
+
+/* ------------------------------------------------------------------
+ * Weight preparation.  The decode path takes FP8 and AWQ weights as inputs;
+ * these entry points make them on the GPU.  Arguments are device pointers;
+ * calls are asynchronous on `stream`; on an invalid argument nothing is
+ * launched and qdl_last_error() explains.
+ * ------------------------------------------------------------------ */
+
+/* Element type of a weight to quantise. */
+typedef enum { QDL_IN_F32 = 0, QDL_IN_BF16 = 1 } qdl_in_dtype;
+
+/* FP8 E4M3 weight in the scale layouts of w8a8_decode.rs (enum W8a8Scale),
+ * with the scale the workloads state for weights:
+ *   PER_ROW : s[r] = absmax_k |w[r,k]| / 448, one per output row;
+ *   BLOCK128: s[i, j] = absmax over rows 128i.. and columns 128j.. / 448,
+ *             stored [ceil(n/128), k/128]; the last block row covers the
+ *             remaining n % 128 rows;
+ *   code    = e4m3(w / s), both divisions binary32, round to nearest even,
+ *             saturating to +-448; a row or block whose absmax is 0 gets
+ *             s = 0 and the codes of its signed zeros.
+ *   w      : device [n, ldw] of w_dtype (qdl_in_dtype), columns 0..k-1 read;
+ *            16-byte aligned, ldw >= k and a multiple of 4 (f32) or 8 (bf16).
+ *   codes  : device [n, k] (row stride k), 8-byte aligned.
+ *   scales : device f32 [n] or [ceil(n/128), k/128], 4-byte aligned.
+ * The result is exactly what qdl_w8a8_weight_init's segments expect.
+ * Checks: format and w_dtype valid; n >= 1; k a positive multiple of 128;
+ * ldw and alignments above. */
+QDL_API qdl_status qdl_fp8_weight_quant(int32_t format, const void *w, int32_t w_dtype, uint32_t ldw, uint32_t n,
+                                        uint32_t k, uint8_t *codes, float *scales, void *stream);
+
+/* AWQ packing in the shift order of fused_int4_qkv.rs (QKV_AWQ_SHIFTS, the
+ * inverse of unpack_awq_qkv): word j of row kk holds the code of column
+ * 8j + i at bits SHIFT[i] .. SHIFT[i] + 3, SHIFT = {0, 16, 4, 20, 8, 24, 12, 28}.
+ *   nib : device u8 [k, n], one 4-bit code per byte (only the low 4 bits
+ *         are used), 8-byte aligned.
+ *   qw  : device u32 [k, n/8], the layout qdl_int4_qkv_gemv reads; 4-byte
+ *         aligned.
+ * Checks: k >= 1; n a positive multiple of 8; alignments above. */
+QDL_API qdl_status qdl_awq_pack(const uint8_t *nib, uint32_t k, uint32_t n, uint32_t *qw, void *stream);
 
 /* Size of the library's own device array used by qdl_w8a8_proj_static. */
 #define QDL_STATIC_SCRATCH_BYTES (4 << 20)

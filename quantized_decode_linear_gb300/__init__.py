@@ -32,7 +32,7 @@ EXPORTS = ("qdl_w8a8_weight_init", "qdl_scratch_bytes", "qdl_act_quant", "qdl_ac
            "qdl_w8a8_gemv", "qdl_w8a8_proj", "qdl_w8a8_proj_silu", "qdl_int4_qkv_gemv",
            "qdl_w8a8_proj_static", "qdl_w8a8_plan", "qdl_check_device_fault", "qdl_selftest_bounded_wait",
            "qdl_kv_quant_int8", "qdl_kv_dequant_int8", "qdl_kv_quant_int4", "qdl_kv_dequant_int4",
-           "qdl_last_error", "qdl_status_string")
+           "qdl_fp8_weight_quant", "qdl_awq_pack", "qdl_last_error", "qdl_status_string")
 
 
 class QdlError(RuntimeError):
@@ -89,6 +89,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "qdl_w8a8_proj_silu": [P, P, P, U32, U32, U32, P, I32, U32, P, P, SZ, SZ, P],
             "qdl_int4_qkv_gemv": [P, U32, U32, U32, U32, U32, P, P, P, P, P],
             "qdl_w8a8_proj_static": [P, P, U32, U32, P, I32, U32, P],
+            "qdl_fp8_weight_quant": [I32, P, I32, U32, U32, U32, P, P, P],
+            "qdl_awq_pack": [P, U32, U32, P, P],
             "qdl_kv_quant_int8": [P, U32, U32, P, P, P],
             "qdl_kv_dequant_int8": [P, P, U32, U32, P, P],
             "qdl_kv_quant_int4": [P, U32, U32, U32, P, P, P, P],
@@ -254,6 +256,21 @@ def int4_qkv_gemv(x, m: int, k: int, nq: int, nkv: int, group: int, qw, sc, zr, 
     arr = lambda xs: (ctypes.c_void_p * 3)(*[_ptr(t) for t in xs])
     _check(load().qdl_int4_qkv_gemv(_ptr(x), m, k, nq, nkv, group, arr(qw), arr(sc), arr(zr), arr(out),
                                     _stream(stream)))
+
+
+IN_F32, IN_BF16 = 0, 1
+
+
+def fp8_weight_quant(fmt: int, w, w_dtype: int, ldw: int, n: int, k: int, codes, scales, stream=None):
+    """FP8 weight [n, k] with per-row ([n]) or 128x128-block ([ceil(n/128), k/128])
+    f32 scales, absmax / 448, from f32 or bf16 w [n, ldw]."""
+    _check(load().qdl_fp8_weight_quant(fmt, _ptr(w), w_dtype, ldw, n, k, _ptr(codes), _ptr(scales),
+                                       _stream(stream)))
+
+
+def awq_pack(nib, k: int, n: int, qw, stream=None):
+    """uint8 codes [k, n] -> uint32 [k, n/8] in the AWQ shift order."""
+    _check(load().qdl_awq_pack(_ptr(nib), k, n, _ptr(qw), _stream(stream)))
 
 
 def kv_quant_int8(x, tokens: int, head_dim: int, q, scale, stream=None):

@@ -573,14 +573,7 @@ template <int NTOK>
 cudaError_t launch_i4(const Int4Args &a, const CUtensorMap (&maps)[9], cudaStream_t s) {
     // zero the outputs (the GEMV's CTAs add into them)
     cudaLaunchAttribute attr[1] = {pdl_attr()};
-    cudaLaunchConfig_t zc = {};
-    const size_t elems = (size_t)a.m * (a.nq + 2 * (size_t)a.nkv);
-    zc.gridDim = dim3((unsigned)((elems + 255) / 256 < 64 ? (elems + 255) / 256 : 64), 1, 1);
-    zc.blockDim = dim3(256, 1, 1);
-    zc.stream = s;
-    zc.attrs = attr;
-    zc.numAttrs = QDL_TUNE_PDL ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&zc, int4_zero_kernel, a);
+    cudaError_t e = launch_int4_zero(a, s);
     if (e != cudaSuccess) return e;
     // one contiguous range of (tile, unit) pairs per CTA: every resident CTA
     // slot, and more CTAs only when a range would exceed kMaxUnits units
@@ -602,6 +595,24 @@ cudaError_t launch_i4(const Int4Args &a, const CUtensorMap (&maps)[9], cudaStrea
 }
 
 }  // namespace
+
+cudaError_t launch_int4_zero(const Int4Args &a, cudaStream_t s) {
+    cudaLaunchAttribute attr[1] = {pdl_attr()};
+    cudaLaunchConfig_t zc = {};
+    const size_t elems = (size_t)a.m * (a.nq + 2 * (size_t)a.nkv);
+    zc.gridDim = dim3((unsigned)((elems + 255) / 256 < 64 ? (elems + 255) / 256 : 64), 1, 1);
+    zc.blockDim = dim3(256, 1, 1);
+    zc.stream = s;
+    zc.attrs = attr;
+    zc.numAttrs = QDL_TUNE_PDL ? 1 : 0;
+    return cudaLaunchKernelEx(&zc, int4_zero_kernel, a);
+}
+
+cudaError_t make_tmap_plain(CUtensorMap *map, bool f32, const void *base, uint64_t inner, uint64_t outer,
+                            uint32_t box_inner, uint32_t box_outer) {
+    return make_tmap_4b(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT32, base, inner, outer,
+                        box_inner, box_outer, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
 
 cudaError_t make_tmap_words(CUtensorMap *map, const void *base, uint64_t words, uint64_t rows, uint32_t box_rows) {
     return make_tmap_4b(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, base, words, rows, 32, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);

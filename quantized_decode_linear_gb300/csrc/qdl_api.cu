@@ -291,12 +291,15 @@ qdl_status qdl_act_quant_silu(int32_t format, const void *gate, const void *up, 
 }
 
 static qdl_status check_gemv(const char *who, const qdl_w8a8_weight *w, const uint8_t *q, const float *q_scale, size_t q_bytes,
-                             size_t scale_bytes, uint32_t rows, const void *out, int32_t out_dtype, uint32_t ldc, bool allow_add = false) {
+                             size_t scale_bytes, uint32_t rows, const void *out, int32_t out_dtype, uint32_t ldc, bool allow_add = false,
+                             uint32_t max_rows = kMaxRows) {
     qdl_status st = check_weight(who, w);
     if (st != QDL_OK) return st;
-    // w8a8_decode_available
-    if (rows < 1 || rows > (uint32_t)kMaxRows || q_scale == nullptr || !fits(q, q_bytes, scale_bytes, rows, w->k, w->format))
-        return fail(rows < 1 || rows > (uint32_t)kMaxRows || q_scale == nullptr ? QDL_ERR_INVALID_ARG : QDL_ERR_SCRATCH_TOO_SMALL,
+    // w8a8_decode_available; more than 256 rows (projections only) run in
+    // passes of 256 rows through the same scratch
+    const uint32_t pass_rows = rows < (uint32_t)kMaxRows ? rows : (uint32_t)kMaxRows;
+    if (rows < 1 || rows > max_rows || q_scale == nullptr || !fits(q, q_bytes, scale_bytes, pass_rows, w->k, w->format))
+        return fail(rows < 1 || rows > max_rows || q_scale == nullptr ? QDL_ERR_INVALID_ARG : QDL_ERR_SCRATCH_TOO_SMALL,
                     "%s: not available for %u rows of [%u, %u] %s", who, rows, w->n, w->k, format_name(w->format));
     if (!aligned(q, 16) || !aligned(q_scale, 4))
         return fail(QDL_ERR_INVALID_ARG, "%s: q must be 16-byte and q_scale 4-byte aligned", who);
@@ -316,39 +319,64 @@ qdl_status qdl_w8a8_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float
     return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+
+// One decode projection of up to 256 rows: the quantiser (plain or SiLU),
+// then the GEMV; or one fused launch where that applies.
+qdl_status proj_pass(const char *who, const qdl_w8a8_weight *w, const void *x, const void *up, uint32_t ldx, uint32_t ld_up,
+                     bool silu, uint32_t rows, void *out, int32_t out_dtype, uint32_t ldc, uint8_t *q, float *q_scale,
+                     cudaStream_t stream) {
+    if (!silu && proj_is_fused(w, rows)) {
+        // one launch: the GEMV quantises its own activation blocks
+        return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, stream, ~0u, kWaitLimitNs, x, ldx);
+    }
+    ActQuantArgs a = {static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(up), ldx, ld_up, rows, w->k, q, q_scale};
+    const bool acc = zero_f32_output(a, w, rows, out, out_dtype, ldc, w->n);
+    cudaError_t e = launch_act_quant(a, w->format, silu, stream);
+    if (e != cudaSuccess) return cuda_fail(who, e);
+    return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, stream, ~0u, kWaitLimitNs, nullptr, 0, acc);
+}
+
+// Rows beyond 256 (a prefill-shaped call) in passes of 256 rows, in order on
+// the stream: each pass quantises into the same scratch, which the next
+// pass's quantiser overwrites only after the previous GEMV has finished
+// (programmatic launch orders every library kernel after its predecessor).
+qdl_status proj_passes(const char *who, const qdl_w8a8_weight *w, const void *x, const void *up, uint32_t ldx, uint32_t ld_up,
+                       bool silu, uint32_t rows, void *out, int32_t out_dtype, uint32_t ldc, uint8_t *q, float *q_scale,
+                       void *stream) {
+    const size_t elt = out_dtype == QDL_OUT_BF16 ? 2 : 4;
+    for (uint32_t done = 0; done < rows; done += (uint32_t)kMaxRows) {
+        const uint32_t n = rows - done < (uint32_t)kMaxRows ? rows - done : (uint32_t)kMaxRows;
+        const uint16_t *xp = static_cast<const uint16_t *>(x) + (size_t)done * ldx;
+        const uint16_t *up_p = silu ? static_cast<const uint16_t *>(up) + (size_t)done * ld_up : nullptr;
+        void *op = static_cast<uint8_t *>(out) + (size_t)done * ldc * elt;
+        qdl_status st = proj_pass(who, w, xp, up_p, ldx, ld_up, silu, n, op, out_dtype, ldc, q, q_scale,
+                                  static_cast<cudaStream_t>(stream));
+        if (st != QDL_OK) return st;
+    }
+    return ok();
+}
+
+}  // namespace
+
 qdl_status qdl_w8a8_proj(const qdl_w8a8_weight *w, const void *x, uint32_t ldx, uint32_t rows, void *out, int32_t out_dtype,
                          uint32_t ldc, uint8_t *q, float *q_scale, size_t q_bytes, size_t scale_bytes, void *stream) {
     const char *who = "w8a8_proj";
-    qdl_status st = check_gemv(who, w, q, q_scale, q_bytes, scale_bytes, rows, out, out_dtype, ldc);
+    qdl_status st = check_gemv(who, w, q, q_scale, q_bytes, scale_bytes, rows, out, out_dtype, ldc, false, QDL_MAX_PROJ_ROWS);
     if (st != QDL_OK) return st;
     if ((st = check_input(who, "x", x, ldx, w->k)) != QDL_OK) return st;
-    if (proj_is_fused(w, rows)) {
-        // one launch: the GEMV quantises its own activation blocks
-        return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, static_cast<cudaStream_t>(stream), ~0u,
-                           kWaitLimitNs, x, ldx);
-    }
-    ActQuantArgs a = {static_cast<const uint16_t *>(x), nullptr, ldx, 0, rows, w->k, q, q_scale};
-    const bool acc = zero_f32_output(a, w, rows, out, out_dtype, ldc, w->n);
-    cudaError_t e = launch_act_quant(a, w->format, false, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(who, e);
-    return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, static_cast<cudaStream_t>(stream), ~0u, kWaitLimitNs,
-                       nullptr, 0, acc);
+    return proj_passes(who, w, x, nullptr, ldx, 0, false, rows, out, out_dtype, ldc, q, q_scale, stream);
 }
 
 qdl_status qdl_w8a8_proj_silu(const qdl_w8a8_weight *w, const void *gate, const void *up, uint32_t ld_gate, uint32_t ld_up,
                               uint32_t rows, void *out, int32_t out_dtype, uint32_t ldc, uint8_t *q, float *q_scale, size_t q_bytes,
                               size_t scale_bytes, void *stream) {
     const char *who = "w8a8_proj_silu";
-    qdl_status st = check_gemv(who, w, q, q_scale, q_bytes, scale_bytes, rows, out, out_dtype, ldc);
+    qdl_status st = check_gemv(who, w, q, q_scale, q_bytes, scale_bytes, rows, out, out_dtype, ldc, false, QDL_MAX_PROJ_ROWS);
     if (st != QDL_OK) return st;
     if ((st = check_input(who, "gate", gate, ld_gate, w->k)) != QDL_OK) return st;
     if ((st = check_input(who, "up", up, ld_up, w->k)) != QDL_OK) return st;
-    ActQuantArgs a = {static_cast<const uint16_t *>(gate), static_cast<const uint16_t *>(up), ld_gate, ld_up, rows, w->k, q, q_scale};
-    const bool acc = zero_f32_output(a, w, rows, out, out_dtype, ldc, w->n);
-    cudaError_t e = launch_act_quant(a, w->format, true, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(who, e);
-    return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, static_cast<cudaStream_t>(stream), ~0u, kWaitLimitNs,
-                       nullptr, 0, acc);
+    return proj_passes(who, w, gate, up, ld_gate, ld_up, true, rows, out, out_dtype, ldc, q, q_scale, stream);
 }
 
 qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq, uint32_t nkv, uint32_t group,
@@ -386,11 +414,13 @@ qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq
     a.tiles_kv = (nkv + 127) / 128;
     a.vec2 = vec2;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // group 128 and widths multiples of 32: the tcgen05 kernel, 32 rows per
-    // pass; other widths multiples of 32: the CUDA-core kernel for up to 4
-    // rows; otherwise the mma.sync kernel, 16 rows per pass
+    // widths multiples of 32: the CUDA-core stream-K kernel for up to
+    // QDL_INT4_CC_MAX_ROWS rows (up to 8 where the tcgen05 kernel does not
+    // apply); above that, group 128: the tcgen05 kernel, 32 rows per pass;
+    // otherwise the mma.sync kernel, 16 rows per pass
     const bool tc = qw16 && int4_tc_supported(nq, nkv, group);
-    if (qw16 && int4_cc_supported(nq, nkv) && (m <= QDL_INT4_CC_MAX_ROWS || (m <= 4 && !tc))) {
+    static_assert(QDL_INT4_CC_MAX_ROWS <= 8, "the CUDA-core kernel takes up to 8 rows");
+    if (qw16 && int4_cc_supported(nq, nkv) && (m <= QDL_INT4_CC_MAX_ROWS || (m <= 8 && !tc))) {
         a.x = x;
         a.out0 = out[0];
         a.out1 = out[1];
@@ -443,6 +473,44 @@ qdl_status check_kv_int4(const char *who, uint32_t tokens, uint32_t head_dim, ui
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------- weight preparation
+
+qdl_status qdl_fp8_weight_quant(int32_t format, const void *w, int32_t w_dtype, uint32_t ldw, uint32_t n, uint32_t k,
+                                uint8_t *codes, float *scales, void *stream) {
+    const char *who = "qdl_fp8_weight_quant";
+    if (format != QDL_SCALE_PER_ROW && format != QDL_SCALE_BLOCK128)
+        return fail(QDL_ERR_INVALID_ARG, "%s: format=%d is not PER_ROW or BLOCK128", who, format);
+    if (w_dtype != QDL_IN_F32 && w_dtype != QDL_IN_BF16)
+        return fail(QDL_ERR_INVALID_ARG, "%s: w_dtype=%d is not F32 or BF16", who, w_dtype);
+    if (n < 1 || k < 128 || k % 128 != 0)
+        return fail(QDL_ERR_INVALID_ARG, "%s: n=%u, k=%u (want n >= 1, k a positive multiple of 128)", who, n, k);
+    const uint32_t lda = w_dtype == QDL_IN_BF16 ? 8 : 4;
+    if (ldw < k || ldw % lda != 0)
+        return fail(QDL_ERR_INVALID_ARG, "%s: ldw=%u (want ldw >= k and a multiple of %u)", who, ldw, lda);
+    if (w == nullptr || codes == nullptr || scales == nullptr)
+        return fail(QDL_ERR_INVALID_ARG, "%s: NULL pointer argument", who);
+    if (!aligned(w, 16) || !aligned(codes, 8) || !aligned(scales, 4))
+        return fail(QDL_ERR_INVALID_ARG, "%s: w must be 16-byte, codes 8-byte, scales 4-byte aligned", who);
+    if (format == QDL_SCALE_PER_ROW && n > 0x7FFFFFFFu)
+        return fail(QDL_ERR_UNSUPPORTED, "%s: n=%u rows exceed the grid", who, n);
+    cudaError_t e = launch_fp8_weight_quant(format, w, w_dtype == QDL_IN_BF16, ldw, n, k, codes, scales,
+                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(who, e);
+}
+
+qdl_status qdl_awq_pack(const uint8_t *nib, uint32_t k, uint32_t n, uint32_t *qw, void *stream) {
+    const char *who = "qdl_awq_pack";
+    if (k < 1 || n < 8 || n % 8 != 0)
+        return fail(QDL_ERR_INVALID_ARG, "%s: k=%u, n=%u (want k >= 1, n a positive multiple of 8)", who, k, n);
+    if (nib == nullptr || qw == nullptr) return fail(QDL_ERR_INVALID_ARG, "%s: NULL pointer argument", who);
+    if (!aligned(nib, 8) || !aligned(qw, 4))
+        return fail(QDL_ERR_INVALID_ARG, "%s: nib must be 8-byte, qw 4-byte aligned", who);
+    cudaError_t e = launch_awq_pack(nib, k, n, qw, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(who, e);
+}
+
+// ---------------------------------------------------------------- KV-cache codecs (entry points)
 
 qdl_status qdl_kv_quant_int8(const float *x, uint32_t tokens, uint32_t head_dim, int8_t *q, float *scale,
                              void *stream) {

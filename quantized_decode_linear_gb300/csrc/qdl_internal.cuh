@@ -18,9 +18,11 @@ namespace qdl {
 #define QDL_TUNE_FUSED 0
 #endif
 #ifndef QDL_INT4_CC_MAX_ROWS
-// token rows up to which the AWQ projection takes the CUDA-core kernel even
-// where the tcgen05 kernel applies (0: never)
-#define QDL_INT4_CC_MAX_ROWS 0
+// token rows (at most 8) up to which the AWQ projection takes the CUDA-core
+// stream-K kernel, also where the tcgen05 kernel applies.  Measured on the
+// K=4096 QKV projection (CUDA cores vs tcgen05): 8.3 vs 12.0 us at M=1,
+// 12.3 vs 12.2 us at M=4, 19.2 us at M=8 vs 13.6 us at M=16.
+#define QDL_INT4_CC_MAX_ROWS 4
 #endif
 #ifndef QDL_TUNE_EARLY_TRIGGER
 // 1: the activation quantiser releases the GEMV before its own dependency
@@ -121,8 +123,10 @@ cudaError_t launch_int4_qkv(const Int4Args &a, cudaStream_t s);
 bool int4_tc_supported(uint32_t nq, uint32_t nkv, uint32_t group);
 cudaError_t launch_int4_qkv_tc(const Int4Args &a, cudaStream_t s);  // up to 32 token rows
 cudaError_t read_and_clear_int4_fault(uint32_t *value);
+// zeroes the three f32 outputs [m, n_p] for a kernel that adds into them
+cudaError_t launch_int4_zero(const Int4Args &a, cudaStream_t s);
 bool int4_cc_supported(uint32_t nq, uint32_t nkv);                  // widths multiples of 32
-cudaError_t launch_int4_qkv_cc(const Int4Args &a, cudaStream_t s);  // 1..4 token rows, CUDA cores
+cudaError_t launch_int4_qkv_cc(const Int4Args &a, cudaStream_t s);  // 1..8 token rows, CUDA cores
 cudaError_t read_and_clear_int4cc_fault(uint32_t *value);
 
 // KV-cache quantisers (kv_cache_quant.wgsl); arguments checked by the C ABI
@@ -133,6 +137,12 @@ cudaError_t launch_kv_quant_int4(const float *x, size_t n, uint32_t group, uint8
                                  cudaStream_t s);
 cudaError_t launch_kv_dequant_int4(const uint8_t *packed, const float *scale, const float *zero, size_t n,
                                    uint32_t group, float *out, cudaStream_t s);
+
+// weight preparation (FP8 per row / 128x128 block, AWQ packing); arguments
+// checked by the C ABI
+cudaError_t launch_fp8_weight_quant(int format, const void *w, bool bf16, uint32_t ldw, uint32_t n, uint32_t k,
+                                    uint8_t *codes, float *scales, cudaStream_t s);
+cudaError_t launch_awq_pack(const uint8_t *nib, uint32_t k, uint32_t n, uint32_t *qw, cudaStream_t s);
 
 int device_sm_count();  // of the current device, cached
 

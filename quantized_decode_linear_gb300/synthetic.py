@@ -16,7 +16,9 @@ Recipe (LLM-shaped decode workloads):
 * AWQ INT4: packed words of uniform random bits (so every nibble is uniform on
   0..15), scales U(0.001, 0.02), zeros uniform on 0..15 (integers by default,
   continuous U(0, 15) on request);
-* KV-cache blocks: float32 N(0, 1) rows of head_dim values.
+* KV-cache blocks: float32 N(0, 1) rows of head_dim values;
+* weight preparation: bf16 weights N(0, std) to quantise, uniform 4-bit codes
+  (one per byte) to pack.
 """
 from __future__ import annotations
 
@@ -145,6 +147,20 @@ class KvWorkload:
     seed: int = 0
 
 
+@dataclasses.dataclass(frozen=True)
+class WeightPrepWorkload:
+    """Weight preparation: `prep` "fp8" quantises a bf16 weight [n, k] ~ N(0, w_std)
+    to FP8 with the given scale layout; "awq" packs uniform 4-bit codes [k, n]."""
+    name: str
+    prep: str
+    n: int
+    k: int
+    scale_format: int = BLOCK128
+    w_std: float = 0.015
+    rows: tuple = (1,)
+    seed: int = 0
+
+
 WORKLOADS = {
     "w8a8_perrow_m1_k1024_n1024": W8A8Workload(
         "w8a8_perrow_m1_k1024_n1024", PER_ROW, 1024, (1024,), (1,), 0.02),
@@ -161,6 +177,9 @@ WORKLOADS = {
         (1, 2, 4, 8, 16, 32, 64, 128, 256), 0.015),
     "kv_int8_t32768_d128": KvWorkload("kv_int8_t32768_d128", 128, 0, (32768,)),
     "kv_int4_t32768_d128_g128": KvWorkload("kv_int4_t32768_d128_g128", 128, 128, (32768,)),
+    "fp8_weight_quant_block128_bf16_n28672_k8192": WeightPrepWorkload(
+        "fp8_weight_quant_block128_bf16_n28672_k8192", "fp8", 28672, 8192),
+    "awq_pack_k4096_n6144": WeightPrepWorkload("awq_pack_k4096_n6144", "awq", 6144, 4096),
 }
 
 HEADLINE = "w8a8_block128_qkv_m8_k4096_n4096+1024+1024"
@@ -191,3 +210,13 @@ def int4_activations(wl: Int4Workload, rows: int) -> np.ndarray:
 def kv_values(wl: KvWorkload, rows: int, copy: int = 0) -> np.ndarray:
     """K or V rows ~ N(0, 1), float32 [rows, head_dim]"""
     return normal_f32((rows, wl.head_dim), wl.seed + 100 + copy)
+
+
+def prep_weight_bf16(wl: WeightPrepWorkload, rows: int | None = None) -> np.ndarray:
+    """bf16 bits [rows or n, k] ~ N(0, w_std)"""
+    return bf16_normal((rows or wl.n, wl.k), wl.seed + 1, wl.w_std)
+
+
+def prep_codes(wl: WeightPrepWorkload, rows: int | None = None) -> np.ndarray:
+    """uniform 4-bit codes, one per byte, [rows or k, n]"""
+    return _rng(wl.seed + 2).integers(0, 16, size=(rows or wl.k, wl.n), dtype=np.uint8)

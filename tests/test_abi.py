@@ -294,3 +294,63 @@ def test_kv_rejects(lib, fn, kw, msg):
 def test_kv_rejects_oversized(lib):
     st, err = _kv(lib, "q8", tokens=1 << 20, dim=4096)
     assert st == UNSUPPORTED and "exceeds 2^31" in err, (st, err)
+
+
+# ---------------------------------------------------------------- weight preparation
+
+def _wq(lib, **kw):
+    a = dict(fmt=0, w=DEV, dtype=0, ldw=256, n=64, k=256, codes=DEV + 0x1000000, scales=DEV + 0x2000000)
+    a.update(kw)
+    st = lib.qdl_fp8_weight_quant(a["fmt"], a["w"], a["dtype"], a["ldw"], a["n"], a["k"], a["codes"], a["scales"],
+                                  None)
+    return st, lib.qdl_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(fmt=2), "format=2"),
+    (dict(dtype=3), "w_dtype=3"),
+    (dict(n=0), "n=0"),
+    (dict(k=200, ldw=256), "k=200"),
+    (dict(k=0), "k=0"),
+    (dict(ldw=128), "ldw=128"),
+    (dict(dtype=1, ldw=260), "multiple of 8"),
+    (dict(ldw=258), "multiple of 4"),
+    (dict(w=0), "NULL"),
+    (dict(w=DEV + 8), "16-byte"),
+    (dict(codes=DEV + 4), "codes 8-byte"),
+    (dict(scales=DEV + 2), "scales 4-byte"),
+])
+def test_fp8_weight_quant_rejects(lib, kw, msg):
+    st, err = _wq(lib, **kw)
+    assert st == INVALID and msg in err, (st, err)
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(k=0), "k=0"),
+    (dict(n=12), "n=12"),
+    (dict(n=0), "n=0"),
+    (dict(nib=0), "NULL"),
+    (dict(nib=DEV + 4), "8-byte"),
+    (dict(qw=DEV + 2), "4-byte"),
+])
+def test_awq_pack_rejects(lib, kw, msg):
+    a = dict(nib=DEV, k=16, n=64, qw=DEV + 0x1000000)
+    a.update(kw)
+    st = lib.qdl_awq_pack(a["nib"], a["k"], a["n"], a["qw"], None)
+    err = lib.qdl_last_error().decode()
+    assert st == INVALID and msg in err, (st, err)
+
+
+@pytest.mark.parametrize("rows,qb,code,msg", [
+    (65537, 1 << 24, INVALID, "not available for 65537 rows"),
+    (1000, 256 * 4096 - 1, SCRATCH, "not available for 1000 rows"),
+    (100, 100 * 4096 - 1, SCRATCH, "not available for 100 rows"),
+])
+def test_proj_row_limits(lib, rows, qb, code, msg):
+    """projections take up to QDL_MAX_PROJ_ROWS rows in passes of 256 through
+    a scratch that holds min(rows, 256) rows"""
+    d = _weight(lib)
+    st = lib.qdl_w8a8_proj(ctypes.byref(d), DEV, 4096, rows, DEV + 0x4000000, 0, 6144,
+                           DEV + 0x1000000, DEV + 0x2000000, qb, 1 << 20, None)
+    err = lib.qdl_last_error().decode()
+    assert st == code and msg in err, (st, err)

@@ -54,14 +54,17 @@ def test_int4_tensor_core_path(m, k, nq, nkv):
         check_close(outs[p], ref[p], bound[p], what=f"proj {p}")
 
 
-@pytest.mark.parametrize("m", [1, 2, 3, 4])
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 8])
 @pytest.mark.parametrize("k,nq,nkv,group", [(128, 32, 32, 128), (1040, 96, 32, 16), (512, 288, 64, 32),
-                                            (4096, 512, 256, 64), (2048, 640, 160, 128), (8192, 32, 64, 128)])
+                                            (4096, 512, 256, 64), (2048, 640, 160, 128), (8192, 32, 64, 128),
+                                            (16, 64, 32, 16), (48, 96, 64, 16), (960, 256, 96, 48),
+                                            (4096, 4096, 1024, 128)])
 def test_int4_cuda_core_path(m, k, nq, nkv, group):
-    """widths multiple of 32 with 1-4 rows and group != 128: the CUDA-core
-    kernel (ragged 256-column tiles, K not a multiple of its 64-row stage,
-    groups 16..64, split-K clusters up to 8); the group-128 cases here cover
-    the tcgen05 kernel's small-row passes"""
+    """widths multiple of 32 with 1-4 rows, and 5-8 rows with group != 128:
+    the CUDA-core stream-K kernel (ragged 256-column tiles, K below one 32-row
+    stage and ending inside one, groups that end in the middle of a stage (16,
+    48), ranges over several tiles, every token-count variant); 5-8 rows with
+    group 128 take the tcgen05 kernel"""
     x = syn.normal_f32((m, k), seed=5 * m + k)
     ws = [syn.int4_awq(k, n, group, seed=p + 7 * nq) for p, n in enumerate((nq, nkv, nkv))]
     outs = _run(x, nq, nkv, group, ws)
@@ -93,3 +96,35 @@ def test_int4_full_qkv_k4096(m):
                                  [w[1] for w in ws], [w[2] for w in ws])
     for p in range(3):
         check_close(outs[p], ref[p], bound[p], what=f"proj {p} m={m}")
+
+
+@pytest.mark.parametrize("m", [1, 3])
+def test_int4_cuda_core_unaligned_outputs(m):
+    """outputs that start 4 bytes past a 16-byte boundary: the CUDA-core
+    kernel adds its totals with scalar atomics instead of 4-wide ones"""
+    k, nq, nkv, group = 1024, 512, 256, 64
+    x = syn.normal_f32((m, k), seed=40 + m)
+    ws = [syn.int4_awq(k, n, group, seed=41 + p) for p, n in enumerate((nq, nkv, nkv))]
+    bufs = [torch.full((m * n + 1,), float("nan"), device="cuda") for n in (nq, nkv, nkv)]
+    outs = [b[1:].view(m, n) for b, n in zip(bufs, (nq, nkv, nkv))]
+    assert all(o.data_ptr() % 16 == 4 for o in outs)
+    qdl.int4_qkv_gemv(dev(x), m, k, nq, nkv, group, [u32_dev(w[0]) for w in ws], [dev(w[1]) for w in ws],
+                      [dev(w[2]) for w in ws], outs)
+    torch.cuda.synchronize()
+    ref, bound = oracle.int4_qkv(x, nq, nkv, group, [w[0] for w in ws], [w[1] for w in ws],
+                                 [w[2] for w in ws])
+    for p in range(3):
+        check_close(host(outs[p]), ref[p], bound[p], what=f"proj {p}")
+
+
+def test_int4_cuda_core_many_tiles():
+    """K = 16 (one stage per tile) over 576 tiles: more CTAs than SMs, since
+    each CTA's range may touch at most four tiles"""
+    m, k, nq, nkv, group = 2, 16, 131072, 8192, 16
+    x = syn.normal_f32((m, k), seed=50)
+    ws = [syn.int4_awq(k, n, group, seed=51 + p) for p, n in enumerate((nq, nkv, nkv))]
+    outs = _run(x, nq, nkv, group, ws)
+    ref, bound = oracle.int4_qkv(x, nq, nkv, group, [w[0] for w in ws], [w[1] for w in ws],
+                                 [w[2] for w in ws])
+    for p in range(3):
+        check_close(outs[p], ref[p], bound[p], what=f"proj {p}")

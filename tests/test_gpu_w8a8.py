@@ -197,3 +197,43 @@ def test_full_perrow_silu_down_m64():
 
 def test_full_block128_gateup_sweep():
     _full_workload("w8a8_block128_gateup_k8192_n14336+14336", samples=600)
+
+
+@pytest.mark.parametrize("fmt", [qdl.PER_ROW, qdl.BLOCK128])
+@pytest.mark.parametrize("rows", [257, 300, 600])
+def test_proj_beyond_256_rows(fmt, rows):
+    """prefill-shaped calls: passes of 256 rows through one 256-row scratch,
+    ragged last pass, row stride beyond K; every output against the oracle"""
+    k = 512
+    sizes = _aligned_sizes(fmt, [256, 128, 72])
+    segs = _segments(fmt, k, sizes, seed=rows)
+    ldx = k + 16
+    x = syn.bf16_normal((rows, ldx), seed=rows + 5)
+    qo, so = oracle.act_quant(fmt, x, k)
+    yo, bo = oracle.w8a8_gemv(fmt, qo, so, segs)
+    w, _keep = upload_weight(segs, fmt)
+    q, s = scratch(256, k, fmt)
+    out = torch.full((rows, w.n), float("nan"), device="cuda")
+    qdl.w8a8_proj(w, bf16_dev(x), rows, out, q, s, ldx=ldx)
+    torch.cuda.synchronize()
+    check_close(host(out), yo, bo, what=f"fmt={fmt} rows={rows}")
+
+
+def test_proj_silu_beyond_256_rows_bf16():
+    """SiLU-fused projection over 300 rows with bf16 output (ldc > N)"""
+    fmt, k, rows = qdl.PER_ROW, 384, 300
+    segs = _segments(fmt, k, [272], seed=3)
+    xb = syn.bf16_normal((rows, 2 * k), seed=11)
+    qo, so = oracle.act_quant_silu(fmt, xb[:, :k], xb[:, k:], k)
+    yo, bo = oracle.w8a8_gemv(fmt, qo, so, segs)
+    w, _keep = upload_weight(segs, fmt)
+    q, s = scratch(256, k, fmt)
+    ldc = w.n + 8
+    out = torch.full((rows, ldc), float("nan"), device="cuda", dtype=torch.bfloat16)
+    d = bf16_dev(xb)
+    qdl.w8a8_proj_silu(w, d[:, :k], d[:, k:], rows, out, q, s, out_dtype=qdl.OUT_BF16, ld_gate=2 * k,
+                       ld_up=2 * k, ldc=ldc)
+    torch.cuda.synchronize()
+    o = host(out.float())[:, :w.n]
+    check_close(o, yo, bo, extra_rel=BF16_REL, what="silu rows=300 bf16")
+    assert torch.isnan(out[:, w.n:].float()).all()
