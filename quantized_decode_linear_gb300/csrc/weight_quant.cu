@@ -6,10 +6,12 @@
 //   s    = absmax over the row / block / 448     (binary32 division)
 //   code = e4m3(w / s)                           (binary32 division, RNE, saturating)
 // a row or block whose absmax is 0 gets s = 0 and the codes of its signed
-// zeros.  One CTA per row or block: each thread keeps up to kChunks chunks
-// of 8 values in registers between the absmax pass and the encode pass
-// (128x128 blocks and rows up to 16384 values are read from memory once),
-// the absmax is reduced across the CTA, and codes leave as 8-byte stores.
+// zeros.  One CTA of 512 threads per row or block: each thread keeps up to
+// kChunks chunks of 8 values in registers between the absmax pass and the
+// encode pass (128x128 blocks and rows up to 16384 values are read from
+// memory once), the absmax is reduced across the CTA, and codes leave as
+// 8-byte stores.  Small register footprint, so that several CTAs share an SM
+// and the divisions of one overlap the loads of another.
 //
 // AWQ (fused_int4_qkv.rs, QKV_AWQ_SHIFTS; the inverse of unpack_awq_qkv):
 // word j of row k holds the code of column 8j + i at bits SHIFT[i] ..
@@ -22,8 +24,8 @@ namespace qdl {
 
 namespace {
 
-constexpr int kThreadsW = 256;
-constexpr int kChunks = 8;  // 8-value chunks a thread keeps in registers
+constexpr int kThreadsW = 512;
+constexpr int kChunks = 4;  // 8-value chunks a thread keeps in registers
 
 template <bool kBf16>
 __device__ __forceinline__ void load8(const void *base, size_t elem, float (&v)[8]) {
@@ -48,7 +50,7 @@ __device__ __forceinline__ float wq_operand(float v, float s) { return s == 0.0f
 // kBlock: region = 128x128 block (blockIdx.x = block row * kb + block col),
 // else one row (blockIdx.x = row).  ldw in elements; k % 128 == 0.
 template <bool kBf16, bool kBlock>
-__global__ void __launch_bounds__(kThreadsW) fp8_weight_quant_kernel(const void *w, uint32_t ldw, uint32_t n,
+__global__ void __launch_bounds__(kThreadsW, 2) fp8_weight_quant_kernel(const void *w, uint32_t ldw, uint32_t n,
                                                                      uint32_t k, uint8_t *codes, float *scales) {
     __shared__ float warp_max[kThreadsW / 32];
     asm volatile("griddepcontrol.wait;" ::: "memory");  // w may come from the previous kernel

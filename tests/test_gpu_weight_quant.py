@@ -104,3 +104,43 @@ def test_quantised_weight_feeds_the_projection():
     qdl.w8a8_proj(w, bf16_dev(x), rows, out, q, s)
     torch.cuda.synchronize()
     check_close(host(out), yo, bo, what="gpu-quantised weight")
+
+
+def _boundary_values() -> np.ndarray:
+    """f32 values at and around every E4M3 rounding decision in [-448, 448]:
+    +-64 ulps about each grid point and each midpoint between neighbours,
+    every in-range bf16 pattern, and random in-range bit patterns"""
+    grid = oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))  # 0 .. 448, codes 0x00..0x7E
+    grid = np.unique(grid.astype(np.float64))
+    mids = (grid[:-1] + grid[1:]) / 2.0
+    centres = np.concatenate([grid, mids]).astype(np.float32).view(np.int32)
+    offs = np.arange(-64, 65, dtype=np.int32)
+    near = (centres[:, None] + offs[None, :]).reshape(-1)
+    near = near[(near >= 0)].view(np.float32)
+    bf = (np.arange(0, 1 << 16, dtype=np.uint32) << 16).view(np.float32)
+    rnd = np.random.default_rng(123).integers(0, 0x43E00001, size=4 << 20, dtype=np.uint32).view(np.float32)
+    v = np.concatenate([near, bf, rnd])
+    v = v[np.isfinite(v) & (np.abs(v) <= 448.0)]
+    return np.concatenate([v, -v]).astype(np.float32)
+
+
+def test_hardware_e4m3_encoding_matches_oracle_at_every_rounding_boundary():
+    """The device conversion (cvt.rn.satfinite.e4m3x2.f32, through the
+    per-row weight quantiser with every row's absmax 448, so s = 1 and the
+    codes are e4m3(v)) against the oracle's encoder written from the OCP
+    definition"""
+    v = _boundary_values()
+    k = 8192
+    per_row = k - 1
+    rows = -(-v.size // per_row)
+    w = np.zeros((rows, k), np.float32)
+    w[:, 0] = 448.0
+    flat = w[:, 1:].reshape(-1)
+    flat[:v.size] = v
+    w[:, 1:] = flat.reshape(rows, per_row)
+    codes, scales = _gpu_quant(qdl.PER_ROW, w, False, rows, k, k)
+    assert np.all(scales == 1.0)
+    got = codes[:, 1:].reshape(-1)[:v.size]
+    want = oracle.e4m3_encode(v)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, (bad.size, v[bad[:5]], got[bad[:5]], want[bad[:5]])
