@@ -305,17 +305,25 @@ __global__ void __launch_bounds__(kThreadsI4, 1)
     // ---------------------------------------------------------------- code stream (before the dependency wait)
     uint32_t codes_issued = 0;
     uint64_t pol_w = 0;
+    // lanes 0, 1, 2 of the producer warp issue a unit's codes, scales and
+    // zeros together (one issuing thread takes about 100 ns per copy); lane 0
+    // also posts the transaction count, which may follow the other lanes'
+    // copies (the phase cannot complete before lane 0 arrives)
     auto load_codes = [&](uint32_t u) {
         const uint32_t slot = u % kRing, v = v0 + u, ku = v % upt;
         const Tile t = tile_of(v / upt);
         uint8_t *st = smem + slot * kStageBytes;
-        mbar_arrive_expect_tx(&full[slot], kStageBytes);
-        tma_load_2d(st, t.w, (int32_t)(t.col0 / 8), (int32_t)(ku * kUnitK), &full[slot], pol_w);
-        tma_load_2d(st + kCodeBytes, t.s, (int32_t)t.col0, (int32_t)ku, &full[slot], pol_w);
-        tma_load_2d(st + kCodeBytes + kCols * 4, t.z, (int32_t)t.col0, (int32_t)ku, &full[slot], pol_w);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&full[slot], kStageBytes);
+            tma_load_2d(st, t.w, (int32_t)(t.col0 / 8), (int32_t)(ku * kUnitK), &full[slot], pol_w);
+        } else if (lane == 1) {
+            tma_load_2d(st + kCodeBytes, t.s, (int32_t)t.col0, (int32_t)ku, &full[slot], pol_w);
+        } else {
+            tma_load_2d(st + kCodeBytes + kCols * 4, t.z, (int32_t)t.col0, (int32_t)ku, &full[slot], pol_w);
+        }
         codes_issued = u + 1;
     };
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && lane < 3) {
         // codes, scales and zeros are read once per call; a 256-byte L2 fill
         // serves the neighbouring column tiles, which read the same K rows at
         // about the same time, so no eviction hint
@@ -368,11 +376,14 @@ __global__ void __launch_bounds__(kThreadsI4, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            // unit s converted: its stage takes unit s + kRing
+        if (lane < 3) {
+            // unit s converted: its stage takes unit s + kRing; the three
+            // lanes take the same decision (lane 0's view of the abort flag)
             for (uint32_t s = 0; s + kRing < nunits; ++s) {
                 wait(&empty[s % kRing], (s / kRing) & 1, 1);
-                if (*abort_flag) break;
+                __syncwarp(0x7u);
+                const uint32_t stop = __shfl_sync(0x7u, *abort_flag ? 1u : 0u, 0);
+                if (stop) break;
                 load_codes(s + kRing);
             }
         }
