@@ -161,13 +161,13 @@ class Int4Case:
         self.gemv_bytes = self.step_bytes
         # the library's dispatch for widths multiple of 32: up to 4 rows the
         # CUDA-core stream-K kernel (f32 products), else (group 128) tcgen05
-        # passes of 32 rows (f16 operands); each is an output-zeroing launch
+        # passes of 16 rows (f16 operands); each is an output-zeroing launch
         # and the GEMV
         if rows <= 4:
             self.gemv_launches = 1
             self.kernel, self.kernel_src, self.dtype = "int4_qkv_sk_kernel", ["int4_qkv_cc.cu"], "f32"
         else:
-            self.gemv_launches = math.ceil(rows / 32)
+            self.gemv_launches = math.ceil(rows / 16)
             self.kernel, self.kernel_src, self.dtype = "int4_qkv_tc_kernel", ["int4_qkv_tc.cu"], "f16"
         self.launches_per_step = 2 * self.gemv_launches
 

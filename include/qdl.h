@@ -197,7 +197,7 @@ QDL_API qdl_status qdl_w8a8_proj_silu(const qdl_w8a8_weight *w, const void *gate
  * With nq and nkv multiples of 32 and every qw[p] 16-byte aligned, up to 4
  * rows (up to 8 with group != 128) take one CUDA-core pass in f32 (x
  * unrounded, exact nibbles), and more rows with group 128 take the tcgen05
- * kernel once per 32 rows, which
+ * kernel once per 16 rows, which
  * multiplies x rounded to f16 with exact nibbles (error within 2^-11 of
  * sum |x w|) and applies zeros and scales per group in f32.  Both make two
  * launches: out is zeroed, then the GEMV adds per-tile partial sums into it

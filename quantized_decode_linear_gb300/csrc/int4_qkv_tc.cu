@@ -637,7 +637,8 @@ bool int4_tc_supported(uint32_t nq, uint32_t nkv, uint32_t group) {
     return group == (uint32_t)kGroupK && nq % 32 == 0 && nkv % 32 == 0;
 }
 
-// Two launches (zeroing, then the GEMV) for up to 32 token rows.
+// Two launches (zeroing, then the GEMV) for up to 32 token rows (the API
+// passes QDL_INT4_TC_PASS_ROWS at a time).
 cudaError_t launch_int4_qkv_tc(const Int4Args &a, cudaStream_t s) {
     CUtensorMap maps[9];
     const uint32_t ns[3] = {a.nq, a.nkv, a.nkv};
@@ -658,7 +659,7 @@ cudaError_t launch_int4_qkv_tc(const Int4Args &a, cudaStream_t s) {
     Int4Args b = a;  // this kernel's tiles are 128 columns wide
     b.tiles_q = (a.nq + kCols - 1) / kCols;
     b.tiles_kv = (a.nkv + kCols - 1) / kCols;
-    return a.m <= 16 ? launch_i4<16>(b, maps, s) : launch_i4<32>(b, maps, s);
+    return a.m <= 16 ? launch_i4<16>(b, maps, s) : launch_i4<32>(b, maps, s);  // the API passes at most QDL_INT4_TC_PASS_ROWS
 }
 
 cudaError_t read_and_clear_int4_fault(uint32_t *value) {

@@ -416,7 +416,8 @@ qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     // widths multiples of 32: the CUDA-core stream-K kernel for up to
     // QDL_INT4_CC_MAX_ROWS rows (up to 8 where the tcgen05 kernel does not
-    // apply); above that, group 128: the tcgen05 kernel, 32 rows per pass;
+    // apply); above that, group 128: the tcgen05 kernel, QDL_INT4_TC_PASS_ROWS
+    // rows per pass;
     // otherwise the mma.sync kernel, 16 rows per pass
     const bool tc = qw16 && int4_tc_supported(nq, nkv, group);
     static_assert(QDL_INT4_CC_MAX_ROWS <= 8, "the CUDA-core kernel takes up to 8 rows");
@@ -430,7 +431,8 @@ qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq
         if (e != cudaSuccess) return cuda_fail(who, e);
         return ok();
     }
-    const uint32_t chunk = tc ? 32 : 16;
+    static_assert(QDL_INT4_TC_PASS_ROWS == 16 || QDL_INT4_TC_PASS_ROWS == 32, "tcgen05 AWQ passes of 16 or 32 rows");
+    const uint32_t chunk = tc ? QDL_INT4_TC_PASS_ROWS : 16;
     for (uint32_t done = 0; done < m; done += chunk) {
         const uint32_t mm = m - done < chunk ? m - done : chunk;
         a.x = x + (size_t)done * k;

@@ -24,6 +24,12 @@ namespace qdl {
 // 12.3 vs 12.2 us at M=4, 19.2 us at M=8 vs 13.6 us at M=16.
 #define QDL_INT4_CC_MAX_ROWS 4
 #endif
+#ifndef QDL_INT4_TC_PASS_ROWS
+// token rows per pass of the tcgen05 AWQ kernel (16 or 32).  Measured on the
+// K=4096 QKV projection: one 32-row pass takes 28.3 us, one 16-row pass
+// 13.2 us, so more rows go faster in passes of 16
+#define QDL_INT4_TC_PASS_ROWS 16
+#endif
 #ifndef QDL_TUNE_EARLY_TRIGGER
 // 1: the activation quantiser releases the GEMV before its own dependency
 // wait, so consecutive calls overlap (the next GEMV streams weights while the
@@ -121,7 +127,7 @@ uint32_t choose_split_k(uint32_t tiles, uint32_t kb, const uint32_t *slots, doub
 void resident_cta_slots(const void *func, int threads, size_t smem, int per_sm, uint32_t *out);
 cudaError_t launch_int4_qkv(const Int4Args &a, cudaStream_t s);
 bool int4_tc_supported(uint32_t nq, uint32_t nkv, uint32_t group);
-cudaError_t launch_int4_qkv_tc(const Int4Args &a, cudaStream_t s);  // up to 32 token rows
+cudaError_t launch_int4_qkv_tc(const Int4Args &a, cudaStream_t s);  // up to QDL_INT4_TC_PASS_ROWS token rows
 cudaError_t read_and_clear_int4_fault(uint32_t *value);
 // zeroes the three f32 outputs [m, n_p] for a kernel that adds into them
 cudaError_t launch_int4_zero(const Int4Args &a, cudaStream_t s);
