@@ -43,6 +43,21 @@ TRAFFIC = {
 }
 
 
+def _nvtx_push(torch, name):
+    """NVTX range around a timed region (visible to ncu --nvtx and nsys)"""
+    try:
+        torch.cuda.nvtx.range_push(name)
+    except Exception:
+        pass
+
+
+def _nvtx_pop(torch):
+    try:
+        torch.cuda.nvtx.range_pop()
+    except Exception:
+        pass
+
+
 def _rank_world():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
         int(os.environ.get("LOCAL_RANK", "0"))
@@ -600,16 +615,20 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _nvtx_push(torch, "qdl timed steps")
     e0.record(stream)
     replay(timed)
     e1.record(stream)
+    _nvtx_pop(torch)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     # dominant kernel alone, same graphs-of-launches method
     d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _nvtx_push(torch, "qdl dominant kernel")
     d0.record(stream)
     replay(dom)
     d1.record(stream)
+    _nvtx_pop(torch)
     torch.cuda.synchronize()
     dom_ms = d0.elapsed_time(d1)
     clk = clocks.stop()
@@ -629,9 +648,11 @@ def run_gpu(args, rank, world, local_rank):
         g.replay()
     torch.cuda.synchronize()
     x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _nvtx_push(torch, "qdl end-to-end steps")
     x0.record(stream)
     replay(e2e_graphs)
     x1.record(stream)
+    _nvtx_pop(torch)
     torch.cuda.synchronize()
     e2e_s = x0.elapsed_time(x1) / 1e3
     if dist:
