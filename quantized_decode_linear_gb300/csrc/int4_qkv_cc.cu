@@ -34,8 +34,10 @@
 // together; a warp waits only for the stages its slice touches.
 //
 // Roles:
-//   warp 0, one lane : TMA producer: per stage the [32 rows x 32 words] codes
-//                      and the [tokens x 32] box of x.
+//   warp 0           : TMA producer (one lane per stage for 1-2 tokens,
+//                      lane 0 for all stages otherwise): the stage's
+//                      [32 rows x 32 words] codes, and its [tokens x 32] box
+//                      of x after the dependency wait.
 //   warps 1..C       : consumers; lane l owns word column l (8 output
 //                      columns).  Per 16-row half: the 16 code words are
 //                      loaded first, then converted and multiplied.  Sums
@@ -182,17 +184,39 @@ __global__ void __launch_bounds__(Sk<MT>::kThreads, 1)
         if (threadIdx.x == 0) fault(4);  // the launcher sizes ranges so this cannot happen
     } else if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // codes before waiting for the previous kernel (weights are not
+        // written by it), x after.  For 1-2 tokens lane l requests stages
+        // l, l + 32, ... (one issuing thread took about 1 us for its first
+        // copy and 100-150 ns for each further one): 8.1 -> 6.6 us at M = 1,
+        // 8.8 -> 7.5 us at M = 2 on the QKV workload.  For more tokens, whose
+        // compute is longer, lane 0 requests them in order (11.6 us at M = 4,
+        // 12.0 with every lane issuing).
+        const uint64_t pol = policy_evict_first();
+        const uint64_t pol_x = policy_evict_last();
+        constexpr uint32_t kTx = kCodeBytes + MT * 128;
         if (lane == 0) {
-            const CUtensorMap *maps[3] = {&tm_q, &tm_k, &tm_v};
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_x);
-            const uint64_t pol = policy_evict_first();
-            const uint64_t pol_x = policy_evict_last();
-            constexpr uint32_t kTx = kCodeBytes + MT * 128;
-            // codes before waiting for the previous kernel (weights are not
-            // written by it), x after
+        }
+        if constexpr (MT <= 2) {
+            Walk w0 = {t_first + (st_first + lane) / stages, (st_first + lane) % stages};
+            Walk wk = w0;
+            for (uint32_t j = lane; j < nloc; j += 32, wk.advance(32, stages)) {
+                uint32_t proj, tile;
+                tile_proj(a, wk.tile, proj, tile);
+                const CUtensorMap *map = proj == 0 ? &tm_q : proj == 1 ? &tm_k : &tm_v;
+                mbar_arrive_expect_tx(&full[j], kTx);
+                tma_load_2d(smem + j * kStageS, map, (int32_t)(tile * 32), (int32_t)(wk.st * kRowsS), &full[j], pol);
+            }
+            issued = nloc;  // every stage was requested (read by lane 0 when draining)
+            asm volatile("griddepcontrol.wait;" ::: "memory");  // x and the zeroed outputs come from earlier kernels
+            Walk wx = w0;
+            for (uint32_t j = lane; j < nloc; j += 32, wx.advance(32, stages))
+                tma_load_2d(smem + j * kStageS + kCodeBytes, &tm_x, (int32_t)(wx.st * kRowsS), 0, &full[j], pol_x);
+        } else if (lane == 0) {
+            const CUtensorMap *maps[3] = {&tm_q, &tm_k, &tm_v};
             Walk wk = {t_first, st_first};
             for (uint32_t j = 0; j < nloc; ++j, wk.advance(1, stages)) {
                 uint32_t proj, tile;
