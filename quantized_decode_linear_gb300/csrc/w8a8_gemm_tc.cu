@@ -77,6 +77,13 @@ namespace cg = cooperative_groups;
 #endif
 // token buckets in which the accumulating Block128 GEMV runs stream-K (at 256
 // tokens the f32 atomics of the shared tiles cost more than the balance wins)
+// ... and for the Block128 128-token variants (the stream-K GEMV of the f32
+// projection among them): 4 stages instead of 3 took the K=8192, N=28672
+// gate/up projection at M=128 from 77.0 to 72.3 us; more budget for the
+// per-row and 256-token variants measured slower
+#ifndef QDL_TC_STAGE_BYTES_B128
+#define QDL_TC_STAGE_BYTES_B128 (144 * 1024)
+#endif
 #ifndef QDL_STREAMK_MIN_NTOK
 #define QDL_STREAMK_MIN_NTOK 32
 #endif
@@ -128,7 +135,9 @@ struct Tc {
     static constexpr uint32_t kABytes = NTOK * 128;
     static constexpr uint32_t kStage = kWBytes + kABytes;  // multiple of 1024 (NTOK % 8 == 0)
     // pipeline depth: as many stages as fit a per-CTA budget, at least 3
-    static constexpr uint32_t kBudget = NTOK >= QDL_TC_BIG_NTOK ? QDL_TC_STAGE_BYTES_BIG : QDL_TC_STAGE_BYTES;
+    static constexpr uint32_t kBudget = kBlock && NTOK == 128 ? QDL_TC_STAGE_BYTES_B128
+                                        : NTOK >= QDL_TC_BIG_NTOK ? QDL_TC_STAGE_BYTES_BIG
+                                                                  : QDL_TC_STAGE_BYTES;
     static constexpr int kMinStages = NTOK <= 64 ? QDL_TC_MIN_STAGES : 3;
     static constexpr int kStages = (int)(kBudget / kStage) < kMinStages ? kMinStages : (int)(kBudget / kStage);
     // Block128 accumulator buffers: the MMA may run kAcc-1 blocks ahead of
