@@ -77,12 +77,18 @@ namespace cg = cooperative_groups;
 #endif
 // token buckets in which the accumulating Block128 GEMV runs stream-K (at 256
 // tokens the f32 atomics of the shared tiles cost more than the balance wins)
-// ... and for the Block128 128-token variants (the stream-K GEMV of the f32
-// projection among them): 4 stages instead of 3 took the K=8192, N=28672
-// gate/up projection at M=128 from 77.0 to 72.3 us; more budget for the
-// per-row and 256-token variants measured slower
+// ... and for the Block128 64- and 128-token variants (the stream-K GEMV of
+// the f32 projection among them), one CTA per SM with a deeper ring: on the
+// K=8192, N=28672 gate/up projection, 7 stages of 24 KB took M=64 from 65.9
+// to 59.3 us (2 CTAs of 3 stages before; 5 stages 61.8, 8 stages 60.0), and 4
+// stages of 32 KB took M=128 from 77.0 to 72.2 us (6 stages 75.4).  Deeper
+// rings measured no better for the 32-token variant (48.0 vs 48.4 us at
+// M=32) and slower for the per-row and 256-token variants.
 #ifndef QDL_TC_STAGE_BYTES_B128
 #define QDL_TC_STAGE_BYTES_B128 (144 * 1024)
+#endif
+#ifndef QDL_TC_STAGE_BYTES_B64
+#define QDL_TC_STAGE_BYTES_B64 (168 * 1024)
 #endif
 #ifndef QDL_STREAMK_MIN_NTOK
 #define QDL_STREAMK_MIN_NTOK 32
@@ -136,6 +142,7 @@ struct Tc {
     static constexpr uint32_t kStage = kWBytes + kABytes;  // multiple of 1024 (NTOK % 8 == 0)
     // pipeline depth: as many stages as fit a per-CTA budget, at least 3
     static constexpr uint32_t kBudget = kBlock && NTOK == 128 ? QDL_TC_STAGE_BYTES_B128
+                                        : kBlock && NTOK == 64  ? QDL_TC_STAGE_BYTES_B64
                                         : NTOK >= QDL_TC_BIG_NTOK ? QDL_TC_STAGE_BYTES_BIG
                                                                   : QDL_TC_STAGE_BYTES;
     static constexpr int kMinStages = NTOK <= 64 ? QDL_TC_MIN_STAGES : 3;
