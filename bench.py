@@ -63,6 +63,45 @@ def _rank_world():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+class Replicas:
+    """N independent replicas of the step, one process per GPU under torchrun.
+    The replicas exchange nothing on the data path: the only collectives are
+    a barrier before each timed region and the maximum of the ranks' elapsed
+    times after it.  `backend`/`device` are NCCL on the GPU; the same code runs
+    over gloo on the CPU."""
+
+    def __init__(self, world, backend="nccl", device="cuda"):
+        self.world, self.device, self.dist = world, device, None
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend)
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist:
+            self.dist.barrier()
+
+    def max(self, v):
+        """the maximum of `v` over all ranks"""
+        if not self.dist:
+            return float(v)
+        import torch
+        t = torch.tensor([float(v)], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist:
+            self.dist.destroy_process_group()
+            self.dist = None
+
+
+def aggregate_gbs(bytes_per_step, steps, world, seconds):
+    """whole-job throughput: the bytes every rank streamed over the slowest
+    rank's time"""
+    return bytes_per_step * steps * world / seconds / 1e9
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -524,19 +563,20 @@ def _cpu_baseline(wl, rows, syn, budget_s=12.0):
 
 # ---------------------------------------------------------------- arms
 
-def run_reference(args, rank, world):
+def run_reference(args, rank, world, budget_s=120.0):
+    """times the oracle on rank 0 alone; `budget_s` sizes each step so the
+    whole warm-up + timed run takes about that long"""
     if rank != 0:
         return
     from quantized_decode_linear_gb300 import synthetic as syn
     import oracle
     wl = syn.WORKLOADS[args.workload]
     rows = args.rows or wl.rows[0]
-    # size one step so that the whole run takes about two minutes of CPU time
     fn, b, desc = _oracle_step_fn(wl, rows, syn, 1.0 / 512)
     t0 = time.perf_counter()
     fn()
     t_probe = max(time.perf_counter() - t0, 1e-4)
-    per_step = 120.0 / max(1, args.steps + args.warmup)
+    per_step = budget_s / max(1, args.steps + args.warmup)
     frac = min(1.0, max(1.0 / 4096, (1.0 / 512) * per_step / t_probe))
     fn, b, desc = _oracle_step_fn(wl, rows, syn, frac)
     for _ in range(args.warmup):
@@ -551,7 +591,8 @@ def run_reference(args, rank, world):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32" if hasattr(wl, "head_dim") else "f64",
             "data": "synthetic",
-            "config": {"workload": wl.name, "rows": rows, "parallelism": "replicas"},
+            "config": {"workload": wl.name, "rows": rows,
+                       "parallelism": "replicas" if world > 1 else "single"},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -566,10 +607,7 @@ def run_gpu(args, rank, world, local_rank):
 
     qbuild.build()
     torch.cuda.set_device(local_rank)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+    group = Replicas(world)
     props = torch.cuda.get_device_properties(local_rank)
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 2**20
 
@@ -610,8 +648,7 @@ def run_gpu(args, rank, world, local_rank):
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
-    if dist:
-        dist.barrier()
+    group.barrier()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -632,12 +669,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     dom_ms = d0.elapsed_time(d1)
     clk = clocks.stop()
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-        if dist:
-            dist.barrier()
+    ms = group.max(ms)
 
     # end to end through the public API with host buffers: every step copies
     # its inputs from pinned host memory, makes the library call and copies
@@ -646,6 +678,7 @@ def run_gpu(args, rank, world, local_rank):
     e2e_graphs = graphs_for(case.e2e_step)
     for g in e2e_graphs[0] + ([e2e_graphs[1]] if e2e_graphs[1] is not None else []):
         g.replay()
+    group.barrier()
     torch.cuda.synchronize()
     x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     _nvtx_push(torch, "qdl end-to-end steps")
@@ -655,10 +688,7 @@ def run_gpu(args, rank, world, local_rank):
     _nvtx_pop(torch)
     torch.cuda.synchronize()
     e2e_s = x0.elapsed_time(x1) / 1e3
-    if dist:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = group.max(e2e_s)
     eager_steps = min(steps, 2000)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -669,7 +699,7 @@ def run_gpu(args, rank, world, local_rank):
     h2d, d2h = case.e2e_bytes()
 
     peak, peak_kind = _peaks()
-    value = case.step_bytes * steps * world / (ms / 1e3) / 1e9
+    value = aggregate_gbs(case.step_bytes, steps, world, ms / 1e3)
     dom_launch_s = dom_ms / 1e3 / (steps * case.gemv_launches)
     achieved = case.gemv_bytes / case.gemv_launches / dom_launch_s / 1e9
     key = f"{wl.name}@{rows}"
@@ -686,7 +716,7 @@ def run_gpu(args, rank, world, local_rank):
                      "kernel": case.kernel,
                      "peak_source": f"{peak_kind} hbm_gbs", "kernel_us": dom_launch_s * 1e6},
         "hbm_frac_step": value / world / peak,
-        "e2e": {"value": case.step_bytes * steps * world / e2e_s / 1e9, "unit": "GB/s",
+        "e2e": {"value": aggregate_gbs(case.step_bytes, steps, world, e2e_s), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_call": e2e_s / steps * 1e6, "method": "graphs of copy-in, call, copy-out",
                 "eager_us_per_call": eager_s / eager_steps * 1e6},
@@ -697,8 +727,7 @@ def run_gpu(args, rank, world, local_rank):
         line["cpu_baseline"] = _cpu_baseline(wl, rows, syn)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
+    group.close()
 
 
 def main():
