@@ -85,6 +85,7 @@ def _load():
             lib.orc_fp8_weight_quant.argtypes = [I, P, S, I, I, P, P]
             lib.orc_awq_pack.argtypes = [P, I, I, P]
             lib.orc_num_threads.restype = I
+            lib.orc_set_num_threads.argtypes = [I]
             _lib = lib
     return _lib
 
@@ -99,6 +100,12 @@ def _c(a, dtype) -> np.ndarray:
 
 def num_threads() -> int:
     return _load().orc_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """threads for the oracle's later parallel loops (timing only; results do
+    not depend on it)"""
+    _load().orc_set_num_threads(int(n))
 
 
 def e4m3_encode(v) -> np.ndarray:

@@ -23,6 +23,14 @@ int orc_num_threads(void) {
 #endif
 }
 
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 static void *malloc_or_die(size_t bytes) {
     void *p = malloc(bytes ? bytes : 1);
     if (!p) {

@@ -107,6 +107,8 @@ void orc_kv_dequant_int4(const uint8_t *packed, const float *scale, const float 
                          float *out);
 
 int orc_num_threads(void);
+/* threads for later parallel loops (OpenMP); no effect in a serial build */
+void orc_set_num_threads(int n);
 
 #ifdef __cplusplus
 }

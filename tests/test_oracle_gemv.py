@@ -117,3 +117,19 @@ def test_sampled_equals_full():
     c = rng.integers(0, 296, 50)
     ys, bs = oracle.w8a8_gemv_sampled(oracle.BLOCK128, q, s, ws, r, c)
     assert np.array_equal(ys, y[r, c]) and np.array_equal(bs, b[r, c])
+
+
+def test_result_does_not_depend_on_thread_count():
+    """the oracle's parallel loops split output columns only, so one thread
+    and all threads give the same bits (the CPU baseline times both)"""
+    q, s, ws = _case(oracle.BLOCK128, 3, 512, [256, 128, 72], seed=11)
+    cores = oracle.num_threads()
+    y, b = oracle.w8a8_gemv(oracle.BLOCK128, q, s, ws)
+    oracle.set_num_threads(1)
+    try:
+        assert oracle.num_threads() == 1 or cores == 1
+        y1, b1 = oracle.w8a8_gemv(oracle.BLOCK128, q, s, ws)
+    finally:
+        oracle.set_num_threads(cores)
+    assert oracle.num_threads() == cores
+    assert np.array_equal(y, y1) and np.array_equal(b, b1)
