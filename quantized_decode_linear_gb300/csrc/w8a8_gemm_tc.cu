@@ -64,9 +64,16 @@ namespace cg = cooperative_groups;
 // kernels as soon as it starts (before its own dependency wait it only
 // streams read-only weights), so that the next call's kernels launch while
 // this one streams.  Measured: 38.1 -> 36.6 us on the K=8192, N=28672 gate/up
-// projection at M=1, but 7.7 -> 8.0 us on the 25 MB QKV projection at M=8 and
-// slower at 256 tokens.
-#define QDL_TC_EARLY_TRIGGER_BYTES (32ull << 20)
+// projection at M=1.  On the 25 MB QKV projection at M=8 it pays only with
+// the 3-stage ring below (8.01 -> 7.58 us per call): with 4 stages, 3 CTAs
+// per SM, the next call's CTAs found almost no free slot and the call slowed
+// (7.7 -> 8.0 us).
+#define QDL_TC_EARLY_TRIGGER_BYTES (16ull << 20)
+#endif
+#ifndef QDL_TC_STAGE_BYTES_16
+// the 16-token variants: 3 stages of 18 KB, so that 4 CTAs share an SM and
+// the next call's early CTAs find free slots while this call streams
+#define QDL_TC_STAGE_BYTES_16 (54 * 1024)
 #endif
 #ifndef QDL_TC_STAGE_BYTES
 #define QDL_TC_STAGE_BYTES (72 * 1024)
@@ -144,6 +151,7 @@ struct Tc {
     static constexpr uint32_t kBudget = kBlock && NTOK == 128 ? QDL_TC_STAGE_BYTES_B128
                                         : kBlock && NTOK == 64  ? QDL_TC_STAGE_BYTES_B64
                                         : NTOK >= QDL_TC_BIG_NTOK ? QDL_TC_STAGE_BYTES_BIG
+                                        : NTOK == 16 && !kFused   ? QDL_TC_STAGE_BYTES_16
                                                                   : QDL_TC_STAGE_BYTES;
     static constexpr int kMinStages = NTOK <= 64 ? QDL_TC_MIN_STAGES : 3;
     static constexpr int kStages = (int)(kBudget / kStage) < kMinStages ? kMinStages : (int)(kBudget / kStage);
