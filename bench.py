@@ -37,7 +37,7 @@ FALLBACK_HBM_GBS = 6800.0
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and rows;
 # valid only while the kernel source hash matches.  Source: profiles/.
 TRAFFIC = {
-    "w8a8_block128_qkv_m8_k4096_n4096+1024+1024@8": {"bytes": 25441792 + 0, "src": "d472853609100ba0"},
+    "w8a8_block128_qkv_m8_k4096_n4096+1024+1024@8": {"bytes": 25441536 + 0, "src": "667d260eb6dfb6f7"},
     "int4_awq_qkv_k4096_nq4096_nkv1024_g128@1": {"bytes": 14220800 + 0, "src": "1918a975bcd9095e"},
     "int4_awq_qkv_k4096_nq4096_nkv1024_g128@4": {"bytes": 14359296 + 0, "src": "1918a975bcd9095e"},
 }

@@ -97,6 +97,9 @@ namespace cg = cooperative_groups;
 #ifndef QDL_TC_STAGE_BYTES_B64
 #define QDL_TC_STAGE_BYTES_B64 (168 * 1024)
 #endif
+#ifndef QDL_TC_ADD_NOCLUSTER
+#define QDL_TC_ADD_NOCLUSTER 1
+#endif
 #ifndef QDL_STREAMK_MIN_NTOK
 #define QDL_STREAMK_MIN_NTOK 32
 #endif
@@ -1012,15 +1015,29 @@ cudaError_t launch_tc_variant(const W8A8Args &a, const CUtensorMap (&maps)[7], c
     cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kAlloc;
     cfg.stream = s;
+    // Split-K ranks that add into a zeroed output never meet.  When the
+    // previous call releases this one early, launching them without a cluster
+    // lets each CTA take a slot as soon as one frees instead of waiting for
+    // `split` free slots in one GPC: 7.58 -> 7.21 us per call on the 25 MB QKV
+    // projection at M=8.  Without the early release, clusters measured faster
+    // (1 MB per-row projection at M=1: 4.44 us clustered, 4.81 without).
+    const bool clustered = split > 1 && !(a.accumulate && a.early_trigger && QDL_TC_ADD_NOCLUSTER);
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = split;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    int na = 0;
+    if (clustered) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = split;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (QDL_TUNE_PDL) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = QDL_TUNE_PDL ? 2 : 1;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, w8a8_gemm_tc_kernel<NTOK, kBlock, kFused>, maps[0], maps[1], maps[2], maps[3],
                               maps[4], maps[5], maps[6], a);
 }
