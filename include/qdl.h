@@ -327,7 +327,9 @@ typedef struct {
     int32_t kernel;      /* 0 = tcgen05 (tensor memory), 1 = mma.sync streaming */
     uint32_t mma_n;      /* token columns per MMA (tcgen05: 16..256) */
     uint32_t tiles;      /* 128-row output tiles */
-    uint32_t split_k;    /* CTAs per tile along K (one cluster) */
+    uint32_t split_k;    /* CTAs per tile along K: one cluster, except where the projection's
+                            accumulating GEMV (16-token bucket, >= 16 MB of weights) adds
+                            the ranks' partials into out and launches them unclustered */
     uint32_t stages;     /* shared-memory pipeline stages per CTA */
     uint32_t threads;    /* threads per CTA */
     uint32_t smem_bytes; /* dynamic shared memory per CTA */
