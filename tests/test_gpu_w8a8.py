@@ -191,6 +191,36 @@ def test_full_block128_qkv_m8():
     _full_workload("w8a8_block128_qkv_m8_k4096_n4096+1024+1024")
 
 
+def test_large_projections_back_to_back():
+    """A 16-token projection over 16 MB of weights or more releases the next
+    call's kernels at its start, and its split-K ranks add into the zeroed
+    output without a cluster.  Back-to-back calls over two such weights, with
+    no host synchronisation between them and one activation scratch, must each
+    match the oracle: no kernel may read or write shared data before the call
+    ahead of it has finished."""
+    wl = syn.WORKLOADS["w8a8_block128_qkv_m8_k4096_n4096+1024+1024"]
+    rows, k = 8, wl.k
+    segs = [syn.w8a8_weights(wl), _segments(wl.fmt, k, wl.segments, seed=900)]
+    weights = [upload_weight(sg, wl.fmt) for sg in segs]
+    xs = [syn.w8a8_activations(wl, rows), syn.bf16_normal((rows, k), seed=901)]
+    xd = [bf16_dev(x) for x in xs]
+    refs = [oracle.act_quant(wl.fmt, x, k) for x in xs]
+    q, s = scratch(rows, k, wl.fmt)
+    outs = [torch.empty((rows, wl.n), device="cuda") for _ in range(4)]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for i, out in enumerate(outs):
+            qdl.w8a8_proj(weights[i % 2][0], xd[i % 2], rows, out, q, s)
+        torch.cuda.synchronize()
+        for i, out in enumerate(outs):
+            qo, so = refs[i % 2]
+            r, c = _samples(rows, wl.n, wl.segments, 400, seed=10 * rep + i)
+            ys, bs = oracle.w8a8_gemv_sampled(wl.fmt, qo, so, segs[i % 2], r, c)
+            o = host(out)
+            check_close(o[r, c], ys, bs, what=f"repeat {rep} call {i}")
+            assert np.all(np.isfinite(o))
+
+
 def test_full_perrow_silu_down_m64():
     _full_workload("w8a8_perrow_silu_down_m64_k14336_n4096")
 
