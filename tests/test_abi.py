@@ -354,3 +354,57 @@ def test_proj_row_limits(lib, rows, qb, code, msg):
                            DEV + 0x1000000, DEV + 0x2000000, qb, 1 << 20, None)
     err = lib.qdl_last_error().decode()
     assert st == code and msg in err, (st, err)
+
+
+def _static(lib, d, rows=8, x=DEV, ldx=4096, out=DEV + 0x4000000, dtype=qdl.OUT_F32, ldc=6144):
+    st = lib.qdl_w8a8_proj_static(ctypes.byref(d), x, ldx, rows, out, dtype, ldc, None)
+    return st, lib.qdl_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,code,msg", [
+    (dict(rows=0), INVALID, "0 rows, want 1..=256"),
+    (dict(rows=257), INVALID, "257 rows, want 1..=256"),
+    (dict(ldc=6143), INVALID, "ldc=6143 < N=6144"),
+    (dict(dtype=qdl.OUT_F32_ADD), INVALID, "output dtype 2"),
+    (dict(out=0), INVALID, "output is NULL"),
+    (dict(out=DEV + 2), INVALID, "misaligned"),
+    (dict(x=0), INVALID, "x is NULL"),
+    (dict(ldx=4095), INVALID, "x stride=4095"),
+    (dict(x=DEV + 8), INVALID, "x must be 16-byte aligned"),
+])
+def test_proj_static_rejects(lib, kw, code, msg):
+    """the no-allocation projection checks everything before it looks up its
+    scratch or launches"""
+    st, err = _static(lib, _weight(lib), **kw)
+    assert st == code and msg in err, (st, err)
+
+
+def test_proj_static_scratch_limit(lib):
+    # 256 rows of K = 16384: 4 MiB of codes plus the scales exceed the 4 MiB buffer
+    st, d, _ = _init(lib, [(128, 16384)], fmt=qdl.BLOCK128)
+    assert st == 0
+    st, err = _static(lib, d, rows=256, ldx=16384, ldc=128)
+    assert st == UNSUPPORTED and "static scratch" in err, (st, err)
+    # K = 15872 is the largest that fits at 256 rows: the call gets past the
+    # scratch check and stops at the next one (an ldc below N, on purpose)
+    st, d, _ = _init(lib, [(128, 15872)], fmt=qdl.BLOCK128)
+    assert st == 0
+    st, err = _static(lib, d, rows=256, ldx=15872, ldc=127)
+    assert st == INVALID and "ldc=127 < N=128" in err, (st, err)
+
+
+def test_proj_static_rejects_uninitialised_weight(lib):
+    st, err = _static(lib, qdl.W8A8WeightDesc())
+    assert st == INVALID and "qdl_w8a8_weight_init" in err
+
+
+def test_plan_rejects(lib):
+    d = _weight(lib)
+    plan = qdl.Plan()
+    assert lib.qdl_w8a8_plan(ctypes.byref(d), 8, None) == INVALID
+    assert "plan is NULL" in lib.qdl_last_error().decode()
+    for rows in (0, 257):
+        assert lib.qdl_w8a8_plan(ctypes.byref(d), rows, ctypes.byref(plan)) == INVALID
+        assert f"{rows} rows, want 1..=256" in lib.qdl_last_error().decode()
+    assert lib.qdl_w8a8_plan(ctypes.byref(qdl.W8A8WeightDesc()), 8, ctypes.byref(plan)) == INVALID
+    assert "qdl_w8a8_weight_init" in lib.qdl_last_error().decode()
