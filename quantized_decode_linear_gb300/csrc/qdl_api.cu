@@ -259,7 +259,7 @@ qdl_status qdl_w8a8_weight_init(qdl_w8a8_weight *out, const qdl_fp8_segment *seg
 
 qdl_status qdl_scratch_bytes(uint32_t max_k, size_t *q_bytes, size_t *scale_bytes) {
     const size_t rows = kMaxRows;
-    const size_t groups = (max_k + kKUnit - 1) / kKUnit;
+    const size_t groups = ((size_t)max_k + kKUnit - 1) / kKUnit;  // no 32-bit wrap near UINT32_MAX
     if (q_bytes) *q_bytes = rows * max_k;
     if (scale_bytes) *scale_bytes = rows * (groups > 1 ? groups : 1) * 4;
     return ok();

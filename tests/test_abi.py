@@ -71,6 +71,8 @@ def test_scratch_bytes(lib):
     assert qdl.scratch_bytes(128) == (32768, 1024)
     assert qdl.scratch_bytes(4096) == (256 * 4096, 256 * 32 * 4)
     assert qdl.scratch_bytes(4097) == (256 * 4097, 256 * 33 * 4)
+    big = 2**32 - 1  # the group count must not wrap in 32 bits
+    assert qdl.scratch_bytes(big) == (256 * big, 256 * 2**25 * 4)
 
 
 # ---------------------------------------------------------------- weight descriptor
