@@ -111,7 +111,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
 
 
 def last_error() -> str:
-    return load().qdl_last_error().decode()
+    return _call("qdl_last_error").decode()
 
 
 def _check(status: int):
@@ -119,13 +119,39 @@ def _check(status: int):
         raise QdlError(status, last_error())
 
 
-def _ptr(t) -> int | None:
-    """device address of a tensor or an int; None -> NULL"""
+def _ptr(t, name: str = "tensor", nbytes: int | None = None) -> int | None:
+    """device address of a CUDA tensor, or a raw device pointer (int) passed
+    through; None -> NULL.  With `nbytes`, the bytes the call reads or writes
+    from the tensor's first element must lie inside the tensor's storage, so
+    that a buffer too small for the call (or of a narrower dtype than the call
+    assumes) is refused here instead of being overrun on the device."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if nbytes is not None:
+        avail = t.untyped_storage().nbytes() - t.storage_offset() * t.element_size()
+        if nbytes > avail:
+            raise ValueError(f"{name}: the call touches {nbytes} bytes from its first element, "
+                             f"but its storage holds {avail}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor, got one on {t.device}")
     return t.data_ptr()
+
+
+def _call(name: str, *args):
+    """calls the library's `name` with arguments marshalled (and checked)
+    beforehand"""
+    return getattr(load(), name)(*args)
+
+
+def _rows_span(rows: int, ld: int, width: int, elt: int) -> int:
+    """bytes of `rows` rows of `width` elements at a row stride of `ld`"""
+    return max(0, (rows - 1) * ld + width) * elt if rows > 0 else 0
+
+
+def _out_elt(out_dtype: int) -> int:
+    return 2 if out_dtype == OUT_BF16 else 4
 
 
 def _nbytes(t) -> int:
@@ -170,54 +196,62 @@ def w8a8_weight_init(segments, fmt: int) -> W8A8Weight:
     segs = (Fp8Segment * max(1, len(segments)))()
     keep = []
     for i, (w, s) in enumerate(segments):
-        segs[i] = Fp8Segment(_ptr(w), _ptr(s), w.shape[0], w.shape[1], fmt)
+        n, k = w.shape[0], w.shape[1]
+        s_bytes = (n if fmt == PER_ROW else -(-n // 128) * (k // 128)) * 4
+        segs[i] = Fp8Segment(_ptr(w, f"segment {i} codes", n * k), _ptr(s, f"segment {i} scales", s_bytes), n, k,
+                             fmt)
         keep += [w, s]
     desc = W8A8WeightDesc()
-    _check(load().qdl_w8a8_weight_init(ctypes.byref(desc), segs, len(segments)))
+    _check(_call("qdl_w8a8_weight_init", ctypes.byref(desc), segs, len(segments)))
     return W8A8Weight(desc, keep)
 
 
 def w8a8_plan(w: W8A8Weight, rows: int) -> dict:
     """Kernel and work split that qdl_w8a8_gemv would use for `rows` rows."""
     p = Plan()
-    _check(load().qdl_w8a8_plan(ctypes.byref(w.desc), rows, ctypes.byref(p)))
+    _check(_call("qdl_w8a8_plan", ctypes.byref(w.desc), rows, ctypes.byref(p)))
     return p.as_dict()
 
 
 def scratch_bytes(max_k: int):
     q = ctypes.c_size_t()
     s = ctypes.c_size_t()
-    _check(load().qdl_scratch_bytes(max_k, ctypes.byref(q), ctypes.byref(s)))
+    _check(_call("qdl_scratch_bytes", max_k, ctypes.byref(q), ctypes.byref(s)))
     return q.value, s.value
 
 
 def act_quant(fmt: int, x, rows: int, k: int, q, q_scale, ldx: int | None = None, stream=None):
     ldx = x.stride(0) if ldx is None else ldx
-    _check(load().qdl_act_quant(fmt, _ptr(x), ldx, rows, k, _ptr(q), _ptr(q_scale), _nbytes(q),
-                                _nbytes(q_scale), _stream(stream)))
+    _check(_call("qdl_act_quant", fmt, _ptr(x, "x", _rows_span(rows, ldx, k, 2)), ldx, rows, k, _ptr(q, "q"),
+                                _ptr(q_scale, "q_scale"), _nbytes(q), _nbytes(q_scale), _stream(stream)))
 
 
 def act_quant_silu(fmt: int, gate, up, rows: int, k: int, q, q_scale, ld_gate: int | None = None,
                    ld_up: int | None = None, stream=None):
     ld_gate = gate.stride(0) if ld_gate is None else ld_gate
     ld_up = up.stride(0) if ld_up is None else ld_up
-    _check(load().qdl_act_quant_silu(fmt, _ptr(gate), _ptr(up), ld_gate, ld_up, rows, k, _ptr(q),
-                                     _ptr(q_scale), _nbytes(q), _nbytes(q_scale), _stream(stream)))
+    _check(_call("qdl_act_quant_silu", fmt, _ptr(gate, "gate", _rows_span(rows, ld_gate, k, 2)),
+                                     _ptr(up, "up", _rows_span(rows, ld_up, k, 2)), ld_gate, ld_up, rows, k,
+                                     _ptr(q, "q"), _ptr(q_scale, "q_scale"), _nbytes(q), _nbytes(q_scale),
+                                     _stream(stream)))
 
 
 def w8a8_gemv(w: W8A8Weight, q, q_scale, rows: int, out, out_dtype: int = OUT_F32,
               ldc: int | None = None, stream=None):
     ldc = out.stride(0) if ldc is None else ldc
-    _check(load().qdl_w8a8_gemv(ctypes.byref(w.desc), _ptr(q), _ptr(q_scale), _nbytes(q),
-                                _nbytes(q_scale), rows, _ptr(out), out_dtype, ldc, _stream(stream)))
+    o = _ptr(out, "out", _rows_span(rows, ldc, w.n, _out_elt(out_dtype)))
+    _check(_call("qdl_w8a8_gemv", ctypes.byref(w.desc), _ptr(q, "q"), _ptr(q_scale, "q_scale"), _nbytes(q),
+                                _nbytes(q_scale), rows, o, out_dtype, ldc, _stream(stream)))
 
 
 def w8a8_proj(w: W8A8Weight, x, rows: int, out, q, q_scale, out_dtype: int = OUT_F32,
               ldx: int | None = None, ldc: int | None = None, stream=None):
     ldx = x.stride(0) if ldx is None else ldx
     ldc = out.stride(0) if ldc is None else ldc
-    _check(load().qdl_w8a8_proj(ctypes.byref(w.desc), _ptr(x), ldx, rows, _ptr(out), out_dtype, ldc,
-                                _ptr(q), _ptr(q_scale), _nbytes(q), _nbytes(q_scale), _stream(stream)))
+    xp = _ptr(x, "x", _rows_span(rows, ldx, w.k, 2))
+    o = _ptr(out, "out", _rows_span(rows, ldc, w.n, _out_elt(out_dtype)))
+    _check(_call("qdl_w8a8_proj", ctypes.byref(w.desc), xp, ldx, rows, o, out_dtype, ldc, _ptr(q, "q"),
+                                _ptr(q_scale, "q_scale"), _nbytes(q), _nbytes(q_scale), _stream(stream)))
 
 
 def w8a8_proj_silu(w: W8A8Weight, gate, up, rows: int, out, q, q_scale, out_dtype: int = OUT_F32,
@@ -226,9 +260,12 @@ def w8a8_proj_silu(w: W8A8Weight, gate, up, rows: int, out, q, q_scale, out_dtyp
     ld_gate = gate.stride(0) if ld_gate is None else ld_gate
     ld_up = up.stride(0) if ld_up is None else ld_up
     ldc = out.stride(0) if ldc is None else ldc
-    _check(load().qdl_w8a8_proj_silu(ctypes.byref(w.desc), _ptr(gate), _ptr(up), ld_gate, ld_up, rows,
-                                     _ptr(out), out_dtype, ldc, _ptr(q), _ptr(q_scale), _nbytes(q),
-                                     _nbytes(q_scale), _stream(stream)))
+    gp = _ptr(gate, "gate", _rows_span(rows, ld_gate, w.k, 2))
+    up_ = _ptr(up, "up", _rows_span(rows, ld_up, w.k, 2))
+    o = _ptr(out, "out", _rows_span(rows, ldc, w.n, _out_elt(out_dtype)))
+    _check(_call("qdl_w8a8_proj_silu", ctypes.byref(w.desc), gp, up_, ld_gate, ld_up, rows, o, out_dtype, ldc,
+                                     _ptr(q, "q"), _ptr(q_scale, "q_scale"), _nbytes(q), _nbytes(q_scale),
+                                     _stream(stream)))
 
 
 STATIC_SCRATCH_BYTES = 4 << 20
@@ -244,8 +281,10 @@ def w8a8_proj_static(w: W8A8Weight, x, rows: int, out, out_dtype: int = OUT_F32,
     each device before any stream capture (it looks up the array's address)."""
     ldx = x.stride(0) if ldx is None else ldx
     ldc = out.stride(0) if ldc is None else ldc
-    _check(load().qdl_w8a8_proj_static(ctypes.byref(w.desc), _ptr(x), ldx, rows, _ptr(out), out_dtype,
-                                       ldc, _stream(stream)))
+    xp = _ptr(x, "x", _rows_span(rows, ldx, w.k, 2))
+    o = _ptr(out, "out", _rows_span(rows, ldc, w.n, _out_elt(out_dtype)))
+    _check(_call("qdl_w8a8_proj_static", ctypes.byref(w.desc), xp, ldx, rows, o, out_dtype, ldc,
+                                       _stream(stream)))
 
 
 # ---------------------------------------------------------------- INT4
@@ -253,8 +292,15 @@ def w8a8_proj_static(w: W8A8Weight, x, rows: int, out, out_dtype: int = OUT_F32,
 
 def int4_qkv_gemv(x, m: int, k: int, nq: int, nkv: int, group: int, qw, sc, zr, out, stream=None):
     """qw/sc/zr/out: 3-sequences (q, k, v) of CUDA tensors or device pointers."""
-    arr = lambda xs: (ctypes.c_void_p * 3)(*[_ptr(t) for t in xs])
-    _check(load().qdl_int4_qkv_gemv(_ptr(x), m, k, nq, nkv, group, arr(qw), arr(sc), arr(zr), arr(out),
+    ns = (nq, nkv, nkv)
+    groups = k // group if group > 0 else 0
+
+    def arr(name, xs, nbytes):
+        return (ctypes.c_void_p * 3)(*[_ptr(t, f"{name}[{p}]", nbytes(ns[p])) for p, t in enumerate(xs)])
+
+    _check(_call("qdl_int4_qkv_gemv", _ptr(x, "x", 4 * m * k), m, k, nq, nkv, group,
+                                    arr("qw", qw, lambda n: k * (n // 8) * 4), arr("sc", sc, lambda n: groups * n * 4),
+                                    arr("zr", zr, lambda n: groups * n * 4), arr("out", out, lambda n: 4 * m * n),
                                     _stream(stream)))
 
 
@@ -264,32 +310,43 @@ IN_F32, IN_BF16 = 0, 1
 def fp8_weight_quant(fmt: int, w, w_dtype: int, ldw: int, n: int, k: int, codes, scales, stream=None):
     """FP8 weight [n, k] with per-row ([n]) or 128x128-block ([ceil(n/128), k/128])
     f32 scales, absmax / 448, from f32 or bf16 w [n, ldw]."""
-    _check(load().qdl_fp8_weight_quant(fmt, _ptr(w), w_dtype, ldw, n, k, _ptr(codes), _ptr(scales),
-                                       _stream(stream)))
+    s_bytes = (n if fmt == PER_ROW else -(-n // 128) * (k // 128)) * 4
+    _check(_call("qdl_fp8_weight_quant", fmt, _ptr(w, "w", _rows_span(n, ldw, k, 2 if w_dtype == IN_BF16 else 4)),
+                                       w_dtype, ldw, n, k, _ptr(codes, "codes", n * k),
+                                       _ptr(scales, "scales", s_bytes), _stream(stream)))
 
 
 def awq_pack(nib, k: int, n: int, qw, stream=None):
     """uint8 codes [k, n] -> uint32 [k, n/8] in the AWQ shift order."""
-    _check(load().qdl_awq_pack(_ptr(nib), k, n, _ptr(qw), _stream(stream)))
+    _check(_call("qdl_awq_pack", _ptr(nib, "nib", k * n), k, n, _ptr(qw, "qw", k * (n // 8) * 4), _stream(stream)))
 
 
 def kv_quant_int8(x, tokens: int, head_dim: int, q, scale, stream=None):
     """KV-cache per-token int8: x f32 [tokens, head_dim] -> q int8, scale f32 [tokens]."""
-    _check(load().qdl_kv_quant_int8(_ptr(x), tokens, head_dim, _ptr(q), _ptr(scale), _stream(stream)))
+    n = tokens * head_dim
+    _check(_call("qdl_kv_quant_int8", _ptr(x, "x", 4 * n), tokens, head_dim, _ptr(q, "q", n),
+                                    _ptr(scale, "scale", 4 * tokens), _stream(stream)))
 
 
 def kv_dequant_int8(q, scale, tokens: int, head_dim: int, out, stream=None):
-    _check(load().qdl_kv_dequant_int8(_ptr(q), _ptr(scale), tokens, head_dim, _ptr(out), _stream(stream)))
+    n = tokens * head_dim
+    _check(_call("qdl_kv_dequant_int8", _ptr(q, "q", n), _ptr(scale, "scale", 4 * tokens), tokens, head_dim,
+                                      _ptr(out, "out", 4 * n), _stream(stream)))
 
 
 def kv_quant_int4(x, tokens: int, head_dim: int, group: int, packed, scale, zero, stream=None):
     """KV-cache per-group INT4: packed uint8 [tokens*head_dim/2], scale/zero f32 [tokens*head_dim/group]."""
-    _check(load().qdl_kv_quant_int4(_ptr(x), tokens, head_dim, group, _ptr(packed), _ptr(scale), _ptr(zero),
-                                    _stream(stream)))
+    n = tokens * head_dim
+    g = n // group if group > 0 else 0
+    _check(_call("qdl_kv_quant_int4", _ptr(x, "x", 4 * n), tokens, head_dim, group, _ptr(packed, "packed", n // 2),
+                                    _ptr(scale, "scale", 4 * g), _ptr(zero, "zero", 4 * g), _stream(stream)))
 
 
 def kv_dequant_int4(packed, scale, zero, tokens: int, head_dim: int, group: int, out, stream=None):
-    _check(load().qdl_kv_dequant_int4(_ptr(packed), _ptr(scale), _ptr(zero), tokens, head_dim, group, _ptr(out),
+    n = tokens * head_dim
+    g = n // group if group > 0 else 0
+    _check(_call("qdl_kv_dequant_int4", _ptr(packed, "packed", n // 2), _ptr(scale, "scale", 4 * g),
+                                      _ptr(zero, "zero", 4 * g), tokens, head_dim, group, _ptr(out, "out", 4 * n),
                                       _stream(stream)))
 
 
@@ -297,9 +354,10 @@ def selftest_bounded_wait(w: W8A8Weight, q, q_scale, rows: int, out, limit_us: i
                           stream=None) -> int:
     """Run the GEMV with one pipeline stage withheld so that its bounded waits
     give up; returns the status (QDL_ERR_DEVICE_TIMEOUT = 5 when they did)."""
-    return load().qdl_selftest_bounded_wait(ctypes.byref(w.desc), _ptr(q), _ptr(q_scale), _nbytes(q),
-                                            _nbytes(q_scale), rows, _ptr(out), limit_us, _stream(stream))
+    o = _ptr(out, "out", _rows_span(rows, w.n, w.n, 4))
+    return _call("qdl_selftest_bounded_wait", ctypes.byref(w.desc), _ptr(q, "q"), _ptr(q_scale, "q_scale"), _nbytes(q),
+                                            _nbytes(q_scale), rows, o, limit_us, _stream(stream))
 
 
 def check_device_fault(stream=None):
-    _check(load().qdl_check_device_fault(_stream(stream)))
+    _check(_call("qdl_check_device_fault", _stream(stream)))

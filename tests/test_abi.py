@@ -410,3 +410,90 @@ def test_plan_rejects(lib):
         assert f"{rows} rows, want 1..=256" in lib.qdl_last_error().decode()
     assert lib.qdl_w8a8_plan(ctypes.byref(qdl.W8A8WeightDesc()), 8, ctypes.byref(plan)) == INVALID
     assert "qdl_w8a8_weight_init" in lib.qdl_last_error().decode()
+
+
+# ---------------------------------------------------------------- Python binding checks
+
+def _wobj(lib):
+    return qdl.W8A8Weight(_weight(lib), [])
+
+
+def test_binding_refuses_host_tensors(lib):
+    import torch
+    w = _wobj(lib)
+    x = torch.zeros((8, 4096), dtype=torch.bfloat16)
+    out = torch.zeros((8, 6144), dtype=torch.float32)
+    q = torch.zeros((8, 4096), dtype=torch.uint8)
+    s = torch.zeros((8, 32), dtype=torch.float32)
+    with pytest.raises(ValueError, match="x: expected a CUDA tensor"):
+        qdl.w8a8_proj(w, x, 8, out, q, s, stream=0)
+    with pytest.raises(ValueError, match="expected a CUDA tensor"):
+        qdl.kv_quant_int8(torch.zeros((4, 128)), 4, 128, torch.zeros((4, 128), dtype=torch.int8),
+                          torch.zeros(4), stream=0)
+
+
+@pytest.mark.parametrize("case", ["bf16_tensor_for_f32_out", "short_out", "short_x_rows", "int4_out", "kv_scale",
+                                  "weight_scales", "fp8_codes"])
+def test_binding_refuses_buffers_too_small_for_the_call(lib, case, monkeypatch):
+    """each buffer must hold every byte the call will touch from its first
+    element; these are refused in Python, before the library is called (host
+    tensors stand in for device ones here, and the library is never reached)"""
+    import torch
+    monkeypatch.setattr(torch.Tensor, "is_cuda", property(lambda self: True))
+    monkeypatch.setattr(qdl, "load", lambda path=None: pytest.fail("the library was called"))
+    w = _wobj(lib)
+    f32, bf16, u8 = torch.float32, torch.bfloat16, torch.uint8
+    x = torch.zeros((8, 4096), dtype=bf16)
+    q, s = torch.zeros((8, 4096), dtype=u8), torch.zeros((8, 32), dtype=f32)
+    with pytest.raises(ValueError, match="storage holds"):
+        if case == "bf16_tensor_for_f32_out":
+            qdl.w8a8_proj(w, x, 8, torch.zeros((8, 6144), dtype=bf16), q, s, stream=0)
+        elif case == "short_out":
+            qdl.w8a8_gemv(w, q, s, 8, torch.zeros((8, 6144), dtype=f32)[1:], stream=0)
+        elif case == "short_x_rows":
+            qdl.w8a8_proj(w, torch.zeros((4, 4096), dtype=bf16), 8, torch.zeros((8, 6144), dtype=f32), q, s,
+                          stream=0)
+        elif case == "int4_out":
+            outs = [torch.zeros((2, 128)), torch.zeros((2, 64)), torch.zeros((1, 64))]
+            qdl.int4_qkv_gemv(torch.zeros((2, 256)), 2, 256, 128, 64, 128,
+                              [torch.zeros((256, n // 8), dtype=torch.int32) for n in (128, 64, 64)],
+                              [torch.zeros((2, n)) for n in (128, 64, 64)],
+                              [torch.zeros((2, n)) for n in (128, 64, 64)], outs, stream=0)
+        elif case == "kv_scale":
+            qdl.kv_quant_int4(torch.zeros((4, 128)), 4, 128, 64, torch.zeros(256, dtype=u8), torch.zeros(7),
+                              torch.zeros(8), stream=0)
+        elif case == "weight_scales":
+            qdl.w8a8_weight_init([(torch.zeros((256, 256), dtype=u8), torch.zeros(3))], qdl.BLOCK128)
+        elif case == "fp8_codes":
+            qdl.fp8_weight_quant(qdl.PER_ROW, torch.zeros((4, 256)), qdl.IN_F32, 256, 4, 256,
+                                 torch.zeros((3, 256), dtype=u8), torch.zeros(4), stream=0)
+
+
+def test_binding_views_are_measured_from_their_first_element(lib, monkeypatch):
+    """a view in the middle of a larger buffer may use the storage after it,
+    and the up half of a [rows, 2K] gate/up buffer is exactly large enough"""
+    import torch
+    w = _wobj(lib)
+    buf = torch.zeros((8, 2 * 4096), dtype=torch.bfloat16)
+    q, s = torch.zeros((8, 4096), dtype=torch.uint8), torch.zeros((8, 32))
+    out = torch.zeros((8 * 6144 + 64,))[64:].view(8, 6144)
+    seen = []
+    monkeypatch.setattr(torch.Tensor, "is_cuda", property(lambda self: True))
+
+    class Lib:  # records the call instead of making it
+        def qdl_w8a8_proj_silu(self, *a):
+            seen.append(a)
+            return 0
+    monkeypatch.setattr(qdl, "load", lambda path=None: Lib())
+    qdl.w8a8_proj_silu(w, buf[:, :4096], buf[:, 4096:], 8, out, q, s, stream=0)
+    assert len(seen) == 1
+    # the up view starts K elements into the buffer; ld_gate = ld_up = 2K
+    assert seen[0][2] - seen[0][1] == 4096 * 2 and seen[0][3] == seen[0][4] == 8192
+    with pytest.raises(ValueError, match="up: the call touches"):
+        qdl.w8a8_proj_silu(w, buf[:, :4096], buf[:, 4097:], 8, out, q, s, ld_up=8192, stream=0)
+
+
+def test_binding_passes_raw_pointers_to_the_library_checks(lib):
+    w = _wobj(lib)
+    with pytest.raises(qdl.QdlError, match="rows"):
+        qdl.w8a8_proj_static(w, DEV, 0, DEV + 0x4000000, ldx=4096, ldc=6144, stream=0)
