@@ -223,7 +223,7 @@ def scratch_bytes(max_k: int):
 def act_quant(fmt: int, x, rows: int, k: int, q, q_scale, ldx: int | None = None, stream=None):
     ldx = x.stride(0) if ldx is None else ldx
     _check(_call("qdl_act_quant", fmt, _ptr(x, "x", _rows_span(rows, ldx, k, 2)), ldx, rows, k, _ptr(q, "q"),
-                                _ptr(q_scale, "q_scale"), _nbytes(q), _nbytes(q_scale), _stream(stream)))
+                 _ptr(q_scale, "q_scale"), _nbytes(q), _nbytes(q_scale), _stream(stream)))
 
 
 def act_quant_silu(fmt: int, gate, up, rows: int, k: int, q, q_scale, ld_gate: int | None = None,
@@ -231,9 +231,9 @@ def act_quant_silu(fmt: int, gate, up, rows: int, k: int, q, q_scale, ld_gate: i
     ld_gate = gate.stride(0) if ld_gate is None else ld_gate
     ld_up = up.stride(0) if ld_up is None else ld_up
     _check(_call("qdl_act_quant_silu", fmt, _ptr(gate, "gate", _rows_span(rows, ld_gate, k, 2)),
-                                     _ptr(up, "up", _rows_span(rows, ld_up, k, 2)), ld_gate, ld_up, rows, k,
-                                     _ptr(q, "q"), _ptr(q_scale, "q_scale"), _nbytes(q), _nbytes(q_scale),
-                                     _stream(stream)))
+                 _ptr(up, "up", _rows_span(rows, ld_up, k, 2)), ld_gate, ld_up, rows, k,
+                 _ptr(q, "q"), _ptr(q_scale, "q_scale"), _nbytes(q), _nbytes(q_scale),
+                 _stream(stream)))
 
 
 def w8a8_gemv(w: W8A8Weight, q, q_scale, rows: int, out, out_dtype: int = OUT_F32,
@@ -241,7 +241,7 @@ def w8a8_gemv(w: W8A8Weight, q, q_scale, rows: int, out, out_dtype: int = OUT_F3
     ldc = out.stride(0) if ldc is None else ldc
     o = _ptr(out, "out", _rows_span(rows, ldc, w.n, _out_elt(out_dtype)))
     _check(_call("qdl_w8a8_gemv", ctypes.byref(w.desc), _ptr(q, "q"), _ptr(q_scale, "q_scale"), _nbytes(q),
-                                _nbytes(q_scale), rows, o, out_dtype, ldc, _stream(stream)))
+                 _nbytes(q_scale), rows, o, out_dtype, ldc, _stream(stream)))
 
 
 def w8a8_proj(w: W8A8Weight, x, rows: int, out, q, q_scale, out_dtype: int = OUT_F32,
@@ -251,7 +251,7 @@ def w8a8_proj(w: W8A8Weight, x, rows: int, out, q, q_scale, out_dtype: int = OUT
     xp = _ptr(x, "x", _rows_span(rows, ldx, w.k, 2))
     o = _ptr(out, "out", _rows_span(rows, ldc, w.n, _out_elt(out_dtype)))
     _check(_call("qdl_w8a8_proj", ctypes.byref(w.desc), xp, ldx, rows, o, out_dtype, ldc, _ptr(q, "q"),
-                                _ptr(q_scale, "q_scale"), _nbytes(q), _nbytes(q_scale), _stream(stream)))
+                 _ptr(q_scale, "q_scale"), _nbytes(q), _nbytes(q_scale), _stream(stream)))
 
 
 def w8a8_proj_silu(w: W8A8Weight, gate, up, rows: int, out, q, q_scale, out_dtype: int = OUT_F32,
@@ -264,8 +264,8 @@ def w8a8_proj_silu(w: W8A8Weight, gate, up, rows: int, out, q, q_scale, out_dtyp
     up_ = _ptr(up, "up", _rows_span(rows, ld_up, w.k, 2))
     o = _ptr(out, "out", _rows_span(rows, ldc, w.n, _out_elt(out_dtype)))
     _check(_call("qdl_w8a8_proj_silu", ctypes.byref(w.desc), gp, up_, ld_gate, ld_up, rows, o, out_dtype, ldc,
-                                     _ptr(q, "q"), _ptr(q_scale, "q_scale"), _nbytes(q), _nbytes(q_scale),
-                                     _stream(stream)))
+                 _ptr(q, "q"), _ptr(q_scale, "q_scale"), _nbytes(q), _nbytes(q_scale),
+                 _stream(stream)))
 
 
 STATIC_SCRATCH_BYTES = 4 << 20
@@ -284,7 +284,7 @@ def w8a8_proj_static(w: W8A8Weight, x, rows: int, out, out_dtype: int = OUT_F32,
     xp = _ptr(x, "x", _rows_span(rows, ldx, w.k, 2))
     o = _ptr(out, "out", _rows_span(rows, ldc, w.n, _out_elt(out_dtype)))
     _check(_call("qdl_w8a8_proj_static", ctypes.byref(w.desc), xp, ldx, rows, o, out_dtype, ldc,
-                                       _stream(stream)))
+                 _stream(stream)))
 
 
 # ---------------------------------------------------------------- INT4
@@ -299,9 +299,9 @@ def int4_qkv_gemv(x, m: int, k: int, nq: int, nkv: int, group: int, qw, sc, zr, 
         return (ctypes.c_void_p * 3)(*[_ptr(t, f"{name}[{p}]", nbytes(ns[p])) for p, t in enumerate(xs)])
 
     _check(_call("qdl_int4_qkv_gemv", _ptr(x, "x", 4 * m * k), m, k, nq, nkv, group,
-                                    arr("qw", qw, lambda n: k * (n // 8) * 4), arr("sc", sc, lambda n: groups * n * 4),
-                                    arr("zr", zr, lambda n: groups * n * 4), arr("out", out, lambda n: 4 * m * n),
-                                    _stream(stream)))
+                 arr("qw", qw, lambda n: k * (n // 8) * 4), arr("sc", sc, lambda n: groups * n * 4),
+                 arr("zr", zr, lambda n: groups * n * 4), arr("out", out, lambda n: 4 * m * n),
+                 _stream(stream)))
 
 
 IN_F32, IN_BF16 = 0, 1
@@ -312,8 +312,8 @@ def fp8_weight_quant(fmt: int, w, w_dtype: int, ldw: int, n: int, k: int, codes,
     f32 scales, absmax / 448, from f32 or bf16 w [n, ldw]."""
     s_bytes = (n if fmt == PER_ROW else -(-n // 128) * (k // 128)) * 4
     _check(_call("qdl_fp8_weight_quant", fmt, _ptr(w, "w", _rows_span(n, ldw, k, 2 if w_dtype == IN_BF16 else 4)),
-                                       w_dtype, ldw, n, k, _ptr(codes, "codes", n * k),
-                                       _ptr(scales, "scales", s_bytes), _stream(stream)))
+                 w_dtype, ldw, n, k, _ptr(codes, "codes", n * k),
+                 _ptr(scales, "scales", s_bytes), _stream(stream)))
 
 
 def awq_pack(nib, k: int, n: int, qw, stream=None):
@@ -325,13 +325,13 @@ def kv_quant_int8(x, tokens: int, head_dim: int, q, scale, stream=None):
     """KV-cache per-token int8: x f32 [tokens, head_dim] -> q int8, scale f32 [tokens]."""
     n = tokens * head_dim
     _check(_call("qdl_kv_quant_int8", _ptr(x, "x", 4 * n), tokens, head_dim, _ptr(q, "q", n),
-                                    _ptr(scale, "scale", 4 * tokens), _stream(stream)))
+                 _ptr(scale, "scale", 4 * tokens), _stream(stream)))
 
 
 def kv_dequant_int8(q, scale, tokens: int, head_dim: int, out, stream=None):
     n = tokens * head_dim
     _check(_call("qdl_kv_dequant_int8", _ptr(q, "q", n), _ptr(scale, "scale", 4 * tokens), tokens, head_dim,
-                                      _ptr(out, "out", 4 * n), _stream(stream)))
+                 _ptr(out, "out", 4 * n), _stream(stream)))
 
 
 def kv_quant_int4(x, tokens: int, head_dim: int, group: int, packed, scale, zero, stream=None):
@@ -339,15 +339,15 @@ def kv_quant_int4(x, tokens: int, head_dim: int, group: int, packed, scale, zero
     n = tokens * head_dim
     g = n // group if group > 0 else 0
     _check(_call("qdl_kv_quant_int4", _ptr(x, "x", 4 * n), tokens, head_dim, group, _ptr(packed, "packed", n // 2),
-                                    _ptr(scale, "scale", 4 * g), _ptr(zero, "zero", 4 * g), _stream(stream)))
+                 _ptr(scale, "scale", 4 * g), _ptr(zero, "zero", 4 * g), _stream(stream)))
 
 
 def kv_dequant_int4(packed, scale, zero, tokens: int, head_dim: int, group: int, out, stream=None):
     n = tokens * head_dim
     g = n // group if group > 0 else 0
     _check(_call("qdl_kv_dequant_int4", _ptr(packed, "packed", n // 2), _ptr(scale, "scale", 4 * g),
-                                      _ptr(zero, "zero", 4 * g), tokens, head_dim, group, _ptr(out, "out", 4 * n),
-                                      _stream(stream)))
+                 _ptr(zero, "zero", 4 * g), tokens, head_dim, group, _ptr(out, "out", 4 * n),
+                 _stream(stream)))
 
 
 def selftest_bounded_wait(w: W8A8Weight, q, q_scale, rows: int, out, limit_us: int = 20000,
@@ -356,7 +356,7 @@ def selftest_bounded_wait(w: W8A8Weight, q, q_scale, rows: int, out, limit_us: i
     give up; returns the status (QDL_ERR_DEVICE_TIMEOUT = 5 when they did)."""
     o = _ptr(out, "out", _rows_span(rows, w.n, w.n, 4))
     return _call("qdl_selftest_bounded_wait", ctypes.byref(w.desc), _ptr(q, "q"), _ptr(q_scale, "q_scale"), _nbytes(q),
-                                            _nbytes(q_scale), rows, o, limit_us, _stream(stream))
+                 _nbytes(q_scale), rows, o, limit_us, _stream(stream))
 
 
 def check_device_fault(stream=None):
