@@ -44,9 +44,10 @@ def test_struct_layout_matches_c(tmp_path):
 #include <stddef.h>
 #include "{HEADER}"
 int main(void) {{
-  printf("%zu %zu %zu %zu %zu\\n", sizeof(qdl_fp8_segment), sizeof(qdl_w8a8_weight),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(qdl_fp8_segment), sizeof(qdl_w8a8_weight),
          offsetof(qdl_w8a8_weight, count), offsetof(qdl_w8a8_weight, n1),
-         offsetof(qdl_w8a8_weight, magic));
+         offsetof(qdl_w8a8_weight, magic), sizeof(qdl_plan), offsetof(qdl_plan, resident_clusters),
+         offsetof(qdl_plan, proj_streamk));
   return 0;
 }}
 ''')
@@ -54,8 +55,9 @@ int main(void) {{
     subprocess.run(["gcc", str(prog), "-o", str(exe)], check=True)
     got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
     W = qdl.W8A8WeightDesc
+    P = qdl.Plan
     want = [ctypes.sizeof(qdl.Fp8Segment), ctypes.sizeof(W), W.count.offset, W.n1.offset,
-            W.magic.offset]
+            W.magic.offset, ctypes.sizeof(P), P.resident_clusters.offset, P.proj_streamk.offset]
     assert got == want
 
 
@@ -497,3 +499,40 @@ def test_binding_passes_raw_pointers_to_the_library_checks(lib):
     w = _wobj(lib)
     with pytest.raises(qdl.QdlError, match="rows"):
         qdl.w8a8_proj_static(w, DEV, 0, DEV + 0x4000000, ldx=4096, ldc=6144, stream=0)
+
+
+def test_c_program_links_and_gets_validation_errors(lib, tmp_path):
+    """the boundary used from C, without Python: a program that includes
+    qdl.h, links libqdl.so and makes calls that are refused on the host"""
+    prog = tmp_path / "use.c"
+    prog.write_text(f'''#include <stdio.h>
+#include <string.h>
+#include "{HEADER}"
+int main(void) {{
+  size_t qb = 0, sb = 0;
+  if (qdl_scratch_bytes(4096, &qb, &sb) != QDL_OK || qb != 256u * 4096 || sb != 256u * 32 * 4) return 1;
+  qdl_fp8_segment seg[3];
+  memset(seg, 0, sizeof seg);
+  const unsigned long long dev = 0x7F0000000000ull;
+  unsigned n[3] = {{4096, 1024, 1024}};
+  for (int i = 0; i < 3; ++i) {{
+    seg[i].weight = (const void *)(dev + 0x100000ull * i);
+    seg[i].scale = (const float *)(dev + 0x8000000ull + 0x1000ull * i);
+    seg[i].n = n[i];
+    seg[i].k = 4096;
+    seg[i].format = QDL_SCALE_BLOCK128;
+  }}
+  qdl_w8a8_weight w;
+  if (qdl_w8a8_weight_init(&w, seg, 3) != QDL_OK || w.n != 6144) return 2;
+  qdl_status st = qdl_w8a8_proj(&w, (const void *)dev, 4096, 0, (void *)(dev + 0x4000000ull), QDL_OUT_F32, 6144,
+                                (unsigned char *)(dev + 0x1000000ull), (float *)(dev + 0x2000000ull), qb, sb, 0);
+  printf("%d %s | %s\\n", (int)st, qdl_status_string(st), qdl_last_error());
+  return st == QDL_ERR_INVALID_ARG ? 0 : 3;
+}}
+''')
+    exe = tmp_path / "use"
+    libdir = os.path.dirname(qdl.LIB_PATH)
+    subprocess.run(["gcc", str(prog), "-o", str(exe), f"-L{libdir}", "-lqdl", f"-Wl,-rpath,{libdir}"], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.startswith("1 QDL_ERR_INVALID_ARG | ") and "0 rows" in r.stdout, r.stdout
