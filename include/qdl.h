@@ -168,7 +168,8 @@ QDL_API qdl_status qdl_w8a8_gemv(const qdl_w8a8_weight *w, const uint8_t *q, con
  * (QDL_OUT_F32_ADD): the order of the split-K additions varies, so results
  * may differ in the last bits from run to run (always within the GEMV's
  * error bound).  bf16 output takes the fixed-order reduction.  out_dtype is
- * QDL_OUT_F32 or QDL_OUT_BF16. */
+ * QDL_OUT_F32 or QDL_OUT_BF16.  Checks: those of qdl_w8a8_gemv, plus the
+ * quantiser's K <= QDL_MAX_K and the x checks of qdl_act_quant. */
 QDL_API qdl_status qdl_w8a8_proj(const qdl_w8a8_weight *w, const void *x, uint32_t ldx, uint32_t rows,
                          void *out, int32_t out_dtype, uint32_t ldc, uint8_t *q, float *q_scale,
                          size_t q_bytes, size_t scale_bytes, void *stream);
@@ -307,14 +308,15 @@ QDL_API qdl_status qdl_awq_pack(const uint8_t *nib, uint32_t k, uint32_t n, uint
  * larger calls return QDL_ERR_UNSUPPORTED (256 rows fit up to K = 15872).
  *   The first call on a device, made with that device current, looks up the
  * array's device address (cudaGetSymbolAddress); make that first call before
- * any stream capture.  The call never uses cudaMalloc, cudaFree or any
- * allocating routine.
+ * any stream capture.  The address is kept for the life of the process, so
+ * the library must not be used on a device after cudaDeviceReset there.
+ * The call never uses cudaMalloc, cudaFree or any allocating routine.
  *   All calls share the one array and it keeps the last call's contents:
  * calls that can overlap on the GPU (different streams, or several host
  * threads) race on it and must be serialised by the caller.  Each call
  * overwrites every byte it later reads, so no clearing is needed.
  * Arguments and checks are those of qdl_w8a8_proj for w, x, ldx, rows, out,
- * out_dtype and ldc. */
+ * out_dtype and ldc (rows at most 256, K <= QDL_MAX_K). */
 QDL_API qdl_status qdl_w8a8_proj_static(const qdl_w8a8_weight *w, const void *x, uint32_t ldx,
                                         uint32_t rows, void *out, int32_t out_dtype, uint32_t ldc,
                                         void *stream);

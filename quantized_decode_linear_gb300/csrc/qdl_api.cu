@@ -81,6 +81,13 @@ qdl_status check_input(const char *who, const char *name, const void *p, uint32_
     return QDL_OK;
 }
 
+// The projections quantise their activations: K is bounded by what the
+// quantiser covers, as for qdl_act_quant.
+qdl_status check_quant_k(const char *who, uint32_t k) {
+    if (k > QDL_MAX_K) return fail(QDL_ERR_INVALID_ARG, "%s: K=%u (want K %% 128 == 0, 0 < K <= %d)", who, k, QDL_MAX_K);
+    return QDL_OK;
+}
+
 qdl_status check_weight(const char *who, const qdl_w8a8_weight *w) {
     if (w == nullptr || w->magic != kWeightMagic)
         return fail(QDL_ERR_INVALID_ARG, "%s: weight descriptor is NULL or was not made by qdl_w8a8_weight_init", who);
@@ -364,6 +371,7 @@ qdl_status qdl_w8a8_proj(const qdl_w8a8_weight *w, const void *x, uint32_t ldx, 
     const char *who = "w8a8_proj";
     qdl_status st = check_gemv(who, w, q, q_scale, q_bytes, scale_bytes, rows, out, out_dtype, ldc, false, QDL_MAX_PROJ_ROWS);
     if (st != QDL_OK) return st;
+    if ((st = check_quant_k(who, w->k)) != QDL_OK) return st;
     if ((st = check_input(who, "x", x, ldx, w->k)) != QDL_OK) return st;
     return proj_passes(who, w, x, nullptr, ldx, 0, false, rows, out, out_dtype, ldc, q, q_scale, stream);
 }
@@ -374,6 +382,7 @@ qdl_status qdl_w8a8_proj_silu(const qdl_w8a8_weight *w, const void *gate, const 
     const char *who = "w8a8_proj_silu";
     qdl_status st = check_gemv(who, w, q, q_scale, q_bytes, scale_bytes, rows, out, out_dtype, ldc, false, QDL_MAX_PROJ_ROWS);
     if (st != QDL_OK) return st;
+    if ((st = check_quant_k(who, w->k)) != QDL_OK) return st;
     if ((st = check_input(who, "gate", gate, ld_gate, w->k)) != QDL_OK) return st;
     if ((st = check_input(who, "up", up, ld_up, w->k)) != QDL_OK) return st;
     return proj_passes(who, w, gate, up, ld_gate, ld_up, true, rows, out, out_dtype, ldc, q, q_scale, stream);
@@ -606,6 +615,7 @@ qdl_status qdl_w8a8_proj_static(const qdl_w8a8_weight *w, const void *x, uint32_
     qdl_status st = check_weight(who, w);
     if (st != QDL_OK) return st;
     if (rows < 1 || rows > (uint32_t)kMaxRows) return fail(QDL_ERR_INVALID_ARG, "%s: %u rows, want 1..=%d", who, rows, kMaxRows);
+    if ((st = check_quant_k(who, w->k)) != QDL_OK) return st;
     const size_t q_bytes = (size_t)rows * w->k;
     const size_t scale_off = (q_bytes + 255) / 256 * 256;
     const size_t scale_bytes = (size_t)rows * scales_per_row(w->format, w->k) * 4;

@@ -221,6 +221,24 @@ def test_proj_checks_input(lib):
     assert st == INVALID and "x stride=4095" in lib.qdl_last_error().decode()
 
 
+def test_projections_refuse_k_beyond_the_quantiser(lib):
+    """the projections quantise their activations, so a weight whose K exceeds
+    QDL_MAX_K (what the quantiser covers) is refused by every projection entry
+    point before any device work, as qdl_act_quant refuses it"""
+    k = 65536 + 128
+    st, d, _ = _init(lib, [(16, k)])
+    assert st == 0
+    big = 1 << 30
+    st = lib.qdl_w8a8_proj(ctypes.byref(d), DEV, k, 1, DEV + 0x4000000, 0, 16,
+                           DEV + 0x1000000, DEV + 0x2000000, big, big, None)
+    assert st == INVALID and "K=65664" in lib.qdl_last_error().decode()
+    st = lib.qdl_w8a8_proj_silu(ctypes.byref(d), DEV, DEV, k, k, 1, DEV + 0x4000000, 0, 16,
+                                DEV + 0x1000000, DEV + 0x2000000, big, big, None)
+    assert st == INVALID and "K=65664" in lib.qdl_last_error().decode()
+    st = lib.qdl_w8a8_proj_static(ctypes.byref(d), DEV, k, 1, DEV + 0x4000000, 0, 16, None)
+    assert st == INVALID and "K=65664" in lib.qdl_last_error().decode()
+
+
 def test_accumulating_output_is_gemv_only(lib):
     """QDL_OUT_F32_ADD (out += y) is accepted by qdl_w8a8_gemv's checks but
     not by the projections, which pick accumulation themselves"""

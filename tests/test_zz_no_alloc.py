@@ -3,11 +3,16 @@
 Some callers cannot allocate device memory -- a plugin that its host
 framework hands only input and output buffers, or a decode loop that may not
 risk cudaMalloc's implicit synchronisation or an allocation failure.  For them
-the library keeps its activation scratch in a built-in device array.  These
-tests check, through the C ABI, that this entry point gives the same outputs
-as qdl_w8a8_proj with caller scratch, on two calls in a row (the second with
-different shapes, so a stale array from the first call would show), and that
-oversize calls are refused before any device work.
+the library keeps its activation scratch in a built-in device array.
+
+These tests call that entry point through the C ABI twice in a row, first a
+large call and then a smaller one of the other scale format, and check each
+output element against the oracle within the GEMV tolerance
+(2e-3 * sum_k |x_hat w_hat|, plus bf16 rounding for bf16 output).  The codes
+the static array holds are checked indirectly but exactly: the output must
+equal, bit for bit, the deterministic qdl_w8a8_gemv run on the oracle's own
+codes and scales, which holds only if the array held exactly those codes and
+scales.  Oversize calls must be refused before any device work.
 
 This file is collected last so that a failure here never hides another test.
 """
@@ -15,43 +20,57 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import quantized_decode_linear_gb300 as qdl
 from quantized_decode_linear_gb300 import synthetic as syn
-from _gpu import TOL, bf16_dev, host, scratch, upload_weight
+from _gpu import BF16_REL, bf16_dev, check_close, dev, f32_bits_equal, host, upload_weight
+
+# (format, rows, k, ldx, segment sizes, out dtype, seed).  The first call
+# writes more of the shared array than the second, which uses the other
+# scale layout, so a second call reading anything it did not write itself
+# (a wrong offset, a stale scale) would read the first call's bytes.
+CALLS = [
+    (qdl.PER_ROW, 40, 4096, 4096 + 64, (1024, 96), qdl.OUT_F32, 2),
+    (qdl.BLOCK128, 16, 1024, 1024, (512, 256, 200), qdl.OUT_BF16, 1),
+]
 
 
-def _case(fmt, rows, k, sizes, seed):
+def _static_call(fmt, rows, k, ldx, sizes, out_dtype, seed):
     segs = [syn.fp8_weight(n, k, fmt, 0.02, seed + i) for i, n in enumerate(sizes)]
-    x = syn.bf16_normal((rows, k), seed=seed + 50)
-    return segs, x
-
-
-def _both(fmt, rows, k, sizes, seed):
-    segs, xb = _case(fmt, rows, k, sizes, seed)
-    w, _keep = upload_weight(segs, fmt)
-    x = bf16_dev(xb)
-    ref = torch.empty((rows, w.n), device="cuda")
-    q, s = scratch(rows, k, fmt)
-    qdl.w8a8_proj(w, x, rows, ref, q, s)
-    out = torch.full((rows, w.n), float("nan"), device="cuda")
-    qdl.w8a8_proj_static(w, x, rows, out)
+    xb = syn.bf16_normal((rows, ldx), seed=seed + 50)
+    w, keep = upload_weight(segs, fmt)
+    tdt = torch.bfloat16 if out_dtype == qdl.OUT_BF16 else torch.float32
+    out = torch.full((rows, w.n), float("nan"), device="cuda", dtype=tdt)
+    qdl.w8a8_proj_static(w, bf16_dev(xb), rows, out, out_dtype=out_dtype, ldx=ldx)
     torch.cuda.synchronize()
-    return host(out), host(ref)
+    return segs, xb, w, keep, host(out.float())
+
+
+def _check(call, segs, xb, w, out):
+    fmt, rows, k, ldx, sizes, out_dtype, seed = call
+    qo, so = oracle.act_quant(fmt, xb, k)
+    yo, bo = oracle.w8a8_gemv(fmt, qo, so, segs)
+    bf16 = out_dtype == qdl.OUT_BF16
+    assert np.all(np.isfinite(out))
+    check_close(out, yo, bo, extra_rel=BF16_REL if bf16 else 0.0, what=f"static fmt={fmt} rows={rows}")
+    # the same GEMV on the oracle's codes and scales (fixed-order reduction,
+    # so reproducible bit for bit) must give exactly the same output
+    tdt = torch.bfloat16 if bf16 else torch.float32
+    ref = torch.full((rows, w.n), float("nan"), device="cuda", dtype=tdt)
+    qdl.w8a8_gemv(w, dev(qo), dev(so if fmt == qdl.BLOCK128 else so[:, None]), rows, ref, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert f32_bits_equal(out, host(ref.float())), f"static fmt={fmt}: output differs from the GEMV on the oracle codes"
 
 
 @pytest.mark.gpu
-def test_static_scratch_matches_caller_scratch_twice():
-    # first call: Block128, 3 segments, 16 rows; second: PerRow, more rows and a
-    # longer K, so it overwrites more of the shared array than the first did
-    calls = [(qdl.BLOCK128, 16, 1024, (512, 256, 200), 1),
-             (qdl.PER_ROW, 40, 4096, (1024, 96), 2)]
-    for fmt, rows, k, sizes, seed in calls:
-        out, ref = _both(fmt, rows, k, sizes, seed)
-        scale = np.abs(ref).max() + 1e-30
-        assert np.all(np.isfinite(out))
-        # both paths run the same kernels on the same codes; allow the parity
-        # tolerance anyway
-        assert np.max(np.abs(out - ref)) <= TOL * scale
+def test_static_scratch_against_the_oracle_twice():
+    results = [(c, _static_call(*c)) for c in CALLS]  # two calls in a row, no host check between
+    for call, (segs, xb, w, _keep, out) in results:
+        _check(call, segs, xb, w, out)
+    # and once more in the other order, each checked straight after its call
+    for call in reversed(CALLS):
+        segs, xb, w, _keep, out = _static_call(*call)
+        _check(call, segs, xb, w, out)
 
 
 @pytest.mark.gpu
