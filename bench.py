@@ -124,15 +124,25 @@ def _src_hash(names):
 class W8A8Case:
     """Device buffers for one W8A8 workload at `rows` token rows."""
 
-    def __init__(self, wl, rows, torch, qdl, syn, l2_bytes):
-        self.wl, self.rows = wl, rows
+    @staticmethod
+    def device_weights(wl, torch, qdl, syn, l2_bytes):
+        """the workload's weight, uploaded once, in enough copies that the
+        copies together are at least 4x the L2 cache; shared by every row
+        count of a sweep"""
         segs = syn.w8a8_weights(wl)
-        self.weight_bytes = sum(c.nbytes + s.nbytes for c, s in segs)
-        self.copies = max(1, math.ceil(4 * l2_bytes / self.weight_bytes))
+        weight_bytes = sum(c.nbytes + s.nbytes for c, s in segs)
+        copies = max(1, math.ceil(4 * l2_bytes / weight_bytes))
         base = [(torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda()) for c, s in segs]
-        self.weights = [qdl.w8a8_weight_init(base, wl.fmt)]
-        for _ in range(self.copies - 1):
-            self.weights.append(qdl.w8a8_weight_init([(c.clone(), s.clone()) for c, s in base], wl.fmt))
+        weights = [qdl.w8a8_weight_init(base, wl.fmt)]
+        for _ in range(copies - 1):
+            weights.append(qdl.w8a8_weight_init([(c.clone(), s.clone()) for c, s in base], wl.fmt))
+        return {"segs": segs, "weights": weights, "weight_bytes": weight_bytes, "copies": copies}
+
+    def __init__(self, wl, rows, torch, qdl, syn, l2_bytes, shared=None):
+        self.wl, self.rows = wl, rows
+        shared = shared or self.device_weights(wl, torch, qdl, syn, l2_bytes)
+        segs = shared["segs"]
+        self.weight_bytes, self.copies, self.weights = shared["weight_bytes"], shared["copies"], shared["weights"]
         xb = syn.w8a8_activations(wl, rows)
         self.x_host = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
         self.x = self.x_host.cuda()
@@ -196,14 +206,20 @@ class W8A8Case:
 
 
 class Int4Case:
-    def __init__(self, wl, rows, torch, qdl, syn, l2_bytes):
-        self.wl, self.rows = wl, rows
+    @staticmethod
+    def device_weights(wl, torch, qdl, syn, l2_bytes):
         ws = syn.int4_weights(wl)
-        self.weight_bytes = sum(a.nbytes for w in ws for a in w)
-        self.copies = max(1, math.ceil(4 * l2_bytes / self.weight_bytes))
+        weight_bytes = sum(a.nbytes for w in ws for a in w)
+        copies = max(1, math.ceil(4 * l2_bytes / weight_bytes))
         base = [[torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else a).cuda() for a in w]
                 for w in ws]
-        self.sets = [base] + [[[a.clone() for a in w] for w in base] for _ in range(self.copies - 1)]
+        sets = [base] + [[[a.clone() for a in w] for w in base] for _ in range(copies - 1)]
+        return {"sets": sets, "weight_bytes": weight_bytes, "copies": copies}
+
+    def __init__(self, wl, rows, torch, qdl, syn, l2_bytes, shared=None):
+        self.wl, self.rows = wl, rows
+        shared = shared or self.device_weights(wl, torch, qdl, syn, l2_bytes)
+        self.weight_bytes, self.copies, self.sets = shared["weight_bytes"], shared["copies"], shared["sets"]
         x = syn.int4_activations(wl, rows)
         self.x_host = torch.from_numpy(x).pin_memory()
         self.x = self.x_host.cuda()
@@ -255,7 +271,11 @@ class KvCase:
     dequantises another (long untouched) block; blocks rotate over enough
     copies that every step streams from HBM."""
 
-    def __init__(self, wl, rows, torch, qdl, syn, l2_bytes):
+    @staticmethod
+    def device_weights(wl, torch, qdl, syn, l2_bytes):
+        return None
+
+    def __init__(self, wl, rows, torch, qdl, syn, l2_bytes, shared=None):
         self.wl, self.rows, self.qdl = wl, rows, qdl
         n = rows * wl.head_dim
         self.n = n
@@ -335,7 +355,11 @@ class PrepCase:
     (fp8) or packs 4-bit codes into AWQ words (awq); buffers rotate over
     enough copies that every step streams from HBM."""
 
-    def __init__(self, wl, rows, torch, qdl, syn, l2_bytes):
+    @staticmethod
+    def device_weights(wl, torch, qdl, syn, l2_bytes):
+        return None
+
+    def __init__(self, wl, rows, torch, qdl, syn, l2_bytes, shared=None):
         self.wl, self.rows, self.qdl = wl, rows, qdl
         self.fp8 = wl.prep == "fp8"
         if self.fp8:
@@ -410,19 +434,71 @@ def _graph(torch, fn, start, count):
     return g
 
 
-def _time_graphs(torch, fn, total, chunk=250):
-    """capture `fn` over `total` consecutive step indices into graphs of
-    `chunk` calls each (kept alive by the returned list)"""
-    graphs = []
-    for start in range(0, total, chunk):
-        graphs.append(_graph(torch, fn, start, chunk))
-    return graphs
+class GraphBlock:
+    """`fn(i)` for `steps` consecutive step indices, captured into CUDA
+    graphs: up to four distinct graphs of `chunk` calls replayed in turn, plus
+    one remainder graph.  `replay()` issues all `steps` calls."""
+
+    def __init__(self, torch, fn, steps, chunk):
+        c = min(chunk, steps)
+        self.full, rem = divmod(steps, c)
+        self.main = [_graph(torch, fn, j * c, c) for j in range(min(self.full, 4))]
+        self.tail = _graph(torch, fn, self.full * c, rem) if rem else None
+        self.steps = steps
+
+    def replay(self):
+        for r in range(self.full):
+            self.main[r % len(self.main)].replay()
+        if self.tail is not None:
+            self.tail.replay()
+
+
+def block_steps(k_steps):
+    """steps per captured block: a whole number of K-step sequences, at least
+    250 calls so that graph launches are rare against the work"""
+    return k_steps * max(1, math.ceil(250 / k_steps))
+
+
+def time_region(torch, stream, group, fn, k_steps, region_s, repeats, name):
+    """Median device time per step of `fn` over `repeats` timed regions.  Each
+    region replays a captured block of whole K-step sequences until at least
+    `region_s` seconds have been timed (exactly K steps, once, when
+    region_s <= 0), bracketed by a barrier and synchronisations, with CUDA
+    events on the launching stream; the slowest rank's time counts."""
+    unit = k_steps if region_s <= 0 else block_steps(k_steps)
+    blk = GraphBlock(torch, fn, unit, unit if unit <= 1000 else 250)
+    blk.replay()  # the first replay uploads the graphs
+    torch.cuda.synchronize()
+    blocks = 1
+    if region_s > 0:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        blk.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        blocks = max(1, math.ceil(region_s / max(e0.elapsed_time(e1) / 1e3, 1e-9)))
+    per_step = []
+    for _ in range(max(1, repeats)):
+        group.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _nvtx_push(torch, name)
+        e0.record(stream)
+        for _ in range(blocks):
+            blk.replay()
+        e1.record(stream)
+        _nvtx_pop(torch)
+        torch.cuda.synchronize()
+        per_step.append(group.max(e0.elapsed_time(e1) / 1e3) / (blocks * unit))
+    del blk
+    return {"s_per_step": statistics.median(per_step), "min": min(per_step), "max": max(per_step),
+            "steps_per_region": blocks * unit, "repeats": len(per_step)}
 
 
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,utilization.gpu")
 
     def __init__(self, gpu_index):
         self.proc = None
@@ -445,22 +521,34 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons = [], None, set()
+        return self.parse(out)
+
+    @staticmethod
+    def parse(out):
+        """median SM clock and throttle reasons from nvidia-smi CSV rows;
+        samples with the GPU under 50% busy are gaps between timed regions
+        (graph capture, host work) and count only in `samples`"""
+        sm, loaded, mx, power, reasons = [], [], None, [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             f = [v.strip() for v in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                mhz, mx, w, util = float(f[1]), float(f[2]), float(f[3]), float(f[9])
             except ValueError:
                 continue
+            sm.append(mhz)
+            power.append(w)
+            if util >= 50.0:
+                loaded.append(mhz)
             for nm, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        use = loaded or sm
+        return {"sm_mhz": statistics.median(use) if use else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm), "samples_under_load": len(loaded),
+                "power_w_max": max(power) if power else None}
 
 
 # ---------------------------------------------------------------- oracle timing
@@ -562,56 +650,135 @@ def _time_oracle(wl, rows, syn, budget_s):
             "sample": desc, "seconds": dt}
 
 
-def _cpu_baseline(wl, rows, syn, budget_s=12.0, single_budget_s=4.0):
-    """the oracle on all host cores, plus a shorter single-threaded sample"""
-    import oracle
-    line = _time_oracle(wl, rows, syn, budget_s)
-    cores = oracle.num_threads()
-    oracle.set_num_threads(1)
-    try:
-        one = _time_oracle(wl, rows, syn, single_budget_s)
-    finally:
-        oracle.set_num_threads(cores)
-    line["single_thread"] = {k: one[k] for k in ("value", "cores", "sample", "seconds")}
-    return line
-
-
 # ---------------------------------------------------------------- arms
 
+# The metric is quoted on the gate/up M sweep; these other workloads are
+# timed more briefly in the same run and reported under "extra".
+EXTRA = [("w8a8_block128_qkv_m8_k4096_n4096+1024+1024", 8),
+         ("w8a8_perrow_m1_k1024_n1024", 1),
+         ("w8a8_perrow_silu_down_m64_k14336_n4096", 64),
+         ("int4_awq_qkv_k4096_nq4096_nkv1024_g128", 1),
+         ("int4_awq_qkv_k4096_nq4096_nkv1024_g128", 4),
+         ("int4_awq_qkv_k4096_nq4096_nkv1024_g128", 16)]
+
+
+def _rows_list(args, wl):
+    return [args.rows] if args.rows else list(wl.rows)
+
+
+def _core_config(wl, rows_list, world):
+    """the workload's shape keys, the same in both arms' JSON lines"""
+    c = {"workload": wl.name, "rows": rows_list if len(rows_list) > 1 else rows_list[0]}
+    if hasattr(wl, "fmt"):
+        c.update(k=wl.k, n_segments=list(wl.segments), scale_format="per_row" if wl.fmt == 0 else "block128",
+                 silu_fused=wl.silu, out_dtype="f32")
+    elif hasattr(wl, "nq"):
+        c.update(k=wl.k, nq=wl.nq, nkv=wl.nkv, group=wl.group)
+    c["parallelism"] = "replicas" if world > 1 else "single"
+    if len(rows_list) > 1:
+        c["step"] = f"one decode call at each of the {len(rows_list)} row counts"
+    return c
+
+
 def run_reference(args, rank, world, budget_s=120.0):
-    """times the oracle on rank 0 alone; `budget_s` sizes each step so the
-    whole warm-up + timed run takes about that long"""
+    """times the oracle on rank 0 alone; one step is the oracle on a bounded
+    sample of every row count of the workload, sized so the whole warm-up +
+    timed run takes about `budget_s`"""
     if rank != 0:
         return
     from quantized_decode_linear_gb300 import synthetic as syn
     import oracle
     wl = syn.WORKLOADS[args.workload]
-    rows = args.rows or wl.rows[0]
-    fn, b, desc = _oracle_step_fn(wl, rows, syn, 1.0 / 512)
-    t0 = time.perf_counter()
-    fn()
-    t_probe = max(time.perf_counter() - t0, 1e-4)
-    per_step = budget_s / max(1, args.steps + args.warmup)
-    frac = min(1.0, max(1.0 / 4096, (1.0 / 512) * per_step / t_probe))
-    fn, b, desc = _oracle_step_fn(wl, rows, syn, frac)
-    for _ in range(args.warmup):
+    rows_list = _rows_list(args, wl)
+    per_rows = budget_s / max(1, args.steps + args.warmup) / len(rows_list)
+    fns = []
+    for rows in rows_list:
+        fn, b, desc = _oracle_step_fn(wl, rows, syn, 1.0 / 512)
+        t0 = time.perf_counter()
         fn()
+        t_probe = max(time.perf_counter() - t0, 1e-4)
+        frac = min(1.0, max(1.0 / 4096, (1.0 / 512) * per_rows / t_probe))
+        fns.append((rows,) + _oracle_step_fn(wl, rows, syn, frac))
+    for _ in range(args.warmup):
+        for _, fn, _, _ in fns:
+            fn()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        fn()
+        for _, fn, _, _ in fns:
+            fn()
     dt = time.perf_counter() - t0
-    value = b * args.steps / dt / 1e9
+    step_bytes = sum(b for _, _, b, _ in fns)
+    value = step_bytes * args.steps / dt / 1e9
+    desc = "; ".join(f"rows={r}: {d}" for r, _, _, d in fns)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32" if hasattr(wl, "head_dim") else "f64",
             "data": "synthetic",
-            "config": {"workload": wl.name, "rows": rows,
-                       "parallelism": "replicas" if world > 1 else "single"},
+            "config": _core_config(wl, rows_list, world),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def _case_class(wl):
+    return (PrepCase if hasattr(wl, "prep") else W8A8Case if hasattr(wl, "fmt") else
+            KvCase if hasattr(wl, "head_dim") else Int4Case)
+
+
+def _measure_case(torch, stream, group, case, args, world, regions):
+    """times one workload at one row count: the decode steps, the dominant
+    kernel alone, the steps end to end with host copies, and warm L2"""
+    K, W = args.steps, args.warmup
+    for i in range(W):  # untimed warm-up steps (eager calls; also loads every kernel)
+        case.step(i)
+    torch.cuda.synchronize()
+    r_steps, r_dom, r_e2e, r_warm = regions
+    t = {"steps": time_region(torch, stream, group, case.step, K, r_steps[0], r_steps[1], "qdl timed steps"),
+         "dominant": time_region(torch, stream, group, case.dominant, K, r_dom[0], r_dom[1],
+                                 "qdl dominant kernel")}
+    if r_e2e[1] > 0:
+        t["e2e"] = time_region(torch, stream, group, case.e2e_step, K, r_e2e[0], r_e2e[1], "qdl end-to-end steps")
+    if r_warm[1] > 0:
+        t["warm"] = time_region(torch, stream, group, lambda i: case.step(0), K, r_warm[0], r_warm[1],
+                                "qdl warm L2")
+    return t
+
+
+def _fp8_peak_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return 2.0 * float(json.load(f)["bf16_tflops"]), "measured bf16 burst x 2 (nominal fp8/bf16 ratio)"
+    except Exception:
+        return 2.0 * 1900.0, "fallback bf16 x 2"
+
+
+def _summary(case, t, peak, world):
+    """per-row-count figures of one measured case"""
+    s = t["steps"]["s_per_step"]
+    d = t["dominant"]["s_per_step"] / case.gemv_launches
+    key = f"{case.wl.name}@{case.rows}"
+    tr = TRAFFIC.get(key)
+    traffic = tr["bytes"] if tr and tr.get("src") == _src_hash(case.kernel_src) else None
+    r = {"rows": case.rows, "us_per_call": s * 1e6, "gbs": case.step_bytes / s / 1e9 * world,
+         "hbm_frac_step": case.step_bytes / s / 1e9 / peak,
+         "us_spread": [t["steps"]["min"] * 1e6, t["steps"]["max"] * 1e6],
+         "steps_timed": t["steps"]["steps_per_region"] * t["steps"]["repeats"],
+         "kernel": case.kernel, "kernel_us": d * 1e6,
+         "kernel_gbs": case.gemv_bytes / case.gemv_launches / d / 1e9,
+         "kernel_frac": case.gemv_bytes / case.gemv_launches / d / 1e9 / peak,
+         "traffic": traffic, "launches_per_step": case.launches_per_step}
+    if isinstance(case, W8A8Case):
+        flops = 2.0 * case.rows * case.wl.n * case.wl.k
+        fp8_peak, _ = _fp8_peak_tflops()
+        r["kernel_tflops"] = flops / case.gemv_launches / d / 1e12
+        r["kernel_fp8_frac"] = r["kernel_tflops"] / fp8_peak
+    if "e2e" in t:
+        r["e2e_us_per_call"] = t["e2e"]["s_per_step"] * 1e6
+    if "warm" in t:
+        r["warm_l2_us_per_call"] = t["warm"]["s_per_step"] * 1e6
+    return r
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -625,156 +792,147 @@ def run_gpu(args, rank, world, local_rank):
     group = Replicas(world)
     props = torch.cuda.get_device_properties(local_rank)
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 2**20
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = _peaks()
+    rs = args.region_s
+    main_regions = ((rs, args.repeats), (rs / 2, args.repeats), (rs / 2, 3), (rs / 4, 3))
+    if rs <= 0:
+        main_regions = ((0, 1), (0, 1), (0, 1), (0, 1))
 
     wl = syn.WORKLOADS[args.workload]
-    rows = args.rows or wl.rows[0]
-    Case = (PrepCase if hasattr(wl, "prep") else W8A8Case if hasattr(wl, "fmt") else
-            KvCase if hasattr(wl, "head_dim") else Int4Case)
-    case = Case(wl, rows, torch, qdl, syn, l2)
-
-    # graphs covering exactly K steps: up to four distinct graphs of c calls
-    # replayed in turn, plus one remainder graph
-    K, W = args.steps, args.warmup
-    c = min(250, K)
-    full, rem = divmod(K, c)
-
-    def graphs_for(fn):
-        main = [_graph(torch, fn, j * c, c) for j in range(min(full, 4))]
-        tail = _graph(torch, fn, full * c, rem) if rem else None
-        return main, tail
-
-    def replay(gs):
-        main, tail = gs
-        for r in range(full):
-            main[r % len(main)].replay()
-        if tail is not None:
-            tail.replay()
-
-    for i in range(W):  # untimed warm-up steps (eager calls; also loads every kernel)
-        case.step(i)
-    torch.cuda.synchronize()
-    timed = graphs_for(case.step)
-    dom = graphs_for(case.dominant)
-    for gs in (timed, dom):  # first replay uploads the graph
-        for g in gs[0] + ([gs[1]] if gs[1] is not None else []):
-            g.replay()
-    torch.cuda.synchronize()
-    steps, warm = K, W
+    Case = _case_class(wl)
+    rows_list = _rows_list(args, wl)
+    shared = Case.device_weights(wl, torch, qdl, syn, l2)
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
-    group.barrier()
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    _nvtx_push(torch, "qdl timed steps")
-    e0.record(stream)
-    replay(timed)
-    e1.record(stream)
-    _nvtx_pop(torch)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    # dominant kernel alone, same graphs-of-launches method
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    _nvtx_push(torch, "qdl dominant kernel")
-    d0.record(stream)
-    replay(dom)
-    d1.record(stream)
-    _nvtx_pop(torch)
-    torch.cuda.synchronize()
-    dom_ms = d0.elapsed_time(d1)
+    sweep, cases = [], []
+    for rows in rows_list:
+        case = Case(wl, rows, torch, qdl, syn, l2, shared)
+        t = _measure_case(torch, stream, group, case, args, world, main_regions)
+        sweep.append(_summary(case, t, peak, world))
+        h2d, d2h = case.e2e_bytes()
+        cases.append((case.step_bytes, case.gemv_bytes, case.gemv_launches, case.launches_per_step, h2d, d2h,
+                      t, case.describe(), case.kernel, getattr(case, "dtype", "e4m3")))
+        del case
+    extra = {}
+    if args.extra:
+        ex_regions = ((rs * 0.3, 3), (rs * 0.3, 3), (rs * 0.2, 1), (0.0, 0)) if rs > 0 else \
+            ((0, 1), (0, 1), (0, 0), (0, 0))
+        for name, rows in EXTRA:
+            ewl = syn.WORKLOADS[name]
+            EC = _case_class(ewl)
+            ec = EC(ewl, rows, torch, qdl, syn, l2)
+            et = _measure_case(torch, stream, group, ec, args, world, ex_regions)
+            extra[f"{name}@{rows}"] = _summary(ec, et, peak, world)
+            del ec
+            torch.cuda.empty_cache()
     clk = clocks.stop()
-    ms = group.max(ms)
 
-    # end to end through the public API with host buffers: every step copies
-    # its inputs from pinned host memory, makes the library call and copies
-    # the result back; replayed from graphs like the device-only steps, and
-    # also timed eagerly (one Python call per step) for reference
-    e2e_graphs = graphs_for(case.e2e_step)
-    for g in e2e_graphs[0] + ([e2e_graphs[1]] if e2e_graphs[1] is not None else []):
-        g.replay()
-    group.barrier()
-    torch.cuda.synchronize()
-    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    _nvtx_push(torch, "qdl end-to-end steps")
-    x0.record(stream)
-    replay(e2e_graphs)
-    x1.record(stream)
-    _nvtx_pop(torch)
-    torch.cuda.synchronize()
-    e2e_s = x0.elapsed_time(x1) / 1e3
-    e2e_s = group.max(e2e_s)
-    eager_steps = min(steps, 2000)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for i in range(eager_steps):
-        case.e2e_step(i)
-    torch.cuda.synchronize()
-    eager_s = time.perf_counter() - t0
-    h2d, d2h = case.e2e_bytes()
-
-    # warm L2, labelled as such and not the headline: every call reuses the
-    # first weight copy, so a workload that fits in L2 reads it from there
-    warm_graphs = graphs_for(lambda i: case.step(0))
-    for g in warm_graphs[0] + ([warm_graphs[1]] if warm_graphs[1] is not None else []):
-        g.replay()
-    group.barrier()
-    torch.cuda.synchronize()
-    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    w0.record(stream)
-    replay(warm_graphs)
-    w1.record(stream)
-    torch.cuda.synchronize()
-    warm_s = group.max(w0.elapsed_time(w1) / 1e3)
-
-    peak, peak_kind = _peaks()
-    value = aggregate_gbs(case.step_bytes, steps, world, ms / 1e3)
-    dom_launch_s = dom_ms / 1e3 / (steps * case.gemv_launches)
-    achieved = case.gemv_bytes / case.gemv_launches / dom_launch_s / 1e9
-    key = f"{wl.name}@{rows}"
-    tr = TRAFFIC.get(key)
-    traffic = tr["bytes"] if tr and tr.get("src") == _src_hash(case.kernel_src) else None
+    # one step = one decode call at every row count of the sweep
+    step_s = sum(c[6]["steps"]["s_per_step"] for c in cases)
+    step_bytes = sum(c[0] for c in cases)
+    dom_s = sum(c[6]["dominant"]["s_per_step"] for c in cases)
+    dom_bytes = sum(c[1] for c in cases)
+    dom_launches = sum(c[2] for c in cases)
+    traffic = [r["traffic"] for r in sweep]
+    value = aggregate_gbs(step_bytes, 1, world, step_s)
+    sw = len(rows_list) > 1
+    cfg = _core_config(wl, rows_list, world)
+    for key in ("weight_copies", "copies", "l2"):
+        if key in cases[0][7]:
+            cfg[key] = cases[0][7][key]
+    cfg["timing"] = (f"median over {main_regions[0][1]} regions of >= {main_regions[0][0]:.2f} s, each "
+                     f"whole {args.steps}-step sequences replayed from CUDA graphs" if rs > 0 else
+                     f"{args.steps} steps, one region")
+    kernels = sorted({r["kernel"] for r in sweep})
     line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
-        "warmup": warm, "ms_per_step": ms / steps, "us_per_call": ms / steps * 1e3,
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "us_per_call": step_s * 1e6 / len(rows_list),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3" if Case is W8A8Case else getattr(case, "dtype", "f16"), "data": "synthetic",
-        "config": dict(case.describe(), parallelism="replicas" if world > 1 else "single"),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": case.kernel,
-                     "peak_source": f"{peak_kind} hbm_gbs", "kernel_us": dom_launch_s * 1e6},
+        "dtype": cases[0][9], "data": "synthetic",
+        "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": dom_bytes / dom_s / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": dom_bytes / dom_s / 1e9 / peak,
+                     "traffic": (sum(traffic) / dom_launches if all(v is not None for v in traffic)
+                                 else None),
+                     "kernel": " + ".join(kernels), "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel_us": dom_s / dom_launches * 1e6,
+                     "algorithmic_bytes_per_launch": dom_bytes / dom_launches,
+                     "note": ("per launch, averaged over the sweep: the dominant launches' algorithmic bytes "
+                              "and event times summed over the row counts" if sw else "per launch")},
         "hbm_frac_step": value / world / peak,
-        "e2e": {"value": aggregate_gbs(case.step_bytes, steps, world, e2e_s), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "us_per_call": e2e_s / steps * 1e6, "method": "graphs of copy-in, call, copy-out",
-                "eager_us_per_call": eager_s / eager_steps * 1e6},
-        "warm_l2": {"value": aggregate_gbs(case.step_bytes, steps, world, warm_s), "unit": "GB/s",
-                    "us_per_call": warm_s / steps * 1e6,
-                    "method": "same steps, one weight copy reused by every call (L2-resident when it fits)"},
-        "gpu_launches": steps * case.launches_per_step,
+        "sweep": sweep,
+        "gpu_launches": sum(c[3] * c[6]["steps"]["steps_per_region"] * c[6]["steps"]["repeats"] for c in cases),
+        "gpu_launches_note": "library kernels in all timed step regions",
         "clocks": clk,
     }
+    if all("e2e" in c[6] for c in cases):
+        e2e_s = sum(c[6]["e2e"]["s_per_step"] for c in cases)
+        line["e2e"] = {"value": aggregate_gbs(step_bytes, 1, world, e2e_s), "unit": "GB/s",
+                       "h2d_bytes_per_step": sum(c[4] for c in cases),
+                       "d2h_bytes_per_step": sum(c[5] for c in cases),
+                       "us_per_step": e2e_s * 1e6,
+                       "method": "graphs of copy-in from pinned host memory, call, copy-out"}
+    if all("warm" in c[6] for c in cases):
+        warm_s = sum(c[6]["warm"]["s_per_step"] for c in cases)
+        line["warm_l2"] = {"value": aggregate_gbs(step_bytes, 1, world, warm_s), "unit": "GB/s",
+                           "us_per_step": warm_s * 1e6,
+                           "method": "same steps, one weight copy reused by every call (L2-resident when it fits)"}
+    fp8_peak, fp8_src = _fp8_peak_tflops()
+    line["fp8_peak_tflops"] = {"value": fp8_peak, "source": fp8_src}
+    if extra:
+        line["extra"] = extra
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = _cpu_baseline(wl, rows, syn)
+        line["cpu_baseline"] = _cpu_baseline_rows(wl, rows_list, syn)
     if rank == 0:
         print(json.dumps(line), flush=True)
     group.close()
 
 
+def _cpu_baseline_rows(wl, rows_list, syn, budget_s=12.0, single_budget_s=4.0):
+    """the oracle on all host cores over a sample of every row count (the
+    budget split evenly), plus a shorter single-threaded sample of the first"""
+    import oracle
+    parts = [_time_oracle(wl, r, syn, budget_s / len(rows_list)) for r in rows_list]
+    secs = sum(p["seconds"] for p in parts)
+    gb = sum(p["value"] * p["seconds"] for p in parts)
+    line = {"value": gb / secs, "unit": "GB/s", "cores": parts[0]["cores"], "kind": "oracle",
+            "sample": "; ".join(f"rows={r}: {p['sample']}" for r, p in zip(rows_list, parts)), "seconds": secs}
+    cores = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        one = _time_oracle(wl, rows_list[0], syn, single_budget_s)
+    finally:
+        oracle.set_num_threads(cores)
+    line["single_thread"] = {k: one[k] for k in ("value", "cores", "sample", "seconds")}
+    line["single_thread"]["rows"] = rows_list[0]
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="qdl", choices=["qdl", "reference"])
-    ap.add_argument("--workload", default=None)
+    ap.add_argument("--workload", default=None,
+                    help="one workload (all its row counts unless --rows); default: the gate/up sweep "
+                         "plus the other workloads under 'extra'")
     ap.add_argument("--rows", type=int, default=None)
+    ap.add_argument("--region-s", type=float, default=1.0,
+                    help="seconds per timed region of the decode steps (the dominant kernel and e2e take half); "
+                         "0: time exactly --steps steps once")
+    ap.add_argument("--repeats", type=int, default=5, help="timed regions per measurement (median reported)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.steps < 1 or args.warmup < 3:
         ap.error("need --steps >= 1 and --warmup >= 3")
+    if args.repeats < 1:
+        ap.error("need --repeats >= 1")
     from quantized_decode_linear_gb300 import synthetic as syn
+    args.extra = args.workload is None and args.rows is None
     args.workload = args.workload or syn.HEADLINE
     if args.workload not in syn.WORKLOADS:
         ap.error(f"unknown workload; choose from {sorted(syn.WORKLOADS)}")

@@ -182,7 +182,7 @@ WORKLOADS = {
     "awq_pack_k4096_n6144": WeightPrepWorkload("awq_pack_k4096_n6144", "awq", 6144, 4096),
 }
 
-HEADLINE = "w8a8_block128_qkv_m8_k4096_n4096+1024+1024"
+HEADLINE = "w8a8_block128_gateup_k8192_n14336+14336"
 
 
 def w8a8_weights(wl: W8A8Workload):

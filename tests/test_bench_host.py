@@ -40,10 +40,39 @@ def test_traffic_records_are_current_and_near_the_algorithmic_bytes():
         assert alg <= rec["bytes"] <= 1.01 * alg, (key, rec["bytes"], alg)
 
 
-def test_headline_algorithmic_bytes():
+def test_qkv_algorithmic_bytes():
     # 25,165,824 weight codes + 6,144 scales + 32,768 codes + 1,024 act scales + 196,608 output
-    wl = syn.WORKLOADS[syn.HEADLINE]
+    wl = syn.WORKLOADS["w8a8_block128_qkv_m8_k4096_n4096+1024+1024"]
     assert _algorithmic_bytes(wl, 8) == 25_402_368
+
+
+def test_headline_is_the_gate_up_sweep():
+    """the metric is quoted on the largest workload: gate/up, K = 8192,
+    N = 14336 + 14336, every row bucket from 1 to 256"""
+    wl = syn.WORKLOADS[syn.HEADLINE]
+    assert (wl.k, wl.segments, wl.fmt) == (8192, (14336, 14336), syn.BLOCK128)
+    assert wl.rows == (1, 2, 4, 8, 16, 32, 64, 128, 256)
+    # weights 234,881,024 + scales 2 * 112 * 64 * 4 = 57,344; one row adds
+    # 8192 codes + 64 act scales * 4 + 28672 * 4 output bytes
+    assert _algorithmic_bytes(wl, 1) == 234_881_024 + 57_344 + 8192 + 256 + 114_688
+
+
+def test_block_steps_are_whole_k_step_sequences():
+    for k in (1, 3, 20, 249, 250, 251, 1000, 100000):
+        b = bench.block_steps(k)
+        assert b % k == 0 and b >= min(250, k) and b >= k
+    assert bench.block_steps(20) == 260 and bench.block_steps(100000) == 100000
+
+
+def test_clock_parse_uses_loaded_samples():
+    rows = ["0, 2070, 2070, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active, 0",
+            "0, 1900, 2070, 900.5, 0x4, Not Active, Not Active, Not Active, Active, 100",
+            "0, 2000, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active, 97",
+            "garbage"]
+    c = bench.ClockSampler.parse("\n".join(rows))
+    assert c["samples"] == 3 and c["samples_under_load"] == 2
+    assert c["sm_mhz"] == 1950.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"] and c["power_w_max"] == 950.0
 
 
 def test_aggregate_throughput_counts_every_rank():

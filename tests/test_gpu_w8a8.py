@@ -5,6 +5,8 @@ Outputs must be within 2e-3 * sum_k |x_hat w_hat| of the oracle's double
 result; activation codes are bit-exact (test_gpu_act_quant.py), so both sides
 see the same x_hat.  Small shapes compare every output; full-size workloads
 compare a sample of outputs the oracle computes one by one."""
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -267,3 +269,44 @@ def test_proj_silu_beyond_256_rows_bf16():
     o = host(out.float())[:, :w.n]
     check_close(o, yo, bo, extra_rel=BF16_REL, what="silu rows=300 bf16")
     assert torch.isnan(out[:, w.n:].float()).all()
+
+
+@functools.lru_cache(maxsize=1)
+def _gateup_segments():
+    return syn.w8a8_weights(syn.WORKLOADS["w8a8_block128_gateup_k8192_n14336+14336"])
+
+
+def _every_tile_samples(rows, n, seed):
+    """one output column per 128-wide output tile for every token row (a
+    random column inside the tile, the tile's last column for the ragged
+    end), so that every (token row, tile) pair is compared"""
+    rng = np.random.default_rng(seed)
+    tiles = (n + 127) // 128
+    r = np.repeat(np.arange(rows, dtype=np.int32), tiles)
+    t = np.tile(np.arange(tiles, dtype=np.int64), rows)
+    c = np.minimum(t * 128 + rng.integers(0, 128, t.size), n - 1).astype(np.int32)
+    return r, c
+
+
+@pytest.mark.parametrize("rows", [32, 64, 128, 256])
+def test_full_gateup_every_tile_every_row(rows):
+    """the gate/up workload at the row counts whose GEMV splits tiles between
+    CTAs (stream-K ranges at 17-128 rows, cluster split-K at 256): every token
+    row of every 128-row output tile is compared with the oracle, so a tile
+    whose shared partial sums went wrong cannot be missed"""
+    wl = syn.WORKLOADS["w8a8_block128_gateup_k8192_n14336+14336"]
+    segs = _gateup_segments()
+    w, _keep = upload_weight(segs, wl.fmt)
+    xb = syn.w8a8_activations(wl, rows)
+    q, s = scratch(rows, wl.k, wl.fmt)
+    out = torch.empty((rows, wl.n), device="cuda")
+    qdl.w8a8_proj(w, bf16_dev(xb), rows, out, q, s)
+    torch.cuda.synchronize()
+    qo, so = oracle.act_quant(wl.fmt, xb, wl.k)
+    assert np.array_equal(host(q), qo)
+    r, c = _every_tile_samples(rows, wl.n, seed=rows)
+    assert len(np.unique(c // 128)) == (wl.n + 127) // 128
+    ys, bs = oracle.w8a8_gemv_sampled(wl.fmt, qo, so, segs, r, c)
+    o = host(out)
+    check_close(o[r, c], ys, bs, what=f"gate/up rows={rows}, every tile")
+    assert np.all(np.isfinite(o))
