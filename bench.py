@@ -37,9 +37,10 @@ FALLBACK_HBM_GBS = 6800.0
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and rows;
 # valid only while the kernel source hash matches.  Source: profiles/.
 TRAFFIC = {
-    "w8a8_block128_qkv_m8_k4096_n4096+1024+1024@8": {"bytes": 25441536 + 0, "src": "667d260eb6dfb6f7"},
-    "int4_awq_qkv_k4096_nq4096_nkv1024_g128@1": {"bytes": 14220800 + 0, "src": "1918a975bcd9095e"},
-    "int4_awq_qkv_k4096_nq4096_nkv1024_g128@4": {"bytes": 14359296 + 0, "src": "1918a975bcd9095e"},
+    "int4_awq_qkv_k4096_nq4096_nkv1024_g128@1": {"bytes": 14220800 + 0, "file": "int4_qkv_cc.cu",
+                                                 "src": "1918a975bcd9095e"},
+    "int4_awq_qkv_k4096_nq4096_nkv1024_g128@4": {"bytes": 14359296 + 0, "file": "int4_qkv_cc.cu",
+                                                 "src": "1918a975bcd9095e"},
 }
 
 
@@ -760,7 +761,8 @@ def _summary(case, t, peak, world):
     d = t["dominant"]["s_per_step"] / case.gemv_launches
     key = f"{case.wl.name}@{case.rows}"
     tr = TRAFFIC.get(key)
-    traffic = tr["bytes"] if tr and tr.get("src") == _src_hash(case.kernel_src) else None
+    traffic = tr["bytes"] if tr and [tr.get("file")] == case.kernel_src and \
+        tr.get("src") == _src_hash(case.kernel_src) else None
     r = {"rows": case.rows, "us_per_call": s * 1e6, "gbs": case.step_bytes / s / 1e9 * world,
          "hbm_frac_step": case.step_bytes / s / 1e9 / peak,
          "us_spread": [t["steps"]["min"] * 1e6, t["steps"]["max"] * 1e6],

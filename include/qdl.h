@@ -11,6 +11,14 @@
  *   W4A16  AWQ INT4 fused Q/K/V projection with per-group scales and zeros.
  *          Defined by fused_int4_qkv.rs (boostr, quant::wgpu::shaders).
  *
+ * Weights are read-only inputs: the decode entry points start streaming
+ * weight codes (and AWQ codes, scales and zeros) as soon as they launch,
+ * before they wait for the kernel ahead of them on the stream, so weights
+ * must be written by work that has finished by then -- anything that does
+ * not release its dependents early, such as qdl_fp8_weight_quant,
+ * qdl_awq_pack, a copy or an ordinary kernel.  Activations, scratch and
+ * outputs are touched only after that wait.
+ *
  * Conventions for every entry point:
  *   - All tensor arguments are device pointers owned by the caller; the
  *     library never allocates, frees or retains them.  Layouts are row-major

@@ -120,6 +120,7 @@ qdl_status launch_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *
     a.debug_skip_iter = debug_skip_iter;
     a.wait_limit_ns = wait_limit_ns;
     a.accumulate = out_dtype == QDL_OUT_F32_ADD || (accumulate && out_dtype == QDL_OUT_F32);
+    a.out_zeroed = accumulate && out_dtype == QDL_OUT_F32;
     // Token rows up to QDL_MMA_MAX_ROWS go to the mma.sync streaming kernel;
     // all others take one pass of the tcgen05 kernel (rows <= 256).
     if (rows > kMmaMaxRows) {

@@ -72,7 +72,8 @@ struct W8A8Args {
     uint32_t kb;        // k / 128
     uint32_t debug_skip_iter;  // self-test only: pipeline stage never loaded (else ~0u)
     uint64_t wait_limit_ns;    // limit of every device-side wait
-    uint32_t accumulate;       // f32 output is zero: split-K ranks add their partials atomically
+    uint32_t accumulate;       // f32 output: out += y, split-K ranks add their partials atomically
+    uint32_t out_zeroed;       // with accumulate: out was set to zero by the quantiser (a plain store suffices)
     uint32_t early_trigger;    // set by the launcher: release dependent kernels at the start
     // fused projection only: bf16 input [m, ldx] and the scratch it fills
     const void *x;
@@ -114,7 +115,8 @@ cudaError_t launch_w8a8_gemm_tc(const W8A8Args &a, int format, const uint8_t *co
 cudaError_t read_and_clear_tc_fault(uint32_t *value);
 uint32_t tc_bucket(uint32_t m);  // MMA N of the tensor-core kernel for m token rows
 // true when the accumulating Block128 GEMV for these rows runs stream-K
-// (one range of (tile, K block) units per CTA; it needs a zeroed f32 output)
+// (one range of (tile, K block) units per CTA; the projection zeroes its f32
+// output for it)
 bool w8a8_streamk_applies(int format, uint32_t rows);
 // true when every split-K rank's K blocks fit the fused variant's ring (rows <= 16)
 bool w8a8_fused_fits(uint32_t n, uint32_t kb);

@@ -52,7 +52,7 @@
 #include <mutex>
 #include <vector>
 
-#include "tma_pipe.cuh"
+#include "tc_ptx.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -186,60 +186,7 @@ struct Tc {
     static_assert(kInFlight % 16 == 0 && kCpt % kInFlight == 0, "epilogue load groups");
 };
 
-// ---------------------------------------------------------------- tcgen05 / PDL PTX
-
-// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle
-// layout (8-row x 128-byte atoms stacked at 1024-byte stride).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
-    d |= (uint64_t)1 << 16;                    // leading byte offset (unused with this swizzle)
-    d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset: next 8-row atom
-    d |= (uint64_t)1 << 46;                    // descriptor version
-    d |= (uint64_t)2 << 61;                    // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor, kind::f8f6f4: D f32, A and B e4m3, both K-major.
-template <int NTOK>
-__device__ __forceinline__ constexpr uint32_t idesc_f8() {
-    return (1u << 4) | ((uint32_t)(NTOK >> 3) << 17) | ((uint32_t)(kTileRows >> 4) << 24);
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        "setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
-        "}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// ---------------------------------------------------------------- kernel helpers
 
 __device__ __forceinline__ void sts64(uint32_t addr, uint32_t lo, uint32_t hi) {
     asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(lo), "r"(hi) : "memory");
@@ -473,7 +420,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f8<NTOK>();
+            constexpr uint32_t idesc = idesc_f8<kTileRows, NTOK>();
             const uint32_t sbase = smem_u32(smem);
             for (uint32_t it = 0; it < niter; ++it) {
                 const uint32_t slot = it % C::kStages, ph = (it / C::kStages) & 1;
@@ -844,7 +791,7 @@ __global__ void __launch_bounds__(Tc<NTOK, true, false>::kThreads, 1) __maxnreg_
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f8<NTOK>();
+            constexpr uint32_t idesc = idesc_f8<kTileRows, NTOK>();
             const uint32_t sbase = smem_u32(smem);
             for (uint32_t it = 0; it < niter; ++it) {
                 const uint32_t slot = it % C::kStages, ph = (it / C::kStages) & 1;
@@ -942,10 +889,14 @@ __global__ void __launch_bounds__(Tc<NTOK, true, false>::kThreads, 1) __maxnreg_
                 if (row < a.n && !*abort_flag) {
                     float *orow = reinterpret_cast<float *>(a.out) + row + (size_t)(cgrp * kCpt) * a.ldc;
                     const uint32_t nt = a.m > (uint32_t)(cgrp * kCpt) ? a.m - cgrp * kCpt : 0u;  // valid tokens here
-                    if (whole) {
+                    if (whole && a.out_zeroed) {  // the only writer of this tile; out holds zeros
 #pragma unroll
                         for (int j = 0; j < kCpt; ++j)
                             if ((uint32_t)j < nt) orow[(size_t)j * a.ldc] = total[j];
+                    } else if (whole) {  // the only writer: out += y
+#pragma unroll
+                        for (int j = 0; j < kCpt; ++j)
+                            if ((uint32_t)j < nt) orow[(size_t)j * a.ldc] += total[j];
                     } else {
 #pragma unroll
                         for (int j = 0; j < kCpt; ++j)

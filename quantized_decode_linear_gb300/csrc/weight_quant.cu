@@ -124,7 +124,9 @@ __global__ void __launch_bounds__(kThreadsW, 2) fp8_weight_quant_kernel(const vo
         load8<kBf16>(w, elem_of(c), v);
         encode(v, c);
     }
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // no early release of dependents: the decode kernels stream weights
+    // before their own dependency wait, so a kernel that writes weights must
+    // have finished before the next one starts
 }
 
 __global__ void __launch_bounds__(256) awq_pack_kernel(const uint8_t *nib, uint32_t k, uint32_t n, uint32_t *qw) {
@@ -144,7 +146,7 @@ __global__ void __launch_bounds__(256) awq_pack_kernel(const uint8_t *nib, uint3
         }
         qw[i] = word;
     }
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // no early release of dependents (see fp8_weight_quant_kernel)
 }
 
 cudaLaunchAttribute pdl_attribute() {

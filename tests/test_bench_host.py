@@ -30,12 +30,11 @@ def _algorithmic_bytes(wl, rows):
 
 
 def test_traffic_records_are_current_and_near_the_algorithmic_bytes():
-    kernel_src = {"w8a8": "w8a8_gemm_tc.cu", "int4": "int4_qkv_cc.cu"}
     assert bench.TRAFFIC
     for key, rec in bench.TRAFFIC.items():
         name, rows = key.rsplit("@", 1)
         wl = syn.WORKLOADS[name]
-        assert rec["src"] == bench._src_hash([kernel_src[name.split("_")[0]]]), key
+        assert rec["src"] == bench._src_hash([rec["file"]]), key
         alg = _algorithmic_bytes(wl, int(rows))
         assert alg <= rec["bytes"] <= 1.01 * alg, (key, rec["bytes"], alg)
 

@@ -95,6 +95,25 @@ def test_gemv_accumulating_output(fmt, n, k, rows):
                 what=f"fmt={fmt} split={qdl.w8a8_plan(w, rows)['split_k']}")
 
 
+@pytest.mark.parametrize("rows", [64, 128, 256])
+def test_gemv_accumulating_output_whole_tiles(rows):
+    """QDL_OUT_F32_ADD on a weight wide enough that CTAs own whole output
+    tiles (20480 rows in 160 tiles of K = 1024): a tile with a single writer
+    must still add to what out held, not overwrite it"""
+    fmt, n, k = qdl.BLOCK128, 20480, 1024
+    segs = _segments(fmt, k, [n], seed=rows + 5)
+    x = syn.bf16_normal((rows, k), seed=rows + 6)
+    qo, so = oracle.act_quant(fmt, x, k)
+    yo, bo = oracle.w8a8_gemv(fmt, qo, so, segs)
+    w, _keep = upload_weight(segs, fmt)
+    base = np.random.default_rng(rows).normal(0.0, 1.0, (rows, n)).astype(np.float32)
+    out = dev(base)
+    qdl.w8a8_gemv(w, dev(qo), dev(so), rows, out, out_dtype=qdl.OUT_F32_ADD)
+    torch.cuda.synchronize()
+    check_close(host(out), base.astype(np.float64) + yo, bo + 2 ** -18 * np.abs(base) / 2e-3,
+                what=f"rows={rows} whole tiles")
+
+
 @pytest.mark.parametrize("fmt", [qdl.PER_ROW, qdl.BLOCK128])
 def test_bf16_output(fmt):
     rows, k = 9, 512
