@@ -165,10 +165,9 @@ class W8A8Case:
         # of the GEMV launches: weights + scales + e4m3 activations + act scales + output
         self.gemv_bytes = sum(n * K + w_scales + p * K + p * spr * 4 + p * n * 4 for _, p in self.passes)
         self.gemv_launches = len(self.passes)
-        # the library's plan per pass: 1 launch when the GEMV quantises its own
-        # activations, else the quantiser + the GEMV (always for the SiLU variant)
+        # the library's plan per pass: the quantiser, then the GEMV
         plans = [qdl.w8a8_plan(self.weights[0], p) for _, p in self.passes]
-        self.launches_per_step = sum(2 if wl.silu else pl["proj_launches"] for pl in plans)
+        self.launches_per_step = sum(pl["proj_launches"] for pl in plans)
         # the GEMV as the projection runs it: with split K it adds into the
         # zeroed f32 output
         self.dom_dtypes = [qdl.OUT_F32_ADD if pl["proj_accumulates"] else qdl.OUT_F32 for pl in plans]

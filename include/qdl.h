@@ -69,8 +69,17 @@ typedef enum { QDL_SCALE_PER_ROW = 0, QDL_SCALE_BLOCK128 = 1 } qdl_scale;
 /* Output element type of the W8A8 GEMV.  QDL_OUT_F32_ADD (qdl_w8a8_gemv
  * only) adds y to the f32 values already in out; split-K partial sums are
  * then added with f32 atomics, so their order, and the last bits of the
- * result, may vary from run to run. */
-typedef enum { QDL_OUT_F32 = 0, QDL_OUT_BF16 = 1, QDL_OUT_F32_ADD = 2 } qdl_dtype;
+ * result, may vary from run to run.  QDL_OUT_F32_DETERMINISTIC writes f32
+ * like QDL_OUT_F32, but the projections then never add split-K partials
+ * with atomics: they meet in a fixed-order reduction, so identical calls
+ * give identical bits (for callers that compare logits across runs), at the
+ * cost of the cluster reduction's time where K is split. */
+typedef enum {
+    QDL_OUT_F32 = 0,
+    QDL_OUT_BF16 = 1,
+    QDL_OUT_F32_ADD = 2,
+    QDL_OUT_F32_DETERMINISTIC = 3
+} qdl_dtype;
 
 #define QDL_MAX_ROWS 256  /* w8a8_decode.rs W8A8_MAX_ROWS */
 #define QDL_K_UNIT 128    /* w8a8_decode.rs W8A8_K_UNIT   */
@@ -175,8 +184,10 @@ QDL_API qdl_status qdl_w8a8_gemv(const qdl_w8a8_weight *w, const uint8_t *q, con
  * first sets out[0..rows)[0..N) to zero and the GEMV adds into it
  * (QDL_OUT_F32_ADD): the order of the split-K additions varies, so results
  * may differ in the last bits from run to run (always within the GEMV's
- * error bound).  bf16 output takes the fixed-order reduction.  out_dtype is
- * QDL_OUT_F32 or QDL_OUT_BF16.  Checks: those of qdl_w8a8_gemv, plus the
+ * error bound).  bf16 output and QDL_OUT_F32_DETERMINISTIC take the
+ * fixed-order reduction and are reproducible bit for bit.  out_dtype is
+ * QDL_OUT_F32, QDL_OUT_BF16 or QDL_OUT_F32_DETERMINISTIC.  Checks: those of
+ * qdl_w8a8_gemv, plus the
  * quantiser's K <= QDL_MAX_K and the x checks of qdl_act_quant. */
 QDL_API qdl_status qdl_w8a8_proj(const qdl_w8a8_weight *w, const void *x, uint32_t ldx, uint32_t rows,
                          void *out, int32_t out_dtype, uint32_t ldc, uint8_t *q, float *q_scale,
@@ -334,7 +345,7 @@ QDL_API qdl_status qdl_w8a8_proj_static(const qdl_w8a8_weight *w, const void *x,
  * for tuning and tests).  Queries the device's occupancy tables; launches
  * nothing. */
 typedef struct {
-    int32_t kernel;      /* 0 = tcgen05 (tensor memory), 1 = mma.sync streaming */
+    int32_t kernel;      /* 0 = tcgen05 (tensor memory); the only W8A8 kernel */
     uint32_t mma_n;      /* token columns per MMA (tcgen05: 16..256) */
     uint32_t tiles;      /* 128-row output tiles */
     uint32_t split_k;    /* CTAs per tile along K: one cluster, except where the projection's
@@ -344,9 +355,8 @@ typedef struct {
     uint32_t threads;    /* threads per CTA */
     uint32_t smem_bytes; /* dynamic shared memory per CTA */
     int32_t resident_clusters; /* clusters of split_k CTAs that fit the device at once */
-    uint32_t proj_launches; /* kernels one qdl_w8a8_proj call makes for these rows: 1 when
-                               the GEMV quantises its own activations (Block128, rows <= 16,
-                               every split-K rank's K blocks fit its ring), else 2 */
+    uint32_t proj_launches; /* kernels one qdl_w8a8_proj call makes for these rows: the
+                               quantiser, then the GEMV (2) */
     uint32_t proj_accumulates; /* 1 when qdl_w8a8_proj with f32 output zeroes out and runs the
                                   GEMV as QDL_OUT_F32_ADD (split K, or the stream-K kernel
                                   that Block128 takes for 17..128 rows), else 0 */

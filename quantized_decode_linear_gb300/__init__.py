@@ -18,6 +18,7 @@ BLOCK128 = 1
 OUT_F32 = 0
 OUT_BF16 = 1
 OUT_F32_ADD = 2  # qdl_w8a8_gemv only: out += y
+OUT_F32_DETERMINISTIC = 3  # f32, split-K partials reduced in a fixed order (reproducible bits)
 MAX_ROWS = 256
 K_UNIT = 128
 

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libqdl.so")
 
-SOURCES = ["qdl_api.cu", "act_quant.cu", "w8a8_gemv_tma.cu", "w8a8_gemm_tc.cu", "int4_qkv.cu", "int4_qkv_tc.cu", "int4_qkv_cc.cu",
+SOURCES = ["qdl_api.cu", "act_quant.cu", "tma_host.cu", "w8a8_gemm_tc.cu", "int4_qkv.cu", "int4_qkv_tc.cu", "int4_qkv_cc.cu",
            "kv_quant.cu", "weight_quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",

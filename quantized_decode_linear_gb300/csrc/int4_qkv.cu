@@ -18,7 +18,9 @@
 // puts the low halves (or high halves) of both words side by side; then
 // (X >> 4j) & 0x000F000F | 0x64006400 is the f16 pair (1024 + nib(k),
 // 1024 + nib(k+1)) of one column, and one f16x2 subtraction of 1024 leaves
-// the exact nibbles, paired along K as the MMA operand wants.
+// the exact nibbles, paired along K as the MMA operand wants.  This is the
+// published AWQ / Marlin-style interleave-to-f16 conversion (the 4-bit value
+// ORed into the mantissa of 1024.0 in f16), implemented from its description.
 //
 // Tiling.  A warp owns 128 columns (16 per 4-lane group: two packed words)
 // as eight m16n8k16 tiles (columns as the MMA's M, tokens as N, K = 16).

@@ -176,6 +176,9 @@ __device__ __forceinline__ uint32_t h2_bits(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// The published AWQ / Marlin-style interleave-to-f16 conversion, implemented
+// from its description: a 4-bit value ORed into the mantissa of the f16
+// pattern of 1024.0 (0x6400) is the f16 number 1024 + nib, two per word.
 __device__ __forceinline__ uint32_t lop3_mask_or(uint32_t v, uint32_t mask) {
     uint32_t r;
     asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(mask), "r"(0x64006400u));  // (v & mask) | 0x64006400
@@ -543,36 +546,6 @@ uint32_t cta_slots_i4() {
     return cache[dev];
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// 2D row-major tensor [outer, inner] of 4-byte elements, row pitch inner * 4
-// bytes, copied in boxes of box_inner x box_outer; elements past either end
-// read as zero.
-cudaError_t make_tmap_4b(CUtensorMap *map, CUtensorMapDataType type, const void *base, uint64_t inner, uint64_t outer,
-                         uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
-    PFN_cuTensorMapEncodeTiled_v12000 fn = tmap_encoder();
-    if (fn == nullptr) return cudaErrorNotSupported;
-    cuuint64_t gdim[2] = {inner, outer};
-    cuuint64_t gstride[1] = {inner * 4};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estride[2] = {1, 1};
-    CUresult r = fn(map, type, 2, const_cast<void *>(base), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 cudaLaunchAttribute pdl_attr() {
     cudaLaunchAttribute at;
     at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -617,20 +590,6 @@ cudaError_t launch_int4_zero(const Int4Args &a, cudaStream_t s) {
     zc.attrs = attr;
     zc.numAttrs = QDL_TUNE_PDL ? 1 : 0;
     return cudaLaunchKernelEx(&zc, int4_zero_kernel, a);
-}
-
-cudaError_t make_tmap_plain(CUtensorMap *map, bool f32, const void *base, uint64_t inner, uint64_t outer,
-                            uint32_t box_inner, uint32_t box_outer) {
-    return make_tmap_4b(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT32, base, inner, outer,
-                        box_inner, box_outer, CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
-cudaError_t make_tmap_words(CUtensorMap *map, const void *base, uint64_t words, uint64_t rows, uint32_t box_rows) {
-    return make_tmap_4b(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, base, words, rows, 32, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
-cudaError_t make_tmap_f32(CUtensorMap *map, const float *x, uint64_t k, uint64_t rows, uint32_t box_rows) {
-    return make_tmap_4b(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x, k, rows, 32, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 bool int4_tc_supported(uint32_t nq, uint32_t nkv, uint32_t group) {

@@ -17,10 +17,6 @@ namespace qdl {
 namespace {
 
 constexpr uint32_t kWeightMagic = 0x51444C57u;  // "QDLW"
-#ifndef QDL_MMA_MAX_ROWS
-#define QDL_MMA_MAX_ROWS 0
-#endif
-constexpr uint32_t kMmaMaxRows = QDL_MMA_MAX_ROWS;  // <= 16
 thread_local std::string g_last_error;
 
 qdl_status fail(qdl_status s, const char *fmt, ...) {
@@ -96,10 +92,7 @@ qdl_status check_weight(const char *who, const qdl_w8a8_weight *w) {
 
 qdl_status launch_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *q_scale, uint32_t rows, void *out,
                        int32_t out_dtype, uint32_t ldc, cudaStream_t stream, uint32_t debug_skip_iter = ~0u,
-                       uint64_t wait_limit_ns = kWaitLimitNs, const void *fused_x = nullptr, uint32_t fused_ldx = 0,
-                       bool accumulate = false) {
-    const size_t spr = scales_per_row(w->format, w->k);
-    const size_t elt = out_dtype == QDL_OUT_BF16 ? 2 : 4;
+                       uint64_t wait_limit_ns = kWaitLimitNs, bool accumulate = false) {
     W8A8Args a = {};
     a.w0 = w->segs[0].weight;
     a.sw0 = w->segs[0].scale;
@@ -110,6 +103,10 @@ qdl_status launch_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *
     const uint8_t *seg_w[3] = {a.w0, a.w1, a.w2};
     const uint32_t seg_n[3] = {w->segs[0].n, w->count > 1 ? w->segs[1].n : w->segs[0].n,
                                w->count > 2 ? w->segs[2].n : w->segs[0].n};
+    a.q = q;
+    a.sa = q_scale;
+    a.out = out;
+    a.m = rows;
     a.ldc = ldc;
     a.out_bf16 = out_dtype == QDL_OUT_BF16;
     a.n = w->n;
@@ -121,40 +118,14 @@ qdl_status launch_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *
     a.wait_limit_ns = wait_limit_ns;
     a.accumulate = out_dtype == QDL_OUT_F32_ADD || (accumulate && out_dtype == QDL_OUT_F32);
     a.out_zeroed = accumulate && out_dtype == QDL_OUT_F32;
-    // Token rows up to QDL_MMA_MAX_ROWS go to the mma.sync streaming kernel;
-    // all others take one pass of the tcgen05 kernel (rows <= 256).
-    if (rows > kMmaMaxRows) {
-        a.q = q;
-        a.sa = q_scale;
-        a.out = out;
-        a.m = rows;
-        if (fused_x != nullptr) {  // Block128, rows <= 16: quantise inside the GEMV
-            a.x = fused_x;
-            a.ldx = fused_ldx;
-            a.q_out = const_cast<uint8_t *>(q);
-            a.sa_out = const_cast<float *>(q_scale);
-            cudaError_t e = launch_w8a8_proj_fused(a, seg_w, seg_n, stream);
-            if (e != cudaSuccess) return cuda_fail("qdl_w8a8_proj", e);
-            return ok();
-        }
-        cudaError_t e = launch_w8a8_gemm_tc(a, w->format, seg_w, seg_n, stream);
-        if (e != cudaSuccess) return cuda_fail("qdl_w8a8_gemv", e);
-        return ok();
-    }
-    (void)spr;
-    (void)elt;
-    a.q = q;
-    a.sa = q_scale;
-    a.out = out;
-    a.m = rows;
-    cudaError_t e = launch_w8a8_gemv_tma(a, w->format, seg_w, seg_n, stream);
+    // one pass of the tcgen05 kernel for any rows <= 256
+    cudaError_t e = launch_w8a8_gemm_tc(a, w->format, seg_w, seg_n, stream);
     if (e != cudaSuccess) return cuda_fail("qdl_w8a8_gemv", e);
     return ok();
 }
 
 // split-K factor the tcgen05 GEMV takes for this weight and row count
 uint32_t gemv_split(const qdl_w8a8_weight *w, uint32_t rows) {
-    if (rows <= kMmaMaxRows) return 1;
     W8A8Args a = {};
     a.n = w->n;
     a.k = w->k;
@@ -178,14 +149,6 @@ bool zero_f32_output(ActQuantArgs &a, const qdl_w8a8_weight *w, uint32_t rows, v
     a.zldc = ldc;
     a.zn = n;
     return true;
-}
-
-// qdl_w8a8_proj makes one launch (the GEMV quantises its own activation
-// blocks) for Block128, up to 16 rows, when every split-K rank's K blocks fit
-// the fused kernel's ring; otherwise the quantiser and the GEMV.
-bool proj_is_fused(const qdl_w8a8_weight *w, uint32_t rows) {
-    return QDL_TUNE_FUSED && w->format == QDL_SCALE_BLOCK128 && rows <= 16 && kMmaMaxRows == 0 &&
-           w8a8_fused_fits(w->n, w->k / kKUnit);
 }
 
 }  // namespace
@@ -312,9 +275,10 @@ static qdl_status check_gemv(const char *who, const qdl_w8a8_weight *w, const ui
     if (!aligned(q, 16) || !aligned(q_scale, 4))
         return fail(QDL_ERR_INVALID_ARG, "%s: q must be 16-byte and q_scale 4-byte aligned", who);
     if (ldc < w->n) return fail(QDL_ERR_INVALID_ARG, "%s: ldc=%u < N=%u", who, ldc, w->n);
-    if (out_dtype != QDL_OUT_F32 && out_dtype != QDL_OUT_BF16 && !(allow_add && out_dtype == QDL_OUT_F32_ADD))
+    if (out_dtype != QDL_OUT_F32 && out_dtype != QDL_OUT_BF16 && out_dtype != QDL_OUT_F32_DETERMINISTIC &&
+        !(allow_add && out_dtype == QDL_OUT_F32_ADD))
         return fail(QDL_ERR_INVALID_ARG, "%s: output dtype %d is not %s", who, (int)out_dtype,
-                    allow_add ? "F32, BF16 or F32_ADD" : "F32 or BF16");
+                    allow_add ? "F32, BF16, F32_ADD or F32_DETERMINISTIC" : "F32, BF16 or F32_DETERMINISTIC");
     if (out == nullptr || !aligned(out, out_dtype == QDL_OUT_BF16 ? 2 : 4))
         return fail(QDL_ERR_INVALID_ARG, "%s: output is NULL or misaligned", who);
     return QDL_OK;
@@ -330,19 +294,15 @@ qdl_status qdl_w8a8_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float
 namespace {
 
 // One decode projection of up to 256 rows: the quantiser (plain or SiLU),
-// then the GEMV; or one fused launch where that applies.
+// then the GEMV.
 qdl_status proj_pass(const char *who, const qdl_w8a8_weight *w, const void *x, const void *up, uint32_t ldx, uint32_t ld_up,
                      bool silu, uint32_t rows, void *out, int32_t out_dtype, uint32_t ldc, uint8_t *q, float *q_scale,
                      cudaStream_t stream) {
-    if (!silu && proj_is_fused(w, rows)) {
-        // one launch: the GEMV quantises its own activation blocks
-        return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, stream, ~0u, kWaitLimitNs, x, ldx);
-    }
     ActQuantArgs a = {static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(up), ldx, ld_up, rows, w->k, q, q_scale};
     const bool acc = zero_f32_output(a, w, rows, out, out_dtype, ldc, w->n);
     cudaError_t e = launch_act_quant(a, w->format, silu, stream);
     if (e != cudaSuccess) return cuda_fail(who, e);
-    return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, stream, ~0u, kWaitLimitNs, nullptr, 0, acc);
+    return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, stream, ~0u, kWaitLimitNs, acc);
 }
 
 // Rows beyond 256 (a prefill-shaped call) in passes of 256 rows, in order on
@@ -624,8 +584,9 @@ qdl_status qdl_w8a8_proj_static(const qdl_w8a8_weight *w, const void *x, uint32_
         return fail(QDL_ERR_UNSUPPORTED, "%s: %u rows of K=%u need %zu bytes of static scratch, the limit is %d", who, rows,
                     w->k, scale_off + scale_bytes, QDL_STATIC_SCRATCH_BYTES);
     if (ldc < w->n) return fail(QDL_ERR_INVALID_ARG, "%s: ldc=%u < N=%u", who, ldc, w->n);
-    if (out_dtype != QDL_OUT_F32 && out_dtype != QDL_OUT_BF16)
-        return fail(QDL_ERR_INVALID_ARG, "%s: output dtype %d is not F32 or BF16", who, (int)out_dtype);
+    if (out_dtype != QDL_OUT_F32 && out_dtype != QDL_OUT_BF16 && out_dtype != QDL_OUT_F32_DETERMINISTIC)
+        return fail(QDL_ERR_INVALID_ARG, "%s: output dtype %d is not F32, BF16 or F32_DETERMINISTIC", who,
+                    (int)out_dtype);
     if (out == nullptr || !aligned(out, out_dtype == QDL_OUT_BF16 ? 2 : 4))
         return fail(QDL_ERR_INVALID_ARG, "%s: output is NULL or misaligned", who);
     if ((st = check_input(who, "x", x, ldx, w->k)) != QDL_OK) return st;
@@ -653,7 +614,7 @@ qdl_status qdl_w8a8_plan(const qdl_w8a8_weight *w, uint32_t rows, qdl_plan *plan
     a.kb = w->k / kKUnit;
     a.m = rows;
     PlanInfo p = {};
-    cudaError_t e = rows > kMmaMaxRows ? plan_w8a8_gemm_tc(a, w->format, &p) : plan_w8a8_gemv_tma(a, w->format, &p);
+    cudaError_t e = plan_w8a8_gemm_tc(a, w->format, &p);
     if (e != cudaSuccess) return cuda_fail(who, e);
     plan->kernel = p.kernel;
     plan->mma_n = p.mma_n;
@@ -663,8 +624,8 @@ qdl_status qdl_w8a8_plan(const qdl_w8a8_weight *w, uint32_t rows, qdl_plan *plan
     plan->threads = p.threads;
     plan->smem_bytes = p.smem;
     plan->resident_clusters = p.clusters;
-    plan->proj_launches = proj_is_fused(w, rows) ? 1u : 2u;
-    plan->proj_accumulates = !proj_is_fused(w, rows) && proj_accumulates(w, rows) ? 1u : 0u;
+    plan->proj_launches = 2u;  // the quantiser, then the GEMV
+    plan->proj_accumulates = proj_accumulates(w, rows) ? 1u : 0u;
     plan->proj_streamk = plan->proj_accumulates && w8a8_streamk_applies(w->format, rows) ? 1u : 0u;
     return ok();
 }
@@ -673,9 +634,7 @@ qdl_status qdl_check_device_fault(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
     uint32_t word = 0, word_tc = 0;
-    if ((e = read_and_clear_gemv_fault(&word)) != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
-    if ((e = read_and_clear_tc_fault(&word_tc)) != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
-    word |= word_tc;
+    if ((e = read_and_clear_tc_fault(&word)) != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
     if ((e = read_and_clear_int4_fault(&word_tc)) != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);
     word |= word_tc;
     if ((e = read_and_clear_int4cc_fault(&word_tc)) != cudaSuccess) return cuda_fail("qdl_check_device_fault", e);

@@ -9,14 +9,6 @@
 
 namespace qdl {
 
-#ifndef QDL_TUNE_FUSED
-// 1: qdl_w8a8_proj quantises Block128 activations inside the GEMV (rows <= 16,
-// short K ranges) in one launch.  Off: measured slower than the quantiser +
-// GEMV pair overlapped by programmatic launch (11.3 vs 9.45 us per call on
-// the M=8, K=4096 QKV projection), since every column tile re-quantises its
-// K range on the critical path.
-#define QDL_TUNE_FUSED 0
-#endif
 #ifndef QDL_INT4_CC_MAX_ROWS
 // token rows (at most 8) up to which the AWQ projection takes the CUDA-core
 // stream-K kernel, also where the tcgen05 kernel applies.  Measured on the
@@ -75,11 +67,6 @@ struct W8A8Args {
     uint32_t accumulate;       // f32 output: out += y, split-K ranks add their partials atomically
     uint32_t out_zeroed;       // with accumulate: out was set to zero by the quantiser (a plain store suffices)
     uint32_t early_trigger;    // set by the launcher: release dependent kernels at the start
-    // fused projection only: bf16 input [m, ldx] and the scratch it fills
-    const void *x;
-    uint32_t ldx;
-    uint8_t *q_out;
-    float *sa_out;
 };
 
 struct Int4Args {
@@ -104,12 +91,8 @@ struct PlanInfo {
     int clusters;
 };
 cudaError_t plan_w8a8_gemm_tc(const W8A8Args &a, int format, PlanInfo *p);
-cudaError_t plan_w8a8_gemv_tma(const W8A8Args &a, int format, PlanInfo *p);
 
 cudaError_t launch_act_quant(const ActQuantArgs &a, int format, bool silu, cudaStream_t s);
-cudaError_t launch_w8a8_gemv_tma(const W8A8Args &a, int format, const uint8_t *const seg_w[3],
-                                 const uint32_t seg_n[3], cudaStream_t s);
-cudaError_t read_and_clear_gemv_fault(uint32_t *value);
 cudaError_t launch_w8a8_gemm_tc(const W8A8Args &a, int format, const uint8_t *const seg_w[3],
                                 const uint32_t seg_n[3], cudaStream_t s);
 cudaError_t read_and_clear_tc_fault(uint32_t *value);
@@ -118,10 +101,6 @@ uint32_t tc_bucket(uint32_t m);  // MMA N of the tensor-core kernel for m token 
 // (one range of (tile, K block) units per CTA; the projection zeroes its f32
 // output for it)
 bool w8a8_streamk_applies(int format, uint32_t rows);
-// true when every split-K rank's K blocks fit the fused variant's ring (rows <= 16)
-bool w8a8_fused_fits(uint32_t n, uint32_t kb);
-cudaError_t launch_w8a8_proj_fused(const W8A8Args &a, const uint8_t *const seg_w[3], const uint32_t seg_n[3],
-                                   cudaStream_t s);
 // Split-K factor minimising waves x (K blocks per CTA + fixed cost), where a
 // split CTA also pays reduce_cost (in K-block units) for the cluster reduction;
 // slots[s-1]: CTAs resident at once when launched in clusters of s.
@@ -246,17 +225,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 // Read-only load through L1 (small operands shared by every warp of a CTA).
 __device__ __forceinline__ uint4 ld_ro_v4(const void *p) {
     return __ldg(reinterpret_cast<const uint4 *>(p));
-}
-
-// D += A * B on the FP8 tensor-core path: m16n8k32, A row-major (16 x 32
-// e4m3), B column-major (32 x 8 e4m3), f32 accumulators.
-__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // D += A * B, m16n8k16, f16 inputs, f32 accumulators.

@@ -20,6 +20,11 @@ cudaError_t make_tmap_words(CUtensorMap *map, const void *base, uint64_t words, 
 // x [rows, k] f32, box 32 values x box_rows rows, 128-byte swizzle; rows past the end read as zero
 cudaError_t make_tmap_f32(CUtensorMap *map, const float *x, uint64_t k, uint64_t rows, uint32_t box_rows);
 
+// [outer, inner] row-major tensor of 4-byte elements of `type`, row pitch
+// inner * 4 bytes, box box_inner x box_outer, the given swizzle; elements past
+// either end read as zero
+cudaError_t make_tmap_4b(CUtensorMap *map, CUtensorMapDataType type, const void *base, uint64_t inner, uint64_t outer,
+                         uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
 // [outer, inner] row-major tensor of 4-byte elements (u32 codes, or f32 when
 // `f32`), row pitch inner * 4 bytes, box box_inner x box_outer, no swizzle;
 // elements past either end read as zero

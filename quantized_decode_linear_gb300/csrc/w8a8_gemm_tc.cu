@@ -8,8 +8,8 @@
 // Roles (one CTA = 128 output rows x a range of 128-wide K blocks):
 //   warp 0, one lane : TMA producer.  Per K block, the 128 x 128-byte weight
 //                      tile (one box, or eight 16-row boxes when the tile
-//                      spans two segments) and, unless fused, the NTOK-row
-//                      activation box land in a shared-memory stage (128-byte
+//                      spans two segments) and the NTOK-row activation box
+//                      land in a shared-memory stage (128-byte
 //                      swizzle = the canonical K-major SW128 operand layout).
 //   warp 1           : allocates the tensor memory; one lane issues
 //                      tcgen05.mma kind::f8f6f4 (M = 128 weight rows,
@@ -18,15 +18,6 @@
 //                      mbarrier.
 //   warp 2 (Block128): stages sa[m, kb] * sw[kb] for each K block in shared
 //                      memory for the epilogue (one buffer per accumulator).
-//   fused variant    : when the CTA's whole K range fits the ring, a prologue
-//                      replaces the activation TMA and the scale warp: one lane
-//                      requests every weight block at once while warps 1..
-//                      quantise the bf16 activations of the CTA's K blocks
-//                      (absmax/448 per token and 128-group, RNE satfinite E4M3,
-//                      the arithmetic of the act-quant kernel) straight into
-//                      the swizzled operands and the block scales into shared
-//                      memory; the CTAs of tile 0 also write the codes and
-//                      scales to the caller's scratch.  One launch per call.
 //   other warps      : epilogue, reading the f32 accumulators with tcgen05.ld.
 //
 // Scales.  PerRow: the accumulator sums the CTA's whole K range; the epilogue
@@ -123,9 +114,6 @@ namespace cg = cooperative_groups;
 #ifndef QDL_TC_REGS_32
 #define QDL_TC_REGS_32 96  // 3 CTAs of 7 warps
 #endif
-#ifndef QDL_TC_REGS_64
-#define QDL_TC_REGS_64 144  // 2 CTAs of 7 warps
-#endif
 #ifndef QDL_TC_BIGBOX
 #define QDL_TC_BIGBOX 1
 #endif
@@ -146,7 +134,7 @@ constexpr uint32_t pow2_at_least(uint32_t v) {
     return p;
 }
 
-template <int NTOK, bool kBlock, bool kFused>
+template <int NTOK, bool kBlock>
 struct Tc {
     static constexpr uint32_t kABytes = NTOK * 128;
     static constexpr uint32_t kStage = kWBytes + kABytes;  // multiple of 1024 (NTOK % 8 == 0)
@@ -154,7 +142,7 @@ struct Tc {
     static constexpr uint32_t kBudget = kBlock && NTOK == 128 ? QDL_TC_STAGE_BYTES_B128
                                         : kBlock && NTOK == 64  ? QDL_TC_STAGE_BYTES_B64
                                         : NTOK >= QDL_TC_BIG_NTOK ? QDL_TC_STAGE_BYTES_BIG
-                                        : NTOK == 16 && !kFused   ? QDL_TC_STAGE_BYTES_16
+                                        : NTOK == 16              ? QDL_TC_STAGE_BYTES_16
                                                                   : QDL_TC_STAGE_BYTES;
     static constexpr int kMinStages = NTOK <= 64 ? QDL_TC_MIN_STAGES : 3;
     static constexpr int kStages = (int)(kBudget / kStage) < kMinStages ? kMinStages : (int)(kBudget / kStage);
@@ -175,43 +163,37 @@ struct Tc {
             ? kCpt
             : (NTOK <= 64 ? QDL_TC_INFLIGHT_SMALL : NTOK == 128 ? QDL_TC_INFLIGHT_128 : QDL_TC_INFLIGHT_256);
     // register cap per thread, so that several CTAs fit an SM (255: none)
-    static constexpr int kMaxRegs = !kBlock || kFused ? 255 : NTOK == 32 ? QDL_TC_REGS_32 : NTOK == 64 ? QDL_TC_REGS_64 : 255;
+    // (the 64-token Block128 variants run one CTA per SM with their deep ring,
+    // so they take all the registers they need: a cap of 144 spilled, and
+    // lifting it took the gate/up projection at M = 64 from 59.3 to 54.9 us)
+    static constexpr int kMaxRegs = !kBlock ? 255 : NTOK == 32 ? QDL_TC_REGS_32 : 255;
     static constexpr uint32_t kTmemCols = pow2_at_least(kAcc * NTOK);
     static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
     static_assert(kTileRows * NTOK * 4 <= kBarOff, "split-K partials must fit in the stage ring");
     static_assert(kTmemCols <= 512, "tensor memory");
     static_assert((2 * kStages + 3 * kAcc + 1) * 8 + 8 <= 512, "barrier area");
     static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
-    static_assert(!kFused || (kBlock && NTOK == 16), "fused quantisation: Block128, up to 16 rows");
     static_assert(kInFlight % 16 == 0 && kCpt % kInFlight == 0, "epilogue load groups");
 };
 
 // ---------------------------------------------------------------- kernel helpers
 
-__device__ __forceinline__ void sts64(uint32_t addr, uint32_t lo, uint32_t hi) {
-    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(lo), "r"(hi) : "memory");
-}
-
-__device__ __forceinline__ float quant_operand(float v, float scale) {
-    return scale == 0.0f ? v : __fdiv_rn(v, scale);
-}
-
 // ---------------------------------------------------------------- kernel
 
-template <int NTOK, bool kBlock, bool kFused>
-__global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnreg__((Tc<NTOK, kBlock, kFused>::kMaxRegs))
+template <int NTOK, bool kBlock>
+__global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc<NTOK, kBlock>::kMaxRegs))
     w8a8_gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                         const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_b0,
                         const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_b2,
                         const __grid_constant__ CUtensorMap tm_a, const W8A8Args a) {
-    using C = Tc<NTOK, kBlock, kFused>;
+    using C = Tc<NTOK, kBlock>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
     uint64_t *empty = full + C::kStages;
     uint64_t *accf = empty + C::kStages;  // [kAcc] accumulator buffer ready
     uint64_t *acce = accf + C::kAcc;      // [kAcc] accumulator buffer drained
-    uint64_t *scal = acce + C::kAcc;      // [kAcc] fused: block scales written
+    uint64_t *scal = acce + C::kAcc;      // [kAcc] block scales written
     uint64_t *done = scal + C::kAcc;      // all MMAs complete
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     volatile uint32_t *abort_flag = tmem_slot + 1;
@@ -305,89 +287,9 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
 #pragma unroll
     for (int j = 0; j < (kBlock ? kCpt : 1); ++j) total[j] = 0.0f;
 
-    if constexpr (kFused) {
-        // ------------------------------------------------------------ fused prologue
-        // The CTA's whole K range fits the ring (the host only takes this
-        // variant when niter <= kStages and niter <= kAcc): one lane requests
-        // the weights of every block at once, and meanwhile warps 1.. quantise
-        // the CTA's activation blocks (16 lanes per 128-value group of a token
-        // row, rows >= m as zeros) straight into the B operands, and the block
-        // scales sa * sw into sbuf.
-        if (warp == 0) {
-            if (lane == 0) {
-                prefetch_tmap(tile_big);
-                for (uint32_t it = 0; it < niter; ++it) {
-                    mbar_arrive_expect_tx(&full[it], kWBytes);
-                    issued = it + 1;
-                    if (it == a.debug_skip_iter) continue;  // self-test: this stage never lands
-                    load_weights(it, smem + it * C::kStage, &full[it]);
-                }
-            }
-        } else {
-            grid_dep_wait();  // x comes from the previous kernel; the scratch may still be read by it
-            const int h = lane & 15, half = lane >> 4;
-            const uint32_t sbase = smem_u32(smem);
-            const uint16_t *x = reinterpret_cast<const uint16_t *>(a.x);
-            const uint32_t ngroups = NTOK * niter;
-            constexpr uint32_t kQWarps = C::kThreads / 32 - 1;
-            constexpr int kPasses = (NTOK * C::kStages + 2 * kQWarps - 1) / (2 * kQWarps);
-            // every load of this warp first (independent), then the arithmetic
-            uint4 raw[kPasses];
-#pragma unroll
-            for (int ps = 0; ps < kPasses; ++ps) {
-                const uint32_t gi = 2 * (warp - 1) + 2 * kQWarps * ps + half;
-                const uint32_t it = gi / NTOK, r = gi % NTOK;
-                raw[ps] = gi < ngroups && r < a.m
-                              ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)r * a.ldx + (kb0 + it) * 128 + 8 * h))
-                              : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int ps = 0; ps < kPasses; ++ps) {
-                const uint32_t gi = 2 * (warp - 1) + 2 * kQWarps * ps + half;
-                const bool valid = gi < ngroups;
-                const uint32_t it = gi / NTOK, r = gi % NTOK, kb = kb0 + it;
-                const uint32_t w[4] = {raw[ps].x, raw[ps].y, raw[ps].z, raw[ps].w};
-                float v[8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    v[2 * j] = bf16_bits_to_f32(w[j] & 0xFFFFu);
-                    v[2 * j + 1] = bf16_bits_to_f32(w[j] >> 16);
-                }
-                float amax = 0.0f;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
-#pragma unroll
-                for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-                const float scale = __fdiv_rn(amax, 448.0f);
-                uint32_t lo = 0, hi = 0;  // token rows >= m: zero codes, nothing to divide
-                if (r < a.m) {
-                    uint32_t c[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        c[j] = cvt_e4m3x2(quant_operand(v[2 * j], scale), quant_operand(v[2 * j + 1], scale));
-                    lo = c[0] | (c[1] << 16);
-                    hi = c[2] | (c[3] << 16);
-                }
-                if (valid) {
-                    // row r, bytes 8h .. 8h+7: 16-byte chunk h/2 (swizzled by r & 7), half h & 1
-                    const uint32_t addr = sbase + it * C::kStage + kWBytes + r * 128 +
-                                          ((((uint32_t)h >> 1) ^ (r & 7)) << 4) + ((uint32_t)h & 1) * 8;
-                    sts64(addr, lo, hi);
-                    if (h == 0) sbuf[it * NTOK + r] = r < a.m ? scale * tile_sw(kb) : 0.0f;
-                    if (blockIdx.x == 0 && r < a.m) {  // tile-0 CTAs also fill the caller's scratch
-                        *reinterpret_cast<uint2 *>(a.q_out + (size_t)r * a.k + kb * 128 + 8 * h) = make_uint2(lo, hi);
-                        if (h == 0) a.sa_out[(size_t)r * a.kb + kb] = scale;
-                    }
-                }
-            }
-            fence_proxy_async_smem();  // the B operands are read by the tensor core
-        }
-        __syncthreads();
-    }
-
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && !kFused) {
+        if (lane == 0) {
             prefetch_tmap(tile_big);
             prefetch_tmap(&tm_a);
             const uint64_t pol_a = policy_evict_last();
@@ -440,7 +342,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
             }
             tc_commit(done);  // completes once every MMA issued above has
         }
-    } else if (kBlock && !kFused && warp == 2) {
+    } else if (kBlock && warp == 2) {
         // ------------------------------------------------------------ scale warp
         // sa[token, kb] * sw[tile, kb] of each K block into sbuf[b], one block
         // ahead in registers; lane l covers tokens l, l + 32, ...
@@ -473,19 +375,17 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
             __syncwarp();
             if (lane == 0) mbar_arrive(&scal[b]);
         }
-    } else if (kFused && warp == 2) {
-        // fused: the prologue already wrote every operand and block scale
     } else {
         // ------------------------------------------------------------ epilogue
         const int e = warp - C::kEpiBase;
         const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
         const int cgrp = e >> 2;    // column group
         const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16);
-        if (!kFused) grid_dep_wait();  // activation scales come from the previous kernel
+        grid_dep_wait();  // activation scales come from the previous kernel
         if constexpr (kBlock) {
             for (uint32_t it = 0; it < niter; ++it) {
                 const uint32_t b = it % C::kAcc;
-                if (!kFused) wait(&scal[b], (it / C::kAcc) & 1, 32);  // sa * sw of this block
+                wait(&scal[b], (it / C::kAcc) & 1, 32);  // sa * sw of this block
                 wait(&accf[b], (it / C::kAcc) & 1, 16);
                 tc_fence_after();
                 // kInFlight columns per wait: several loads in flight hide the
@@ -650,14 +550,14 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock, kFused>::kThreads, 1) __maxnr
 // current tile; when the CTA's range leaves that tile it stores them if the
 // CTA covered the whole tile, and otherwise adds them into the output with f32
 // atomics (a tile shared by two or more CTAs).  Roles, barriers and bounded waits are those
-// of w8a8_gemm_tc_kernel<NTOK, true, false>.
+// of w8a8_gemm_tc_kernel<NTOK, true>.
 template <int NTOK>
-__global__ void __launch_bounds__(Tc<NTOK, true, false>::kThreads, 1) __maxnreg__((Tc<NTOK, true, false>::kMaxRegs))
+__global__ void __launch_bounds__(Tc<NTOK, true>::kThreads, 1) __maxnreg__((Tc<NTOK, true>::kMaxRegs))
     w8a8_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                         const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_b0,
                         const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_b2,
                         const __grid_constant__ CUtensorMap tm_a, const W8A8Args a) {
-    using C = Tc<NTOK, true, false>;
+    using C = Tc<NTOK, true>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
@@ -889,14 +789,13 @@ __global__ void __launch_bounds__(Tc<NTOK, true, false>::kThreads, 1) __maxnreg_
                 if (row < a.n && !*abort_flag) {
                     float *orow = reinterpret_cast<float *>(a.out) + row + (size_t)(cgrp * kCpt) * a.ldc;
                     const uint32_t nt = a.m > (uint32_t)(cgrp * kCpt) ? a.m - cgrp * kCpt : 0u;  // valid tokens here
-                    if (whole && a.out_zeroed) {  // the only writer of this tile; out holds zeros
+                    // a tile this CTA covers whole over a zeroed output is stored; any
+                    // other (shared, or QDL_OUT_F32_ADD) is added with reductions, which
+                    // for a single writer is one exact add per element
+                    if (whole && a.out_zeroed) {
 #pragma unroll
                         for (int j = 0; j < kCpt; ++j)
                             if ((uint32_t)j < nt) orow[(size_t)j * a.ldc] = total[j];
-                    } else if (whole) {  // the only writer: out += y
-#pragma unroll
-                        for (int j = 0; j < kCpt; ++j)
-                            if ((uint32_t)j < nt) orow[(size_t)j * a.ldc] += total[j];
                     } else {
 #pragma unroll
                         for (int j = 0; j < kCpt; ++j)
@@ -936,9 +835,9 @@ __global__ void __launch_bounds__(Tc<NTOK, true, false>::kThreads, 1) __maxnreg_
 // with the token count (measured: one K block of time per 4 tokens).
 constexpr double tc_reduce_cost(int ntok) { return ntok / 4.0; }
 
-template <int NTOK, bool kBlock, bool kFused>
+template <int NTOK, bool kBlock>
 const uint32_t *cta_slots_tc() {
-    using C = Tc<NTOK, kBlock, kFused>;
+    using C = Tc<NTOK, kBlock>;
     static std::mutex mu;
     static std::vector<std::vector<uint32_t>> cache;
     int dev = 0;
@@ -946,8 +845,8 @@ const uint32_t *cta_slots_tc() {
     std::lock_guard<std::mutex> lock(mu);
     if ((int)cache.size() <= dev) cache.resize(dev + 1);
     if (cache[dev].empty()) {
-        const void *f = (const void *)w8a8_gemm_tc_kernel<NTOK, kBlock, kFused>;
-        cudaFuncSetAttribute(w8a8_gemm_tc_kernel<NTOK, kBlock, kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        const void *f = (const void *)w8a8_gemm_tc_kernel<NTOK, kBlock>;
+        cudaFuncSetAttribute(w8a8_gemm_tc_kernel<NTOK, kBlock>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::kAlloc);
         cache[dev].assign(8, 0);
         resident_cta_slots(f, C::kThreads, C::kAlloc, resident_ctas(f, C::kThreads, C::kAlloc, C::kTmemCols),
@@ -956,11 +855,11 @@ const uint32_t *cta_slots_tc() {
     return cache[dev].data();
 }
 
-template <int NTOK, bool kBlock, bool kFused>
+template <int NTOK, bool kBlock>
 cudaError_t launch_tc_variant(const W8A8Args &a, const CUtensorMap (&maps)[7], cudaStream_t s) {
-    using C = Tc<NTOK, kBlock, kFused>;
+    using C = Tc<NTOK, kBlock>;
     const uint32_t tiles = (a.n + kTileRows - 1) / kTileRows;
-    const uint32_t split = choose_split_k(tiles, a.kb, cta_slots_tc<NTOK, kBlock, kFused>(), tc_reduce_cost(NTOK));
+    const uint32_t split = choose_split_k(tiles, a.kb, cta_slots_tc<NTOK, kBlock>(), tc_reduce_cost(NTOK));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tiles, split, 1);
     cfg.blockDim = dim3(C::kThreads, 1, 1);
@@ -989,14 +888,14 @@ cudaError_t launch_tc_variant(const W8A8Args &a, const CUtensorMap (&maps)[7], c
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, w8a8_gemm_tc_kernel<NTOK, kBlock, kFused>, maps[0], maps[1], maps[2], maps[3],
+    return cudaLaunchKernelEx(&cfg, w8a8_gemm_tc_kernel<NTOK, kBlock>, maps[0], maps[1], maps[2], maps[3],
                               maps[4], maps[5], maps[6], a);
 }
 
-template <int NTOK, bool kBlock, bool kFused>
+template <int NTOK, bool kBlock>
 void plan_tc_variant(const W8A8Args &a, PlanInfo *p) {
-    using C = Tc<NTOK, kBlock, kFused>;
-    const uint32_t *slots = cta_slots_tc<NTOK, kBlock, kFused>();
+    using C = Tc<NTOK, kBlock>;
+    const uint32_t *slots = cta_slots_tc<NTOK, kBlock>();
     p->kernel = 0;
     p->mma_n = NTOK;
     p->tiles = (a.n + kTileRows - 1) / kTileRows;
@@ -1010,22 +909,22 @@ void plan_tc_variant(const W8A8Args &a, PlanInfo *p) {
 template <bool kBlock>
 void plan_tc_rows(const W8A8Args &a, uint32_t ntok, PlanInfo *p) {
     switch (ntok) {
-        case 16: return plan_tc_variant<16, kBlock, false>(a, p);
-        case 32: return plan_tc_variant<32, kBlock, false>(a, p);
-        case 64: return plan_tc_variant<64, kBlock, false>(a, p);
-        case 128: return plan_tc_variant<128, kBlock, false>(a, p);
-        default: return plan_tc_variant<256, kBlock, false>(a, p);
+        case 16: return plan_tc_variant<16, kBlock>(a, p);
+        case 32: return plan_tc_variant<32, kBlock>(a, p);
+        case 64: return plan_tc_variant<64, kBlock>(a, p);
+        case 128: return plan_tc_variant<128, kBlock>(a, p);
+        default: return plan_tc_variant<256, kBlock>(a, p);
     }
 }
 
 template <bool kBlock>
 cudaError_t launch_tc_rows(const W8A8Args &a, const CUtensorMap (&maps)[7], uint32_t ntok, cudaStream_t s) {
     switch (ntok) {
-        case 16: return launch_tc_variant<16, kBlock, false>(a, maps, s);
-        case 32: return launch_tc_variant<32, kBlock, false>(a, maps, s);
-        case 64: return launch_tc_variant<64, kBlock, false>(a, maps, s);
-        case 128: return launch_tc_variant<128, kBlock, false>(a, maps, s);
-        default: return launch_tc_variant<256, kBlock, false>(a, maps, s);
+        case 16: return launch_tc_variant<16, kBlock>(a, maps, s);
+        case 32: return launch_tc_variant<32, kBlock>(a, maps, s);
+        case 64: return launch_tc_variant<64, kBlock>(a, maps, s);
+        case 128: return launch_tc_variant<128, kBlock>(a, maps, s);
+        default: return launch_tc_variant<256, kBlock>(a, maps, s);
     }
 }
 
@@ -1033,7 +932,7 @@ cudaError_t launch_tc_rows(const W8A8Args &a, const CUtensorMap (&maps)[7], uint
 // the split-K Block128 variant, no cluster), at most one unit each.
 template <int NTOK>
 cudaError_t launch_streamk_variant(const W8A8Args &a, const CUtensorMap (&maps)[7], cudaStream_t s) {
-    using C = Tc<NTOK, true, false>;
+    using C = Tc<NTOK, true>;
     static std::mutex mu;
     static std::vector<uint32_t> slots;  // per device
     int dev = 0;
@@ -1112,25 +1011,6 @@ cudaError_t launch_w8a8_gemm_tc(const W8A8Args &a, int format, const uint8_t *co
 bool w8a8_streamk_applies(int format, uint32_t rows) {
     const uint32_t ntok = tc_bucket(rows);
     return format == QDL_SCALE_BLOCK128 && ntok >= QDL_STREAMK_MIN_NTOK && ntok <= QDL_STREAMK_MAX_NTOK;
-}
-
-// Block128 projection with the activation quantisation fused in (rows <= 16):
-// a.x is the bf16 input, a.q / a.sa the caller's scratch that tile-0 CTAs fill.
-bool w8a8_fused_fits(uint32_t n, uint32_t kb) {
-    using C = Tc<16, true, true>;
-    const uint32_t tiles = (n + kTileRows - 1) / kTileRows;
-    const uint32_t split = choose_split_k(tiles, kb, cta_slots_tc<16, true, true>(), tc_reduce_cost(16));
-    const uint32_t niter = (kb + split - 1) / split;  // the largest rank's K blocks
-    return niter <= (uint32_t)C::kStages && niter <= (uint32_t)C::kAcc;
-}
-
-cudaError_t launch_w8a8_proj_fused(const W8A8Args &a, const uint8_t *const seg_w[3], const uint32_t seg_n[3],
-                                   cudaStream_t s) {
-    CUtensorMap maps[7];
-    cudaError_t e = weight_maps(a, seg_w, seg_n, maps);
-    if (e != cudaSuccess) return e;
-    maps[6] = maps[0];  // unused: activations are quantised in the kernel
-    return launch_tc_variant<16, true, true>(a, maps, s);
 }
 
 cudaError_t plan_w8a8_gemm_tc(const W8A8Args &a, int format, PlanInfo *p) {

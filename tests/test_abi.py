@@ -200,7 +200,7 @@ def _gemv(lib, d, rows=8, q=DEV + 0x1000000, s=DEV + 0x2000000, qb=1 << 24, sb=1
     (dict(qb=8 * 4096 - 1), SCRATCH, "not available for 8 rows"),
     (dict(sb=8 * 32 * 4 - 1), SCRATCH, "not available"),
     (dict(ldc=6143), INVALID, "ldc=6143 < N=6144"),
-    (dict(dtype=3), INVALID, "output dtype 3"),
+    (dict(dtype=4), INVALID, "output dtype 4"),
     (dict(out=0), INVALID, "output is NULL"),
     (dict(out=DEV + 2), INVALID, "misaligned"),
 ])
@@ -245,7 +245,7 @@ def test_accumulating_output_is_gemv_only(lib):
     d = _weight(lib)
     st = lib.qdl_w8a8_proj(ctypes.byref(d), DEV, 4096, 8, DEV + 0x4000000, qdl.OUT_F32_ADD, 6144,
                            DEV + 0x1000000, DEV + 0x2000000, 1 << 24, 1 << 20, None)
-    assert st == INVALID and "output dtype 2 is not F32 or BF16" in lib.qdl_last_error().decode()
+    assert st == INVALID and "output dtype 2 is not F32, BF16 or F32_DETERMINISTIC" in lib.qdl_last_error().decode()
     st, err = _gemv(lib, d, dtype=qdl.OUT_F32_ADD, ldc=6143)  # fails on ldc, after the dtype check passed
     assert st == INVALID and "ldc=6143" in err, err
 

@@ -329,3 +329,32 @@ def test_full_gateup_every_tile_every_row(rows):
     o = host(out)
     check_close(o[r, c], ys, bs, what=f"gate/up rows={rows}, every tile")
     assert np.all(np.isfinite(o))
+
+
+@pytest.mark.parametrize("name,rows", [("w8a8_block128_qkv_m8_k4096_n4096+1024+1024", 8),
+                                       ("w8a8_block128_qkv_m8_k4096_n4096+1024+1024", 64),
+                                       ("w8a8_block128_gateup_k8192_n14336+14336", 16)])
+def test_deterministic_f32_projection(name, rows):
+    """QDL_OUT_F32_DETERMINISTIC: on shapes where the f32 projection adds
+    split-K partials with atomics (the plan says it accumulates), repeated
+    calls give identical bits and match the oracle"""
+    wl = syn.WORKLOADS[name]
+    segs = _gateup_segments() if wl.k == 8192 else syn.w8a8_weights(wl)
+    w, _keep = upload_weight(segs, wl.fmt)
+    assert qdl.w8a8_plan(w, rows)["proj_accumulates"] == 1
+    xb = syn.bf16_normal((rows, wl.k), seed=rows + 77)
+    x = bf16_dev(xb)
+    q, s = scratch(rows, wl.k, wl.fmt)
+    outs = []
+    for _ in range(3):
+        out = torch.full((rows, wl.n), float("nan"), device="cuda")
+        qdl.w8a8_proj(w, x, rows, out, q, s, out_dtype=qdl.OUT_F32_DETERMINISTIC)
+        outs.append(out)
+    torch.cuda.synchronize()
+    first = host(outs[0])
+    for o in outs[1:]:
+        assert f32_bits_equal(first, host(o)), "deterministic output differs between identical calls"
+    qo, so = oracle.act_quant(wl.fmt, xb, wl.k)
+    r, c = _every_tile_samples(rows, wl.n, seed=rows)
+    ys, bs = oracle.w8a8_gemv_sampled(wl.fmt, qo, so, segs, r, c)
+    check_close(first[r, c], ys, bs, what=f"{name} rows={rows} deterministic")
