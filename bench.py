@@ -31,6 +31,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "quantized decode GEMV µs/call & weight-stream GB/s (% of GB300 HBM roofline)"
+DETERMINISTIC = False  # --deterministic: W8A8 projections with QDL_OUT_F32_DETERMINISTIC output
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM traffic per launch of the dominant kernel from one ncu capture
@@ -170,7 +171,9 @@ class W8A8Case:
         self.launches_per_step = sum(pl["proj_launches"] for pl in plans)
         # the GEMV as the projection runs it: with split K it adds into the
         # zeroed f32 output
-        self.dom_dtypes = [qdl.OUT_F32_ADD if pl["proj_accumulates"] else qdl.OUT_F32 for pl in plans]
+        self.out_dtype = qdl.OUT_F32_DETERMINISTIC if DETERMINISTIC else qdl.OUT_F32
+        self.dom_dtypes = [qdl.OUT_F32_ADD if pl["proj_accumulates"] and not DETERMINISTIC else qdl.OUT_F32
+                           for pl in plans]
         self.kernel = "w8a8_streamk_kernel" if plans[0]["proj_streamk"] else "w8a8_gemm_tc_kernel"
         self.kernel_src = ["w8a8_gemm_tc.cu"]
 
@@ -179,9 +182,9 @@ class W8A8Case:
         wl, k, qdl = self.wl, self.wl.k, self.qdl
         if wl.silu:
             qdl.w8a8_proj_silu(w, self.x[:, :k], self.x[:, k:], self.rows, self.out, self.q, self.s,
-                               ld_gate=2 * k, ld_up=2 * k)
+                               ld_gate=2 * k, ld_up=2 * k, out_dtype=self.out_dtype)
         else:
-            qdl.w8a8_proj(w, self.x, self.rows, self.out, self.q, self.s)
+            qdl.w8a8_proj(w, self.x, self.rows, self.out, self.q, self.s, out_dtype=self.out_dtype)
 
     def dominant(self, i):
         w = self.weights[i % self.copies]
@@ -200,7 +203,7 @@ class W8A8Case:
         wl = self.wl
         return {"workload": wl.name, "rows": self.rows, "k": wl.k, "n_segments": list(wl.segments),
                 "scale_format": "per_row" if wl.fmt == 0 else "block128", "silu_fused": wl.silu,
-                "out_dtype": "f32", "weight_copies": self.copies,
+                "out_dtype": "f32 deterministic" if DETERMINISTIC else "f32", "weight_copies": self.copies,
                 "l2": f"inputs larger than L2: weights rotate over {self.copies} copies "
                       f"({self.copies * self.weight_bytes / 1e6:.0f} MB)"}
 
@@ -671,7 +674,7 @@ def _core_config(wl, rows_list, world):
     c = {"workload": wl.name, "rows": rows_list if len(rows_list) > 1 else rows_list[0]}
     if hasattr(wl, "fmt"):
         c.update(k=wl.k, n_segments=list(wl.segments), scale_format="per_row" if wl.fmt == 0 else "block128",
-                 silu_fused=wl.silu, out_dtype="f32")
+                 silu_fused=wl.silu, out_dtype="f32 deterministic" if DETERMINISTIC else "f32")
     elif hasattr(wl, "nq"):
         c.update(k=wl.k, nq=wl.nq, nkv=wl.nkv, group=wl.group)
     c["parallelism"] = "replicas" if world > 1 else "single"
@@ -927,7 +930,11 @@ def main():
                          "0: time exactly --steps steps once")
     ap.add_argument("--repeats", type=int, default=5, help="timed regions per measurement (median reported)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="W8A8 projections write f32 with the fixed-order split-K reduction")
     args = ap.parse_args()
+    global DETERMINISTIC
+    DETERMINISTIC = args.deterministic
     if args.steps < 1 or args.warmup < 3:
         ap.error("need --steps >= 1 and --warmup >= 3")
     if args.repeats < 1:

@@ -359,7 +359,9 @@ typedef struct {
                                quantiser, then the GEMV (2) */
     uint32_t proj_accumulates; /* 1 when qdl_w8a8_proj with f32 output zeroes out and runs the
                                   GEMV as QDL_OUT_F32_ADD (split K, or the stream-K kernel
-                                  that Block128 takes for 17..128 rows), else 0 */
+                                  that Block128 takes for 17..128 rows), else 0; with its ranks
+                                  adding atomically the GEMV may split K where the plain
+                                  GEMV's plan (split_k) does not (129..256 rows) */
     uint32_t proj_streamk;     /* 1 when that accumulating GEMV is the stream-K kernel (one
                                   contiguous range of (tile, K block) units per CTA), else 0 */
 } qdl_plan;

@@ -58,14 +58,36 @@ __device__ __forceinline__ void dependent_launch_prologue() {
 #endif
 }
 
+// Zero out[0..rows)[0..zn) (row stride zldc) with the whole grid: chunks of 4
+// columns (float4 stores where the rows allow), walked as (row, chunk) pairs
+// from one division per thread.
+__device__ __forceinline__ void zero_rows(const ActQuantArgs &a) {
+    const bool vec = (reinterpret_cast<uintptr_t>(a.zout) % 16 == 0) && a.zldc % 4 == 0;
+    const uint32_t cw = vec ? 4u : 1u;             // columns per chunk
+    const uint32_t cpr = (a.zn + cw - 1) / cw;     // chunks per row
+    const uint32_t nthreads = gridDim.x * blockDim.x, t = blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t dr = nthreads / cpr, dc = nthreads % cpr;
+    uint32_t r = t / cpr, c = t % cpr;
+    while (r < a.rows) {
+        float *row = a.zout + (size_t)r * a.zldc;
+        const uint32_t col = c * cw;
+        if (vec && col + 4 <= a.zn)
+            *reinterpret_cast<float4 *>(row + col) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        else
+            for (uint32_t i = col; i < col + cw && i < a.zn; ++i) row[i] = 0.0f;
+        r += dr;
+        c += dc;
+        if (c >= cpr) {
+            c -= cpr;
+            ++r;
+        }
+    }
+}
+
 template <bool kSilu>
 __global__ void __launch_bounds__(256) act_quant_g128_kernel(ActQuantArgs a) {
     dependent_launch_prologue();
-    if (a.zout != nullptr) {  // the whole grid zeroes the output rows
-        const uint32_t total = a.rows * a.zn, stride = gridDim.x * blockDim.x;
-        for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += stride)
-            a.zout[(size_t)(e / a.zn) * a.zldc + e % a.zn] = 0.0f;
-    }
+    if (a.zout != nullptr) zero_rows(a);  // the whole grid zeroes the output rows
     const uint32_t groups_per_row = a.k / kKUnit;
     const uint32_t gid = blockIdx.x * 8 + (threadIdx.x >> 5);
     const uint32_t lane = threadIdx.x & 31;

@@ -124,9 +124,11 @@ qdl_status launch_gemv(const qdl_w8a8_weight *w, const uint8_t *q, const float *
     return ok();
 }
 
-// split-K factor the tcgen05 GEMV takes for this weight and row count
+// split-K factor the tcgen05 GEMV takes for this weight and row count when
+// its ranks add into a zeroed f32 output (as the projection runs it)
 uint32_t gemv_split(const qdl_w8a8_weight *w, uint32_t rows) {
     W8A8Args a = {};
+    a.accumulate = 1;
     a.n = w->n;
     a.k = w->k;
     a.kb = w->k / kKUnit;

@@ -833,7 +833,12 @@ __global__ void __launch_bounds__(Tc<NTOK, true>::kThreads, 1) __maxnreg__((Tc<N
 
 // Cluster reduction of one split CTA, in K-block units: its partials grow
 // with the token count (measured: one K block of time per 4 tokens).
-constexpr double tc_reduce_cost(int ntok) { return ntok / 4.0; }
+// Where split-K ranks add into a zeroed output with f32 reductions instead,
+// the 256-token ranks cost about 4 blocks: split 2 took the 256-row gate/up
+// GEMV from 123.8 to 103.7 us (1.47 waves of 224 tiles become 2.95).
+constexpr double tc_reduce_cost(int ntok, bool accumulate) {
+    return accumulate && ntok >= 256 ? 4.0 : ntok / 4.0;
+}
 
 template <int NTOK, bool kBlock>
 const uint32_t *cta_slots_tc() {
@@ -859,7 +864,7 @@ template <int NTOK, bool kBlock>
 cudaError_t launch_tc_variant(const W8A8Args &a, const CUtensorMap (&maps)[7], cudaStream_t s) {
     using C = Tc<NTOK, kBlock>;
     const uint32_t tiles = (a.n + kTileRows - 1) / kTileRows;
-    const uint32_t split = choose_split_k(tiles, a.kb, cta_slots_tc<NTOK, kBlock>(), tc_reduce_cost(NTOK));
+    const uint32_t split = choose_split_k(tiles, a.kb, cta_slots_tc<NTOK, kBlock>(), tc_reduce_cost(NTOK, a.accumulate != 0));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tiles, split, 1);
     cfg.blockDim = dim3(C::kThreads, 1, 1);
@@ -899,7 +904,7 @@ void plan_tc_variant(const W8A8Args &a, PlanInfo *p) {
     p->kernel = 0;
     p->mma_n = NTOK;
     p->tiles = (a.n + kTileRows - 1) / kTileRows;
-    p->split = choose_split_k(p->tiles, a.kb, slots, tc_reduce_cost(NTOK));
+    p->split = choose_split_k(p->tiles, a.kb, slots, tc_reduce_cost(NTOK, a.accumulate != 0));
     p->stages = C::kStages;
     p->threads = C::kThreads;
     p->smem = C::kAlloc;

@@ -86,5 +86,10 @@ def test_plan_is_consistent(fmt, n, k, rows):
     assert p["proj_launches"] == 2
     # the f32 projection accumulates when K is split or Block128 runs stream-K
     streamk = fmt == qdl.BLOCK128 and 16 < rows <= 128
-    assert p["proj_accumulates"] == (1 if p["split_k"] > 1 or streamk else 0)
+    # (the 256-token bucket may split K only when its ranks add atomically, so
+    # the projection can accumulate where the plain GEMV's plan has no split)
+    must = p["split_k"] > 1 or streamk
+    assert p["proj_accumulates"] in ((1,) if must else (0, 1))
+    if p["proj_accumulates"] and not must:
+        assert fmt == qdl.BLOCK128 and rows > 128
     assert p["proj_streamk"] == (1 if streamk else 0)
