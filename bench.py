@@ -38,6 +38,24 @@ FALLBACK_HBM_GBS = 6800.0
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and rows;
 # valid only while the kernel source hash matches.  Source: profiles/.
 TRAFFIC = {
+    "w8a8_block128_gateup_k8192_n14336+14336@1": {"bytes": 235104512 + 132608, "file": "w8a8_gemm_tc.cu",
+                                                   "src": "85e25b8d554372c7"},
+    "w8a8_block128_gateup_k8192_n14336+14336@2": {"bytes": 235230976 + 135936, "file": "w8a8_gemm_tc.cu",
+                                                   "src": "85e25b8d554372c7"},
+    "w8a8_block128_gateup_k8192_n14336+14336@4": {"bytes": 235499008 + 129280, "file": "w8a8_gemm_tc.cu",
+                                                   "src": "85e25b8d554372c7"},
+    "w8a8_block128_gateup_k8192_n14336+14336@8": {"bytes": 235991296 + 83712, "file": "w8a8_gemm_tc.cu",
+                                                   "src": "85e25b8d554372c7"},
+    "w8a8_block128_gateup_k8192_n14336+14336@16": {"bytes": 236957440 + 159488, "file": "w8a8_gemm_tc.cu",
+                                                   "src": "85e25b8d554372c7"},
+    "w8a8_block128_gateup_k8192_n14336+14336@32": {"bytes": 241497600 + 1496064, "file": "w8a8_gemm_tc.cu",
+                                                   "src": "85e25b8d554372c7"},
+    "w8a8_block128_gateup_k8192_n14336+14336@64": {"bytes": 241414656 + 2819840, "file": "w8a8_gemm_tc.cu",
+                                                   "src": "85e25b8d554372c7"},
+    "w8a8_block128_gateup_k8192_n14336+14336@128": {"bytes": 246664192 + 5933824, "file": "w8a8_gemm_tc.cu",
+                                                   "src": "85e25b8d554372c7"},
+    "w8a8_block128_gateup_k8192_n14336+14336@256": {"bytes": 266703872 + 5189632, "file": "w8a8_gemm_tc.cu",
+                                                   "src": "85e25b8d554372c7"},
     "int4_awq_qkv_k4096_nq4096_nkv1024_g128@1": {"bytes": 14220800 + 0, "file": "int4_qkv_cc.cu",
                                                  "src": "1918a975bcd9095e"},
     "int4_awq_qkv_k4096_nq4096_nkv1024_g128@4": {"bytes": 14359296 + 0, "file": "int4_qkv_cc.cu",

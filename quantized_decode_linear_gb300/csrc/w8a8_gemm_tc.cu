@@ -61,6 +61,9 @@ namespace cg = cooperative_groups;
 // (7.7 -> 8.0 us).
 #define QDL_TC_EARLY_TRIGGER_BYTES (16ull << 20)
 #endif
+#ifndef QDL_TC_EARLY_MAX_NTOK
+#define QDL_TC_EARLY_MAX_NTOK 16  // token buckets that release their dependents at the start
+#endif
 #ifndef QDL_TC_STAGE_BYTES_16
 // the 16-token variants: 3 stages of 18 KB, so that 4 CTAs share an SM and
 // the next call's early CTAs find free slots while this call streams
@@ -1009,7 +1012,7 @@ cudaError_t launch_w8a8_gemm_tc(const W8A8Args &a, int format, const uint8_t *co
     if (e != cudaSuccess) return e;
     if (a.accumulate && w8a8_streamk_applies(format, a.m)) return launch_streamk_rows(a, maps, ntok, s);
     W8A8Args b = a;
-    b.early_trigger = ntok == 16 && (uint64_t)a.n * a.k >= QDL_TC_EARLY_TRIGGER_BYTES ? 1u : 0u;
+    b.early_trigger = ntok <= QDL_TC_EARLY_MAX_NTOK && (uint64_t)a.n * a.k >= QDL_TC_EARLY_TRIGGER_BYTES ? 1u : 0u;
     return format == QDL_SCALE_BLOCK128 ? launch_tc_rows<true>(b, maps, ntok, s) : launch_tc_rows<false>(b, maps, ntok, s);
 }
 

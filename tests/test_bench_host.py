@@ -36,7 +36,9 @@ def test_traffic_records_are_current_and_near_the_algorithmic_bytes():
         wl = syn.WORKLOADS[name]
         assert rec["src"] == bench._src_hash([rec["file"]]), key
         alg = _algorithmic_bytes(wl, int(rows))
-        assert alg <= rec["bytes"] <= 1.01 * alg, (key, rec["bytes"], alg)
+        # within 3%: ncu empties the caches before a captured launch, so the
+        # outputs that split-K ranks add into atomically are read back from DRAM
+        assert alg <= rec["bytes"] <= 1.03 * alg, (key, rec["bytes"], alg)
 
 
 def test_qkv_algorithmic_bytes():
