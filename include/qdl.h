@@ -176,10 +176,13 @@ QDL_API qdl_status qdl_w8a8_gemv(const qdl_w8a8_weight *w, const uint8_t *q, con
  * weight's format and K, then qdl_w8a8_gemv, on one stream.  q and q_scale
  * are the caller's activation scratch (sizes from qdl_scratch_bytes).
  * rows may exceed 256 (a prefill-shaped call; the page stops at
- * W8A8_MAX_ROWS = 256), up to QDL_MAX_PROJ_ROWS: the call then runs in
- * passes of 256 rows, in order on the stream, each quantising into the same
- * 256-row scratch and streaming the weights once more; pass p covers rows
- * 256p.. of x and out. The scratch needs to hold min(rows, 256) rows.
+ * W8A8_MAX_ROWS = 256), up to QDL_MAX_PROJ_ROWS.  When q_bytes and
+ * scale_bytes hold all rows (rows * k and rows * scales_per_row * 4 bytes),
+ * the rows are quantised into them 256 at a time and one GEMV launch covers
+ * every row, streaming the weights once.  Otherwise the call runs in passes
+ * of 256 rows, in order on the stream, each quantising into the same 256-row
+ * scratch and streaming the weights once more; pass p covers rows 256p.. of
+ * x and out.  The scratch needs to hold min(rows, 256) rows.
  * With f32 output, when the GEMV splits K over several CTAs, the quantiser
  * first sets out[0..rows)[0..N) to zero and the GEMV adds into it
  * (QDL_OUT_F32_ADD): the order of the split-K additions varies, so results

@@ -307,14 +307,37 @@ qdl_status proj_pass(const char *who, const qdl_w8a8_weight *w, const void *x, c
     return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, stream, ~0u, kWaitLimitNs, acc);
 }
 
-// Rows beyond 256 (a prefill-shaped call) in passes of 256 rows, in order on
-// the stream: each pass quantises into the same scratch, which the next
-// pass's quantiser overwrites only after the previous GEMV has finished
-// (programmatic launch orders every library kernel after its predecessor).
+// Rows beyond 256 (a prefill-shaped call).  When the scratch holds every
+// row, the rows are quantised 256 at a time into their own parts of it and
+// one GEMV launch covers them all: its token blocks of one weight tile run
+// side by side, so the weights stream from HBM once.  Otherwise the call runs
+// in passes of 256 rows, in order on the stream: each pass quantises into the
+// same scratch, which the next pass's quantiser overwrites only after the
+// previous GEMV has finished (programmatic launch orders every library kernel
+// after its predecessor), and each pass streams the weights again.
 qdl_status proj_passes(const char *who, const qdl_w8a8_weight *w, const void *x, const void *up, uint32_t ldx, uint32_t ld_up,
                        bool silu, uint32_t rows, void *out, int32_t out_dtype, uint32_t ldc, uint8_t *q, float *q_scale,
-                       void *stream) {
+                       size_t q_bytes, size_t scale_bytes, void *stream) {
     const size_t elt = out_dtype == QDL_OUT_BF16 ? 2 : 4;
+    if (rows > (uint32_t)kMaxRows && fits(q, q_bytes, scale_bytes, rows, w->k, w->format)) {
+        const cudaStream_t s = static_cast<cudaStream_t>(stream);
+        const size_t spr = scales_per_row(w->format, w->k);
+        const bool acc = out_dtype == QDL_OUT_F32 && proj_accumulates(w, rows);
+        for (uint32_t done = 0; done < rows; done += (uint32_t)kMaxRows) {
+            const uint32_t n = rows - done < (uint32_t)kMaxRows ? rows - done : (uint32_t)kMaxRows;
+            ActQuantArgs a = {static_cast<const uint16_t *>(x) + (size_t)done * ldx,
+                              silu ? static_cast<const uint16_t *>(up) + (size_t)done * ld_up : nullptr,
+                              ldx, ld_up, n, w->k, q + (size_t)done * w->k, q_scale + (size_t)done * spr};
+            if (acc) {  // this chunk's quantiser zeroes its rows of the output
+                a.zout = reinterpret_cast<float *>(static_cast<uint8_t *>(out) + (size_t)done * ldc * elt);
+                a.zldc = ldc;
+                a.zn = w->n;
+            }
+            cudaError_t e = launch_act_quant(a, w->format, silu, s);
+            if (e != cudaSuccess) return cuda_fail(who, e);
+        }
+        return launch_gemv(w, q, q_scale, rows, out, out_dtype, ldc, s, ~0u, kWaitLimitNs, acc);
+    }
     for (uint32_t done = 0; done < rows; done += (uint32_t)kMaxRows) {
         const uint32_t n = rows - done < (uint32_t)kMaxRows ? rows - done : (uint32_t)kMaxRows;
         const uint16_t *xp = static_cast<const uint16_t *>(x) + (size_t)done * ldx;
@@ -336,7 +359,8 @@ qdl_status qdl_w8a8_proj(const qdl_w8a8_weight *w, const void *x, uint32_t ldx, 
     if (st != QDL_OK) return st;
     if ((st = check_quant_k(who, w->k)) != QDL_OK) return st;
     if ((st = check_input(who, "x", x, ldx, w->k)) != QDL_OK) return st;
-    return proj_passes(who, w, x, nullptr, ldx, 0, false, rows, out, out_dtype, ldc, q, q_scale, stream);
+    return proj_passes(who, w, x, nullptr, ldx, 0, false, rows, out, out_dtype, ldc, q, q_scale, q_bytes, scale_bytes,
+                       stream);
 }
 
 qdl_status qdl_w8a8_proj_silu(const qdl_w8a8_weight *w, const void *gate, const void *up, uint32_t ld_gate, uint32_t ld_up,
@@ -348,7 +372,8 @@ qdl_status qdl_w8a8_proj_silu(const qdl_w8a8_weight *w, const void *gate, const 
     if ((st = check_quant_k(who, w->k)) != QDL_OK) return st;
     if ((st = check_input(who, "gate", gate, ld_gate, w->k)) != QDL_OK) return st;
     if ((st = check_input(who, "up", up, ld_up, w->k)) != QDL_OK) return st;
-    return proj_passes(who, w, gate, up, ld_gate, ld_up, true, rows, out, out_dtype, ldc, q, q_scale, stream);
+    return proj_passes(who, w, gate, up, ld_gate, ld_up, true, rows, out, out_dtype, ldc, q, q_scale, q_bytes, scale_bytes,
+                       stream);
 }
 
 qdl_status qdl_int4_qkv_gemv(const float *x, uint32_t m, uint32_t k, uint32_t nq, uint32_t nkv, uint32_t group,

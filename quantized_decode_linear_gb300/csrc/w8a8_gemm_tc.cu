@@ -204,7 +204,13 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
     float *red = reinterpret_cast<float *>(smem);  // split-K partials [NTOK][128], reuse the ring at the end
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t tile_row0 = blockIdx.x * kTileRows;
+    // token blocks of NTOK rows (more than one only beyond 256 rows): the
+    // blocks of one weight tile are neighbours in the grid, so they run side by
+    // side and the tile's weights come from HBM once
+    const uint32_t tbs = (a.m + NTOK - 1) / NTOK, tb = blockIdx.x % tbs;
+    const uint32_t tile_row0 = (blockIdx.x / tbs) * kTileRows;
+    const uint32_t tok0 = tb * NTOK;                                             // first token row
+    const uint32_t m_loc = a.m - tok0 < (uint32_t)NTOK ? a.m - tok0 : (uint32_t)NTOK;  // rows of this block
     const uint32_t split = gridDim.y, sidx = blockIdx.y;
     const uint32_t kb0 = (a.kb * sidx) / split, kb1 = (a.kb * (sidx + 1)) / split;
     const uint32_t niter = kb1 - kb0;
@@ -308,8 +314,8 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
             grid_dep_wait();  // activations are written by the previous kernel
             for (uint32_t it = 0; it < head; ++it)
                 if (it != a.debug_skip_iter)
-                    tma_load_2d(smem + it * C::kStage + kWBytes, &tm_a, (int32_t)((kb0 + it) * 128), 0, &full[it],
-                                pol_a);
+                    tma_load_2d(smem + it * C::kStage + kWBytes, &tm_a, (int32_t)((kb0 + it) * 128), (int32_t)tok0,
+                                &full[it], pol_a);
             for (uint32_t it = head; it < niter; ++it) {
                 const uint32_t slot = it % C::kStages, ph = (it / C::kStages) & 1;
                 wait(&empty[slot], ph ^ 1, 1);
@@ -319,7 +325,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
                 if (it == a.debug_skip_iter) continue;
                 uint8_t *st = smem + slot * C::kStage;
                 load_weights(it, st, &full[slot]);
-                tma_load_2d(st + kWBytes, &tm_a, (int32_t)((kb0 + it) * 128), 0, &full[slot], pol_a);
+                tma_load_2d(st + kWBytes, &tm_a, (int32_t)((kb0 + it) * 128), (int32_t)tok0, &full[slot], pol_a);
             }
         }
     } else if (warp == 1) {
@@ -359,8 +365,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
 #pragma unroll
             for (int j = 0; j < kPer; ++j) {
                 const uint32_t tok = 32 * j + lane;
-                v[j] = (it < niter && tok < a.m && tok < (uint32_t)NTOK) ? __ldg(a.sa + (size_t)tok * a.kb + kb) * sw
-                                                                      : 0.0f;
+                v[j] = (it < niter && tok < m_loc) ? __ldg(a.sa + (size_t)(tok0 + tok) * a.kb + kb) * sw : 0.0f;
             }
         };
         float next[kPer];
@@ -441,17 +446,19 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
     // split-K ranks add into the zeroed f32 output (red.global.add.f32)
     // instead of meeting in the cluster reduction
     const bool add_out = a.accumulate && split > 1;
+    // (tok: token row within this block)
     auto add = [&](uint32_t tok, uint32_t r, float v) {
-        if (tok < a.m && r < a.n) atomicAdd(reinterpret_cast<float *>(a.out) + (size_t)tok * a.ldc + r, v);
+        if (tok < m_loc && r < a.n) atomicAdd(reinterpret_cast<float *>(a.out) + (size_t)(tok0 + tok) * a.ldc + r, v);
     };
     auto store = [&](uint32_t tok, uint32_t r, float v) {  // the single writer of (tok, r)
-        if (tok < a.m && r < a.n) {
+        if (tok < m_loc && r < a.n) {
+            const size_t o = (size_t)(tok0 + tok) * a.ldc + r;
             if (a.out_bf16)
-                reinterpret_cast<__nv_bfloat16 *>(a.out)[(size_t)tok * a.ldc + r] = __float2bfloat16_rn(v);
+                reinterpret_cast<__nv_bfloat16 *>(a.out)[o] = __float2bfloat16_rn(v);
             else if (a.accumulate)
-                reinterpret_cast<float *>(a.out)[(size_t)tok * a.ldc + r] += v;
+                reinterpret_cast<float *>(a.out)[o] += v;
             else
-                reinterpret_cast<float *>(a.out)[(size_t)tok * a.ldc + r] = v;
+                reinterpret_cast<float *>(a.out)[o] = v;
         }
     };
 
@@ -495,7 +502,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const uint32_t tok = 16 * c + i;
-                    const float s = tok < a.m ? __ldg(a.sa + tok) * swr : 0.0f;
+                    const float s = tok < m_loc ? __ldg(a.sa + tok0 + tok) * swr : 0.0f;
                     if (split == 1)
                         store(tok, row, v[i] * s);
                     else if (add_out)
@@ -516,7 +523,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
         cluster.sync();
         const uint32_t r_lo = (kTileRows * sidx) / split, r_hi = (kTileRows * (sidx + 1)) / split;
         const uint32_t span = r_hi - r_lo;
-        const uint32_t m_used = a.m < (uint32_t)NTOK ? a.m : (uint32_t)NTOK;
+        const uint32_t m_used = m_loc;
         const float *peer[8];
 #pragma unroll
         for (int rk = 0; rk < 8; ++rk) peer[rk] = cluster.map_shared_rank(red, rk < (int)split ? rk : 0);
@@ -866,7 +873,8 @@ const uint32_t *cta_slots_tc() {
 template <int NTOK, bool kBlock>
 cudaError_t launch_tc_variant(const W8A8Args &a, const CUtensorMap (&maps)[7], cudaStream_t s) {
     using C = Tc<NTOK, kBlock>;
-    const uint32_t tiles = (a.n + kTileRows - 1) / kTileRows;
+    // output tiles x token blocks (more than one block only beyond 256 rows)
+    const uint32_t tiles = (a.n + kTileRows - 1) / kTileRows * ((a.m + NTOK - 1) / NTOK);
     const uint32_t split = choose_split_k(tiles, a.kb, cta_slots_tc<NTOK, kBlock>(), tc_reduce_cost(NTOK, a.accumulate != 0));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tiles, split, 1);
@@ -907,7 +915,7 @@ void plan_tc_variant(const W8A8Args &a, PlanInfo *p) {
     p->kernel = 0;
     p->mma_n = NTOK;
     p->tiles = (a.n + kTileRows - 1) / kTileRows;
-    p->split = choose_split_k(p->tiles, a.kb, slots, tc_reduce_cost(NTOK, a.accumulate != 0));
+    p->split = choose_split_k(p->tiles * ((a.m + NTOK - 1) / NTOK), a.kb, slots, tc_reduce_cost(NTOK, a.accumulate != 0));
     p->stages = C::kStages;
     p->threads = C::kThreads;
     p->smem = C::kAlloc;
@@ -1008,7 +1016,7 @@ cudaError_t launch_w8a8_gemm_tc(const W8A8Args &a, int format, const uint8_t *co
     cudaError_t e = weight_maps(a, seg_w, seg_n, maps);
     if (e != cudaSuccess) return e;
     const uint32_t ntok = tc_bucket(a.m);
-    e = make_tmap_u8(&maps[6], a.q, a.k, a.m, a.k, 128, ntok);
+    e = make_tmap_u8(&maps[6], a.q, a.k, a.m, a.k, 128, ntok < 256 ? ntok : 256);
     if (e != cudaSuccess) return e;
     if (a.accumulate && w8a8_streamk_applies(format, a.m)) return launch_streamk_rows(a, maps, ntok, s);
     W8A8Args b = a;

@@ -358,3 +358,51 @@ def test_deterministic_f32_projection(name, rows):
     r, c = _every_tile_samples(rows, wl.n, seed=rows)
     ys, bs = oracle.w8a8_gemv_sampled(wl.fmt, qo, so, segs, r, c)
     check_close(first[r, c], ys, bs, what=f"{name} rows={rows} deterministic")
+
+
+@pytest.mark.parametrize("fmt", [qdl.PER_ROW, qdl.BLOCK128])
+@pytest.mark.parametrize("rows,dtype", [(257, qdl.OUT_F32), (300, qdl.OUT_BF16), (600, qdl.OUT_F32),
+                                        (513, qdl.OUT_F32_DETERMINISTIC)])
+def test_proj_beyond_256_rows_one_launch(fmt, rows, dtype):
+    """prefill-shaped calls whose scratch holds every row: the rows are
+    quantised 256 at a time and one GEMV launch covers them all (token blocks
+    of 256); ragged last block, row stride beyond K, ldc beyond N; every
+    output against the oracle, columns past N untouched"""
+    k = 512
+    sizes = _aligned_sizes(fmt, [256, 128, 72])
+    segs = _segments(fmt, k, sizes, seed=rows + 1)
+    ldx = k + 16
+    x = syn.bf16_normal((rows, ldx), seed=rows + 9)
+    qo, so = oracle.act_quant(fmt, x, k)
+    yo, bo = oracle.w8a8_gemv(fmt, qo, so, segs)
+    w, _keep = upload_weight(segs, fmt)
+    q, s = scratch(rows, k, fmt)
+    ldc = w.n + 4
+    tdt = torch.bfloat16 if dtype == qdl.OUT_BF16 else torch.float32
+    out = torch.full((rows, ldc), -3.0, device="cuda", dtype=tdt)
+    qdl.w8a8_proj(w, bf16_dev(x), rows, out, q, s, ldx=ldx, ldc=ldc, out_dtype=dtype)
+    torch.cuda.synchronize()
+    o = host(out.float())
+    assert np.all(o[:, w.n:] == -3.0), "columns past N were written"
+    assert np.array_equal(host(q), qo)
+    check_close(o[:, :w.n], yo, bo, extra_rel=BF16_REL if dtype == qdl.OUT_BF16 else 0.0,
+                what=f"fmt={fmt} rows={rows}")
+
+
+def test_full_gateup_512_rows_one_launch():
+    """the gate/up workload at 512 rows through one GEMV launch: every token
+    row of every 128-row tile compared with the oracle"""
+    wl = syn.WORKLOADS["w8a8_block128_gateup_k8192_n14336+14336"]
+    rows = 512
+    segs = _gateup_segments()
+    w, _keep = upload_weight(segs, wl.fmt)
+    xb = syn.bf16_normal((rows, wl.k), seed=512)
+    q, s = scratch(rows, wl.k, wl.fmt)
+    out = torch.empty((rows, wl.n), device="cuda")
+    qdl.w8a8_proj(w, bf16_dev(xb), rows, out, q, s)
+    torch.cuda.synchronize()
+    qo, so = oracle.act_quant(wl.fmt, xb, wl.k)
+    assert np.array_equal(host(q), qo)
+    r, c = _every_tile_samples(rows, wl.n, seed=rows)
+    ys, bs = oracle.w8a8_gemv_sampled(wl.fmt, qo, so, segs, r, c)
+    check_close(host(out)[r, c], ys, bs, what="gate/up rows=512 one launch")
