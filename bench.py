@@ -38,24 +38,6 @@ FALLBACK_HBM_GBS = 6800.0
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and rows;
 # valid only while the kernel source hash matches.  Source: profiles/.
 TRAFFIC = {
-    "w8a8_block128_gateup_k8192_n14336+14336@1": {"bytes": 235103744 + 125440, "file": "w8a8_gemm_tc.cu",
-                                                   "src": "7aaf3309be3a5a51"},
-    "w8a8_block128_gateup_k8192_n14336+14336@2": {"bytes": 235227136 + 54016, "file": "w8a8_gemm_tc.cu",
-                                                   "src": "7aaf3309be3a5a51"},
-    "w8a8_block128_gateup_k8192_n14336+14336@4": {"bytes": 235479296 + 124928, "file": "w8a8_gemm_tc.cu",
-                                                   "src": "7aaf3309be3a5a51"},
-    "w8a8_block128_gateup_k8192_n14336+14336@8": {"bytes": 235968512 + 50432, "file": "w8a8_gemm_tc.cu",
-                                                   "src": "7aaf3309be3a5a51"},
-    "w8a8_block128_gateup_k8192_n14336+14336@16": {"bytes": 236956416 + 337408, "file": "w8a8_gemm_tc.cu",
-                                                   "src": "7aaf3309be3a5a51"},
-    "w8a8_block128_gateup_k8192_n14336+14336@32": {"bytes": 241520896 + 1473792, "file": "w8a8_gemm_tc.cu",
-                                                   "src": "7aaf3309be3a5a51"},
-    "w8a8_block128_gateup_k8192_n14336+14336@64": {"bytes": 241412096 + 2776320, "file": "w8a8_gemm_tc.cu",
-                                                   "src": "7aaf3309be3a5a51"},
-    "w8a8_block128_gateup_k8192_n14336+14336@128": {"bytes": 246671616 + 5936896, "file": "w8a8_gemm_tc.cu",
-                                                   "src": "7aaf3309be3a5a51"},
-    "w8a8_block128_gateup_k8192_n14336+14336@256": {"bytes": 266678016 + 5045760, "file": "w8a8_gemm_tc.cu",
-                                                   "src": "7aaf3309be3a5a51"},
     "int4_awq_qkv_k4096_nq4096_nkv1024_g128@1": {"bytes": 14220800 + 0, "file": "int4_qkv_cc.cu",
                                                  "src": "1918a975bcd9095e"},
     "int4_awq_qkv_k4096_nq4096_nkv1024_g128@4": {"bytes": 14359296 + 0, "file": "int4_qkv_cc.cu",

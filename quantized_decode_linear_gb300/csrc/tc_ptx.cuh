@@ -61,6 +61,43 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 lanes x 8R columns in the 16x256b shape (the m16n8 accumulator-fragment
+// layout): registers 4j, 4j+1 hold lane (base + t/4), columns 8j + 2(t%4) and
+// 8j + 2(t%4) + 1; registers 4j+2, 4j+3 the same columns of lane base + 8 + t/4
+// (t = thread in warp).  A thread thus holds 4 rows x 2 columns of every
+// 16-lane x 8-column chunk, instead of one row x 8 columns in the 32x32b shape.
+template <int R>
+__device__ __forceinline__ void tc_ld_16x256b(uint32_t taddr, float (&v)[4 * R]);
+
+template <>
+__device__ __forceinline__ void tc_ld_16x256b<2>(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <>
+__device__ __forceinline__ void tc_ld_16x256b<4>(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <>
+__device__ __forceinline__ void tc_ld_16x256b<8>(uint32_t taddr, float (&v)[32]) {
+    float *lo = v, *hi = v + 16;
+    tc_ld_16x256b<4>(taddr, *reinterpret_cast<float(*)[16]>(lo));
+    tc_ld_16x256b<4>(taddr + 32, *reinterpret_cast<float(*)[16]>(hi));  // x4 spans 32 columns
+}
+
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_alloc(uint32_t *slot, uint32_t cols) {

@@ -117,6 +117,18 @@ namespace cg = cooperative_groups;
 #ifndef QDL_TC_REGS_32
 #define QDL_TC_REGS_32 96  // 3 CTAs of 7 warps
 #endif
+#ifndef QDL_TC_EPI_256
+#define QDL_TC_EPI_256 16  // epilogue warps of the 256-token Block128 variant
+#endif
+#ifndef QDL_TC_REGS_256
+#define QDL_TC_REGS_256 104  // one CTA of 19 warps: all the registers it can have
+#endif
+#ifndef QDL_TC_FFMA2
+#define QDL_TC_FFMA2 1
+#endif
+#ifndef QDL_TC_FRAG_MIN_NTOK
+#define QDL_TC_FRAG_MIN_NTOK 128
+#endif
 #ifndef QDL_TC_BIGBOX
 #define QDL_TC_BIGBOX 1
 #endif
@@ -153,11 +165,23 @@ struct Tc {
     // the epilogue that folds each block's scales
     static constexpr int kAcc = kBlock ? (NTOK <= 64 ? 4 : 2) : 1;
     static constexpr uint32_t kBarOff = kStages * kStage;
-    static constexpr uint32_t kScaleOff = kBarOff + 512;  // Block128: [kAcc][NTOK] block scales
-    static constexpr uint32_t kBytes = kScaleOff + (kBlock ? kAcc * NTOK * 4 : 0);
+    static constexpr uint32_t kScaleOff = kBarOff + 512;  // Block128: [kAcc][kSBuf] block scales
+    // Block128 epilogue fragments: 16x256b (a thread holds 4 rows x 2 token
+    // columns per 8 columns) for NTOK >= QDL_TC_FRAG_MIN_NTOK, else 32x32b (one
+    // row x every column).  The 16-lane shape reads tensor memory at about half
+    // the rate (measured ~250 against >= 400 B/clk per SM) but needs a quarter
+    // of the scale broadcasts, which pays only for wide token blocks.
+    static constexpr bool kFrag = kBlock && NTOK >= QDL_TC_FRAG_MIN_NTOK;
+    // Scales of one accumulator buffer in the order the fragments use them:
+    // 32x32b, token t at [t]; 16x256b, token t at [(t % 8) / 2][2 (t / 8) + t % 2],
+    // four rows of kSRow floats (padded by 16 bytes so that the four rows the
+    // lanes of a quarter-warp read fall in different banks)
+    static constexpr uint32_t kSRow = kFrag ? NTOK / 4 + 4 : NTOK;
+    static constexpr uint32_t kSBuf = kFrag ? 4 * kSRow : NTOK;
+    static constexpr uint32_t kBytes = kScaleOff + (kBlock ? kAcc * kSBuf * 4 : 0);
     static constexpr uint32_t kAlloc = kBytes + 1024;
     static constexpr int kEpiBase = kBlock ? 3 : 2;                          // first epilogue warp
-    static constexpr int kEpi = kBlock ? (NTOK <= 64 ? 4 : NTOK / 16) : 4;  // epilogue warps
+    static constexpr int kEpi = kBlock ? (NTOK <= 64 ? 4 : NTOK == 256 ? QDL_TC_EPI_256 : NTOK / 16) : 4;  // epilogue warps
     static constexpr int kCpt = kBlock ? NTOK * 4 / kEpi : 16;               // columns per epilogue thread
     static constexpr int kThreads = (kEpiBase + kEpi) * 32;
     // columns per tensor-memory wait in the Block128 epilogue
@@ -169,7 +193,7 @@ struct Tc {
     // (the 64-token Block128 variants run one CTA per SM with their deep ring,
     // so they take all the registers they need: a cap of 144 spilled, and
     // lifting it took the gate/up projection at M = 64 from 59.3 to 54.9 us)
-    static constexpr int kMaxRegs = !kBlock ? 255 : NTOK == 32 ? QDL_TC_REGS_32 : 255;
+    static constexpr int kMaxRegs = !kBlock ? 255 : NTOK == 32 ? QDL_TC_REGS_32 : NTOK == 256 ? QDL_TC_REGS_256 : 255;
     static constexpr uint32_t kTmemCols = pow2_at_least(kAcc * NTOK);
     static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
     static_assert(kTileRows * NTOK * 4 <= kBarOff, "split-K partials must fit in the stage ring");
@@ -180,6 +204,94 @@ struct Tc {
 };
 
 // ---------------------------------------------------------------- kernel helpers
+
+// Block128 epilogue layout.  Epilogue warp e reads tensor-memory lanes
+// 32 (warp % 4) .. +31 (weight rows) and token columns kCpt (e / 4) .. +kCpt-1.
+// A thread's total j is the accumulator of
+//   32x32b : token kCpt (e / 4) + j, row 32 (warp % 4) + lane
+//   16x256b: token kCpt (e / 4) + 8 (j / 8) + 2 (lane % 4) + j % 2,
+//            row   32 (warp % 4) + 16 ((j / 4) % 2) + 8 ((j / 2) % 2) + lane / 4
+template <bool kFrag>
+__device__ __forceinline__ uint32_t frag_tok(int j, uint32_t lane) {
+    return kFrag ? 8u * (uint32_t)(j >> 3) + 2u * (lane & 3u) + (uint32_t)(j & 1) : (uint32_t)j;
+}
+template <bool kFrag>
+__device__ __forceinline__ uint32_t frag_row(int j, uint32_t lane) {
+    return kFrag ? 16u * (uint32_t)((j >> 2) & 1) + 8u * (uint32_t)((j >> 1) & 1) + (lane >> 2) : lane;
+}
+// position of token t's scale in one accumulator buffer's scale block
+template <int NTOK>
+__device__ __forceinline__ uint32_t scale_slot(uint32_t t) {
+    using C = Tc<NTOK, true>;
+    return C::kFrag ? ((t & 7u) >> 1) * C::kSRow + 2u * (t >> 3) + (t & 1u) : t;
+}
+// this thread's first scale in a buffer (epilogue column group cgrp)
+template <int NTOK>
+__device__ __forceinline__ uint32_t scale_row(uint32_t cgrp, uint32_t lane) {
+    using C = Tc<NTOK, true>;
+    return C::kFrag ? (lane & 3u) * C::kSRow + cgrp * C::kCpt / 4 : cgrp * C::kCpt;
+}
+
+// total[j, j+1] += (v0, v1) * (s0, s1) as one packed f32x2 FMA (each half
+// rounded as the scalar fmaf would be)
+__device__ __forceinline__ void fma_pair(float &t0, float &t1, float v0, float v1, float s0, float s1) {
+#if QDL_TC_FFMA2
+    const float2 r = __ffma2_rn(make_float2(v0, v1), make_float2(s0, s1), make_float2(t0, t1));
+    t0 = r.x;
+    t1 = r.y;
+#else
+    t0 = fmaf(v0, s0, t0);
+    t1 = fmaf(v1, s1, t1);
+#endif
+}
+
+// Fold the finished accumulator buffer at tensor-memory column `col_b` into
+// the totals: total[j] += D[row(j), tok(j)] * s[tok(j)], with `sq` this
+// thread's first scale (scale_row).
+template <int NTOK>
+__device__ __forceinline__ void fold_block(uint32_t taddr, uint32_t col_b, const float *sq,
+                                           float (&total)[Tc<NTOK, true>::kCpt]) {
+    using C = Tc<NTOK, true>;
+    constexpr int kCpt = C::kCpt, kF = C::kInFlight;
+#pragma unroll
+    for (int g = 0; g < kCpt / kF; ++g) {
+        if constexpr (C::kFrag) {
+            float va[kF / 2], vb[kF / 2];  // lanes +0..15 and +16..31 of the warp's 32
+            tc_ld_16x256b<kF / 8>(taddr + col_b + kF * g, va);
+            tc_ld_16x256b<kF / 8>(taddr + (16u << 16) + col_b + kF * g, vb);
+            tc_wait_ld();
+            const float4 *sp = reinterpret_cast<const float4 *>(sq + kF / 4 * g);
+#pragma unroll
+            for (int q4 = 0; q4 < kF / 16; ++q4) {
+                const float4 s4 = sp[q4];  // the scales of two 8-column chunks
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int j = 2 * q4 + h;  // chunk within the group
+                    const float se = h ? s4.z : s4.x, so = h ? s4.w : s4.y;
+                    float *t = total + kF * g + 8 * j;
+                    fma_pair(t[0], t[1], va[4 * j + 0], va[4 * j + 1], se, so);
+                    fma_pair(t[2], t[3], va[4 * j + 2], va[4 * j + 3], se, so);
+                    fma_pair(t[4], t[5], vb[4 * j + 0], vb[4 * j + 1], se, so);
+                    fma_pair(t[6], t[7], vb[4 * j + 2], vb[4 * j + 3], se, so);
+                }
+            }
+        } else {
+            float v[kF];
+#pragma unroll
+            for (int c = 0; c < kF / 16; ++c)
+                tc_ld16(taddr + col_b + kF * g + 16 * c, *reinterpret_cast<float(*)[16]>(v + 16 * c));
+            tc_wait_ld();
+            const float4 *sp = reinterpret_cast<const float4 *>(sq + kF * g);
+#pragma unroll
+            for (int q4 = 0; q4 < kF / 4; ++q4) {
+                const float4 s4 = sp[q4];  // the same address in every lane: a broadcast
+                float *t = total + kF * g + 4 * q4;
+                fma_pair(t[0], t[1], v[4 * q4 + 0], v[4 * q4 + 1], s4.x, s4.y);
+                fma_pair(t[2], t[3], v[4 * q4 + 2], v[4 * q4 + 3], s4.z, s4.w);
+            }
+        }
+    }
+}
 
 // ---------------------------------------------------------------- kernel
 
@@ -200,7 +312,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
     uint64_t *done = scal + C::kAcc;      // all MMAs complete
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     volatile uint32_t *abort_flag = tmem_slot + 1;
-    float *sbuf = reinterpret_cast<float *>(smem + C::kScaleOff);  // Block128: [kAcc][NTOK] sa * sw
+    float *sbuf = reinterpret_cast<float *>(smem + C::kScaleOff);  // Block128: [kAcc][kSBuf] sa * sw
     float *red = reinterpret_cast<float *>(smem);  // split-K partials [NTOK][128], reuse the ring at the end
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -379,7 +491,8 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
             wait(&acce[b], ((it / C::kAcc) & 1) ^ 1, 64);  // the epilogue is done with sbuf[b]
 #pragma unroll
             for (int j = 0; j < kPer; ++j)
-                if (32 * j + lane < (uint32_t)NTOK) sbuf[b * NTOK + 32 * j + lane] = cur[j];
+                if (32 * j + lane < (uint32_t)NTOK)
+                    sbuf[b * C::kSBuf + scale_slot<NTOK>(32 * j + lane)] = cur[j];
             __syncwarp();
             if (lane == 0) mbar_arrive(&scal[b]);
         }
@@ -391,33 +504,13 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
         const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16);
         grid_dep_wait();  // activation scales come from the previous kernel
         if constexpr (kBlock) {
+            const uint32_t sq = scale_row<NTOK>(cgrp, lane);
             for (uint32_t it = 0; it < niter; ++it) {
                 const uint32_t b = it % C::kAcc;
                 wait(&scal[b], (it / C::kAcc) & 1, 32);  // sa * sw of this block
                 wait(&accf[b], (it / C::kAcc) & 1, 16);
                 tc_fence_after();
-                // kInFlight columns per wait: several loads in flight hide the
-                // tensor-memory latency
-                constexpr int kF = C::kInFlight;
-#pragma unroll
-                for (int g = 0; g < kCpt / kF; ++g) {
-                    float v[kF];
-                    const uint32_t col = cgrp * kCpt + kF * g;
-#pragma unroll
-                    for (int c = 0; c < kF / 16; ++c)
-                        tc_ld16(taddr + b * NTOK + col + 16 * c, *reinterpret_cast<float(*)[16]>(v + 16 * c));
-                    tc_wait_ld();
-                    const float4 *sp = reinterpret_cast<const float4 *>(sbuf + b * NTOK + col);
-#pragma unroll
-                    for (int q4 = 0; q4 < kF / 4; ++q4) {
-                        const float4 s4 = sp[q4];  // the same address in every lane: a broadcast
-                        float *t = total + kF * g + 4 * q4;
-                        t[0] = fmaf(v[4 * q4 + 0], s4.x, t[0]);
-                        t[1] = fmaf(v[4 * q4 + 1], s4.y, t[1]);
-                        t[2] = fmaf(v[4 * q4 + 2], s4.z, t[2]);
-                        t[3] = fmaf(v[4 * q4 + 3], s4.w, t[3]);
-                    }
-                }
+                fold_block<NTOK>(taddr, b * NTOK + cgrp * kCpt, sbuf + b * C::kSBuf + sq, total);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acce[b]);
@@ -474,13 +567,14 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
         if constexpr (kBlock) {
 #pragma unroll
             for (int j = 0; j < kCpt; ++j) {
-                const uint32_t tok = cgrp * kCpt + j;
+                const uint32_t tok = cgrp * kCpt + frag_tok<C::kFrag>(j, lane);
+                const uint32_t jrow = 32 * quad + frag_row<C::kFrag>(j, lane);
                 if (split == 1)
-                    store(tok, row, total[j]);
+                    store(tok, tile_row0 + jrow, total[j]);
                 else if (add_out)
-                    add(tok, row, total[j]);
+                    add(tok, tile_row0 + jrow, total[j]);
                 else
-                    red[tok * kTileRows + lrow] = total[j];
+                    red[tok * kTileRows + jrow] = total[j];
             }
         } else {
             // PerRow: scale the accumulator by sa[token] sw[row], 16 columns at a time
@@ -749,7 +843,8 @@ __global__ void __launch_bounds__(Tc<NTOK, true>::kThreads, 1) __maxnreg__((Tc<N
             wait(&acce[b], ((it / C::kAcc) & 1) ^ 1, 64);
 #pragma unroll
             for (int j = 0; j < kPer; ++j)
-                if (32 * j + lane < (uint32_t)NTOK) sbuf[b * NTOK + 32 * j + lane] = cur[j];
+                if (32 * j + lane < (uint32_t)NTOK)
+                    sbuf[b * C::kSBuf + scale_slot<NTOK>(32 * j + lane)] = cur[j];
             __syncwarp();
             if (lane == 0) mbar_arrive(&scal[b]);
         }
@@ -759,33 +854,14 @@ __global__ void __launch_bounds__(Tc<NTOK, true>::kThreads, 1) __maxnreg__((Tc<N
         const int quad = warp & 3;
         const int cgrp = e >> 2;
         const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16);
-        const uint32_t lrow = 32 * quad + lane;
+        const uint32_t sq = scale_row<NTOK>(cgrp, lane);
         grid_dep_wait();  // scales come from, and the output is shared with, earlier kernels
         for (uint32_t it = 0; it < niter; ++it) {
             const uint32_t b = it % C::kAcc;
             wait(&scal[b], (it / C::kAcc) & 1, 32);
             wait(&accf[b], (it / C::kAcc) & 1, 16);
             tc_fence_after();
-            constexpr int kF = C::kInFlight;
-#pragma unroll
-            for (int g = 0; g < kCpt / kF; ++g) {
-                float v[kF];
-                const uint32_t col = cgrp * kCpt + kF * g;
-#pragma unroll
-                for (int c = 0; c < kF / 16; ++c)
-                    tc_ld16(taddr + b * NTOK + col + 16 * c, *reinterpret_cast<float(*)[16]>(v + 16 * c));
-                tc_wait_ld();
-                const float4 *sp = reinterpret_cast<const float4 *>(sbuf + b * NTOK + col);
-#pragma unroll
-                for (int q4 = 0; q4 < kF / 4; ++q4) {
-                    const float4 s4 = sp[q4];
-                    float *t = total + kF * g + 4 * q4;
-                    t[0] = fmaf(v[4 * q4 + 0], s4.x, t[0]);
-                    t[1] = fmaf(v[4 * q4 + 1], s4.y, t[1]);
-                    t[2] = fmaf(v[4 * q4 + 2], s4.z, t[2]);
-                    t[3] = fmaf(v[4 * q4 + 3], s4.w, t[3]);
-                }
-            }
+            fold_block<NTOK>(taddr, b * NTOK + cgrp * kCpt, sbuf + b * C::kSBuf + sq, total);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acce[b]);
@@ -795,21 +871,31 @@ __global__ void __launch_bounds__(Tc<NTOK, true>::kThreads, 1) __maxnreg__((Tc<N
             if (it + 1 == niter || (u + 1) % a.kb == 0) {
                 const uint32_t tile = u / a.kb;
                 const bool whole = tile * a.kb >= u0 && (tile + 1) * a.kb <= u1;
-                const uint32_t row = tile * kTileRows + lrow;
-                if (row < a.n && !*abort_flag) {
-                    float *orow = reinterpret_cast<float *>(a.out) + row + (size_t)(cgrp * kCpt) * a.ldc;
-                    const uint32_t nt = a.m > (uint32_t)(cgrp * kCpt) ? a.m - cgrp * kCpt : 0u;  // valid tokens here
+                if (!*abort_flag) {
+                    // this thread's first output (total 0) and how many tokens
+                    // and rows from it exist; total j lies frag_tok(j) - frag_tok(0)
+                    // tokens and frag_row(j) - frag_row(0) rows further on
+                    const uint32_t tok0 = cgrp * kCpt + frag_tok<C::kFrag>(0, lane);
+                    const uint32_t row0 = tile * kTileRows + 32 * quad + frag_row<C::kFrag>(0, lane);
+                    const int nt = (int)a.m - (int)tok0, nr = (int)a.n - (int)row0;
+                    float *o0 = reinterpret_cast<float *>(a.out) + (size_t)tok0 * a.ldc + row0;
                     // a tile this CTA covers whole over a zeroed output is stored; any
                     // other (shared, or QDL_OUT_F32_ADD) is added with reductions, which
                     // for a single writer is one exact add per element
                     if (whole && a.out_zeroed) {
 #pragma unroll
-                        for (int j = 0; j < kCpt; ++j)
-                            if ((uint32_t)j < nt) orow[(size_t)j * a.ldc] = total[j];
+                        for (int j = 0; j < kCpt; ++j) {
+                            const int dt = (int)(frag_tok<C::kFrag>(j, lane) - frag_tok<C::kFrag>(0, lane));
+                            const int dr = (int)(frag_row<C::kFrag>(j, lane) - frag_row<C::kFrag>(0, lane));
+                            if (dt < nt && dr < nr) o0[(size_t)dt * a.ldc + dr] = total[j];
+                        }
                     } else {
 #pragma unroll
-                        for (int j = 0; j < kCpt; ++j)
-                            if ((uint32_t)j < nt) atomicAdd(orow + (size_t)j * a.ldc, total[j]);
+                        for (int j = 0; j < kCpt; ++j) {
+                            const int dt = (int)(frag_tok<C::kFrag>(j, lane) - frag_tok<C::kFrag>(0, lane));
+                            const int dr = (int)(frag_row<C::kFrag>(j, lane) - frag_row<C::kFrag>(0, lane));
+                            if (dt < nt && dr < nr) atomicAdd(o0 + (size_t)dt * a.ldc + dr, total[j]);
+                        }
                     }
                 }
 #pragma unroll
