@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kThreadsI4, 1)
             if (i < items && tok < m_used) {
                 const uint32_t ku = (v0 + u) % upt;
                 const float4 *xp = reinterpret_cast<const float4 *>(a.x + (size_t)tok * a.k + ku * kUnitK + 8 * c);
-                const float4 p0 = __ldg(xp), p1 = __ldg(xp + 1);
+                const float4 p0 = ld_dep(xp), p1 = ld_dep(xp + 1);
                 h = make_uint4(h2_bits(p0.x, p0.y), h2_bits(p0.z, p0.w), h2_bits(p1.x, p1.y), h2_bits(p1.z, p1.w));
                 const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&h.x));
                 const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&h.y));

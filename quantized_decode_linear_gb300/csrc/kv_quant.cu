@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(kKvThreads) kv_quant_int8_kernel(const float *
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
             const uint32_t t = t0 + i, ch = lane + 32 * c;
-            v[i][c] = (t < tokens && ch < chunks) ? __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * dim) + ch)
+            v[i][c] = (t < tokens && ch < chunks) ? ld_dep(reinterpret_cast<const float4 *>(x + (size_t)t * dim) + ch)
                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kKvThreads) kv_quant_int8_wide_kernel(const fl
     const float4 *row = reinterpret_cast<const float4 *>(x + (size_t)t * dim);
     float m = 0.0f;
     for (uint32_t ch = lane; ch < chunks; ch += 32) {
-        const float4 v = __ldg(row + ch);
+        const float4 v = ld_dep(row + ch);
         m = fmaxf(fmaxf(fmaxf(m, fabsf(v.x)), fmaxf(fabsf(v.y), fabsf(v.z))), fabsf(v.w));
     }
 #pragma unroll
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kKvThreads) kv_quant_int8_wide_kernel(const fl
     const float s = kv_scale_int8(m);
     if (lane == 0) scale[t] = s;
     for (uint32_t ch = lane; ch < chunks; ch += 32) {
-        const float4 v = __ldg(row + ch);
+        const float4 v = ld_dep(row + ch);
         q[(size_t)t * chunks + ch] = q_int8(v.x, s) | (q_int8(v.y, s) << 8) | (q_int8(v.z, s) << 16) | (q_int8(v.w, s) << 24);
     }
 }
@@ -128,8 +128,8 @@ __global__ void __launch_bounds__(kKvThreads) kv_dequant_int8_kernel(const uint3
     const uint32_t wpt = dim / 4;  // words per token
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < words; i += stride) {
-        const uint32_t w = __ldg(q + i);
-        const float s = __ldg(scale + i / wpt);
+        const uint32_t w = ld_dep(q + i);
+        const float s = ld_dep(scale + i / wpt);
         float4 o;
         o.x = __fmul_rn((float)(int8_t)(w & 0xFF), s);
         o.y = __fmul_rn((float)(int8_t)((w >> 8) & 0xFF), s);
@@ -188,8 +188,8 @@ __global__ void __launch_bounds__(kKvThreads) kv_quant_int4_kernel(const float *
         const uint32_t g = (warp * kRounds + r) * kGpw + lane / L;
         const float4 *p = reinterpret_cast<const float4 *>(x + (size_t)g * kGroup + 8 * chunk);
         const bool ok = g < groups;
-        v[r][0] = ok ? __ldg(p) : make_float4(0.f, 0.f, 0.f, 0.f);
-        v[r][1] = ok ? __ldg(p + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[r][0] = ok ? ld_dep(p) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[r][1] = ok ? ld_dep(p + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int r = 0; r < kRounds; ++r) {
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kKvThreads) kv_quant_int4_wide_kernel(const fl
     float mn = __int_as_float(0x7f800000), mx = -__int_as_float(0x7f800000);
     for (uint32_t c = lane; c < chunks; c += 32) {
         float a, b;
-        minmax8(__ldg(p + 2 * c), __ldg(p + 2 * c + 1), a, b);
+        minmax8(ld_dep(p + 2 * c), ld_dep(p + 2 * c + 1), a, b);
         mn = fminf(mn, a);
         mx = fmaxf(mx, b);
     }
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(kKvThreads) kv_quant_int4_wide_kernel(const fl
         zero[g] = f.zero;
     }
     for (uint32_t c = lane; c < chunks; c += 32)
-        packed[(size_t)g * chunks + c] = pack_int4(__ldg(p + 2 * c), __ldg(p + 2 * c + 1), f);
+        packed[(size_t)g * chunks + c] = pack_int4(ld_dep(p + 2 * c), ld_dep(p + 2 * c + 1), f);
 }
 
 // v' = q scale - zero scale, eight values (one code word) per thread and step
@@ -251,9 +251,9 @@ __global__ void __launch_bounds__(kKvThreads) kv_dequant_int4_kernel(const uint3
     const uint32_t wpg = group / 8;  // words per group
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < words; i += stride) {
-        const uint32_t w = __ldg(packed + i);
+        const uint32_t w = ld_dep(packed + i);
         const size_t g = i / wpg;
-        const float s = __ldg(scale + g), zs = __fmul_rn(__ldg(zero + g), s);
+        const float s = ld_dep(scale + g), zs = __fmul_rn(ld_dep(zero + g), s);
         float o[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) o[j] = __fsub_rn(__fmul_rn((float)((w >> (4 * j)) & 0xFu), s), zs);

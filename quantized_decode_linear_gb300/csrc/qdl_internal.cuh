@@ -190,6 +190,42 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
     return __fmul_rn(s, u);
 }
 
+// Loads of data that an earlier kernel on the stream writes (activations,
+// activation scales, KV values and codes, weights being quantised).  The
+// kernels are launched with programmatic stream serialisation, so they may
+// start while that kernel still runs and read such data only after
+// griddepcontrol.wait.  A non-coherent load (ld.global.nc, __ldg) is valid only
+// for data that no kernel writes while this one runs, and the compiler may
+// schedule it before the wait; these are plain coherent loads, in volatile asm
+// so that they stay after the wait.
+__device__ __forceinline__ float ld_dep(const float *p) {
+    float v;
+    asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 ld_dep(const float4 *p) {
+    float4 v;
+    asm volatile("ld.global.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ uint4 ld_dep(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ uint2 ld_dep(const uint2 *p) {
+    uint2 v;
+    asm volatile("ld.global.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_dep(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Streaming 16-byte load of data read exactly once (weights): bypass L1 and
 // mark the lines evict-first in L2 so activations and scales stay resident.
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p, uint64_t policy) {

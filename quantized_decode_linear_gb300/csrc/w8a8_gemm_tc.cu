@@ -361,6 +361,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
         if (!*abort_flag && !mbar_wait(bar, parity, a.wait_limit_ns)) fault(code);
     };
 
+
     // segment of this tile's first row (Block128 tiles never straddle segments)
     const float *tile_scale;
     const CUtensorMap *tile_big;
@@ -477,7 +478,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
 #pragma unroll
             for (int j = 0; j < kPer; ++j) {
                 const uint32_t tok = 32 * j + lane;
-                v[j] = (it < niter && tok < m_loc) ? __ldg(a.sa + (size_t)(tok0 + tok) * a.kb + kb) * sw : 0.0f;
+                v[j] = (it < niter && tok < m_loc) ? ld_dep(a.sa + (size_t)(tok0 + tok) * a.kb + kb) * sw : 0.0f;
             }
         };
         float next[kPer];
@@ -596,7 +597,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const uint32_t tok = 16 * c + i;
-                    const float s = tok < m_loc ? __ldg(a.sa + tok0 + tok) * swr : 0.0f;
+                    const float s = tok < m_loc ? ld_dep(a.sa + tok0 + tok) * swr : 0.0f;
                     if (split == 1)
                         store(tok, row, v[i] * s);
                     else if (add_out)
@@ -713,6 +714,7 @@ __global__ void __launch_bounds__(Tc<NTOK, true>::kThreads, 1) __maxnreg__((Tc<N
     auto wait = [&](uint64_t *bar, uint32_t parity, uint32_t code) {
         if (!*abort_flag && !mbar_wait(bar, parity, a.wait_limit_ns)) fault(code);
     };
+
     // segment of a tile (Block128 tiles never straddle segments)
     struct TileSeg {
         const float *scale;
@@ -828,7 +830,7 @@ __global__ void __launch_bounds__(Tc<NTOK, true>::kThreads, 1) __maxnreg__((Tc<N
 #pragma unroll
             for (int j = 0; j < kPer; ++j) {
                 const uint32_t tok = 32 * j + lane;
-                v[j] = (it < niter && tok < a.m && tok < (uint32_t)NTOK) ? __ldg(a.sa + (size_t)tok * a.kb + kb) * sw
+                v[j] = (it < niter && tok < a.m && tok < (uint32_t)NTOK) ? ld_dep(a.sa + (size_t)tok * a.kb + kb) * sw
                                                                       : 0.0f;
             }
         };

@@ -30,7 +30,7 @@ constexpr int kChunks = 4;  // 8-value chunks a thread keeps in registers
 template <bool kBf16>
 __device__ __forceinline__ void load8(const void *base, size_t elem, float (&v)[8]) {
     if (kBf16) {
-        const uint4 r = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + elem));
+        const uint4 r = ld_dep(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + elem));
         const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -39,7 +39,7 @@ __device__ __forceinline__ void load8(const void *base, size_t elem, float (&v)[
         }
     } else {
         const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(base) + elem);
-        const float4 a = __ldg(p), b = __ldg(p + 1);
+        const float4 a = ld_dep(p), b = ld_dep(p + 1);
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
         v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     }
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(256) awq_pack_kernel(const uint8_t *nib, uint3
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += stride) {
         // word i = row i / words, word i % words: bytes 8 i .. 8 i + 7 of nib
-        const uint2 b = __ldg(reinterpret_cast<const uint2 *>(nib + 8 * i));
+        const uint2 b = ld_dep(reinterpret_cast<const uint2 *>(nib + 8 * i));
         constexpr int kShift[8] = {0, 16, 4, 20, 8, 24, 12, 28};
         uint32_t word = 0;
 #pragma unroll

@@ -251,6 +251,30 @@ def test_full_block128_gateup_sweep():
 
 
 @pytest.mark.parametrize("fmt", [qdl.PER_ROW, qdl.BLOCK128])
+@pytest.mark.parametrize("rows", [8, 64, 256])
+def test_back_to_back_calls_share_the_scratch(fmt, rows):
+    """three projections queued with no host wait, each quantising into the
+    same scratch that the previous call's GEMV reads: every GEMV must read
+    its own call's codes and scales, never the previous call's (the kernels
+    overlap under programmatic launch, so a scale read scheduled before the
+    dependency wait would see the stale values)"""
+    k = 512
+    sizes = _aligned_sizes(fmt, [256, 128, 72])
+    segs = _segments(fmt, k, sizes, seed=rows + 40)
+    w, _keep = upload_weight(segs, fmt)
+    q, s = scratch(rows, k, fmt)
+    xs = [syn.bf16_normal((rows, k), seed=rows + 50 + i) for i in range(3)]
+    outs = [torch.full((rows, w.n), float("nan"), device="cuda") for _ in xs]
+    for x, out in zip(xs, outs):
+        qdl.w8a8_proj(w, bf16_dev(x), rows, out, q, s)
+    torch.cuda.synchronize()
+    for i, (x, out) in enumerate(zip(xs, outs)):
+        qo, so = oracle.act_quant(fmt, x, k)
+        yo, bo = oracle.w8a8_gemv(fmt, qo, so, segs)
+        check_close(host(out), yo, bo, what=f"fmt={fmt} rows={rows} call {i}")
+
+
+@pytest.mark.parametrize("fmt", [qdl.PER_ROW, qdl.BLOCK128])
 @pytest.mark.parametrize("rows", [257, 300, 600])
 def test_proj_beyond_256_rows(fmt, rows):
     """prefill-shaped calls: passes of 256 rows through one 256-row scratch,
