@@ -123,6 +123,15 @@ namespace cg = cooperative_groups;
 #ifndef QDL_TC_REGS_256
 #define QDL_TC_REGS_256 104  // one CTA of 19 warps: all the registers it can have
 #endif
+#ifndef QDL_TC_ACC_128
+#define QDL_TC_ACC_128 4  // accumulator buffers of the 128-token Block128 variants
+#endif
+#ifndef QDL_TC_SCALE_AHEAD
+// K blocks whose scales the Block128 scale warp has in flight: its global
+// reads wait out the memory latency of a loaded GPU (measured on the 256-row
+// gate/up projection: the scale reads one block ahead cost ~10 us of 83)
+#define QDL_TC_SCALE_AHEAD 4
+#endif
 #ifndef QDL_TC_FFMA2
 #define QDL_TC_FFMA2 1
 #endif
@@ -142,6 +151,9 @@ namespace {
 constexpr int kTileRows = 128;
 constexpr uint32_t kWBytes = kTileRows * 128;  // weight tile per stage
 constexpr uint32_t kWBox = 16 * 128;
+// totals staged in the freed stage ring at the end: [token][kRedStride] floats
+// (the 4-float pad puts the rows that one warp store covers in distinct banks)
+constexpr uint32_t kRedStride = kTileRows + 4;
 
 constexpr uint32_t pow2_at_least(uint32_t v) {
     uint32_t p = 32;
@@ -163,7 +175,7 @@ struct Tc {
     static constexpr int kStages = (int)(kBudget / kStage) < kMinStages ? kMinStages : (int)(kBudget / kStage);
     // Block128 accumulator buffers: the MMA may run kAcc-1 blocks ahead of
     // the epilogue that folds each block's scales
-    static constexpr int kAcc = kBlock ? (NTOK <= 64 ? 4 : 2) : 1;
+    static constexpr int kAcc = kBlock ? (NTOK <= 64 ? 4 : NTOK == 128 ? QDL_TC_ACC_128 : 2) : 1;
     static constexpr uint32_t kBarOff = kStages * kStage;
     static constexpr uint32_t kScaleOff = kBarOff + 512;  // Block128: [kAcc][kSBuf] block scales
     // Block128 epilogue fragments: 16x256b (a thread holds 4 rows x 2 token
@@ -178,7 +190,12 @@ struct Tc {
     // lanes of a quarter-warp read fall in different banks)
     static constexpr uint32_t kSRow = kFrag ? NTOK / 4 + 4 : NTOK;
     static constexpr uint32_t kSBuf = kFrag ? 4 * kSRow : NTOK;
-    static constexpr uint32_t kBytes = kScaleOff + (kBlock ? kAcc * kSBuf * 4 : 0);
+    // Block128: raw activation scales of kSAhead K blocks ahead, copied in by
+    // the scale warp ([kSAhead][kSStage]: NTOK tokens, then the block's weight scale)
+    static constexpr int kSAhead = QDL_TC_SCALE_AHEAD;
+    static constexpr uint32_t kSStage = NTOK + 4;
+    static constexpr uint32_t kStageOff = kScaleOff + (kBlock ? kAcc * kSBuf * 4 : 0);
+    static constexpr uint32_t kBytes = kStageOff + (kBlock ? kSAhead * kSStage * 4 : 0);
     static constexpr uint32_t kAlloc = kBytes + 1024;
     static constexpr int kEpiBase = kBlock ? 3 : 2;                          // first epilogue warp
     static constexpr int kEpi = kBlock ? (NTOK <= 64 ? 4 : NTOK == 256 ? QDL_TC_EPI_256 : NTOK / 16) : 4;  // epilogue warps
@@ -196,7 +213,7 @@ struct Tc {
     static constexpr int kMaxRegs = !kBlock ? 255 : NTOK == 32 ? QDL_TC_REGS_32 : NTOK == 256 ? QDL_TC_REGS_256 : 255;
     static constexpr uint32_t kTmemCols = pow2_at_least(kAcc * NTOK);
     static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
-    static_assert(kTileRows * NTOK * 4 <= kBarOff, "split-K partials must fit in the stage ring");
+    static_assert(NTOK * kRedStride * 4 <= kBarOff, "the staged totals must fit in the stage ring");
     static_assert(kTmemCols <= 512, "tensor memory");
     static_assert((2 * kStages + 3 * kAcc + 1) * 8 + 8 <= 512, "barrier area");
     static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
@@ -313,7 +330,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     volatile uint32_t *abort_flag = tmem_slot + 1;
     float *sbuf = reinterpret_cast<float *>(smem + C::kScaleOff);  // Block128: [kAcc][kSBuf] sa * sw
-    float *red = reinterpret_cast<float *>(smem);  // split-K partials [NTOK][128], reuse the ring at the end
+    float *red = reinterpret_cast<float *>(smem);  // totals [NTOK][kRedStride], in the ring at the end
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // token blocks of NTOK rows (more than one only beyond 256 rows): the
@@ -360,7 +377,6 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
     auto wait = [&](uint64_t *bar, uint32_t parity, uint32_t code) {
         if (!*abort_flag && !mbar_wait(bar, parity, a.wait_limit_ns)) fault(code);
     };
-
 
     // segment of this tile's first row (Block128 tiles never straddle segments)
     const float *tile_scale;
@@ -466,29 +482,42 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
         }
     } else if (kBlock && warp == 2) {
         // ------------------------------------------------------------ scale warp
-        // sa[token, kb] * sw[tile, kb] of each K block into sbuf[b], one block
-        // ahead in registers; lane l covers tokens l, l + 32, ...
-        constexpr int kPer = (NTOK + 31) / 32;
+        // sa[token, kb] * sw[tile, kb] of each K block into sbuf[b].  The raw
+        // scales of the next kSAhead blocks are in flight (cp.async into the
+        // stage ring); lane l covers tokens l, l + 32, ..., lane 0 the weight scale.
+        constexpr int kPer = (NTOK + 31) / 32, kD = C::kSAhead;
+        float *stage = reinterpret_cast<float *>(smem + C::kStageOff);
         grid_dep_wait();  // activation scales come from the previous kernel
-        auto load = [&](uint32_t it, float (&v)[kPer]) {
-            const uint32_t kb = kb0 + it;
-            const float sw = (it < niter && tile_row0 < a.n)
-                                 ? __ldg(tile_scale + (size_t)(tile_lrow0 >> 7) * a.kb + kb)
-                                 : 0.0f;
+        auto issue = [&](uint32_t it) {  // copies of block it into stage slot it % kD
+            if (it < niter) {
+                float *dst = stage + (it % kD) * C::kSStage;
+                const uint32_t kb = kb0 + it;
+#pragma unroll
+                for (int j = 0; j < kPer; ++j) {
+                    const uint32_t tok = 32 * j + lane;
+                    if (tok < m_loc) cp_async4(dst + tok, a.sa + (size_t)(tok0 + tok) * a.kb + kb);
+                }
+                if (lane == 0 && tile_row0 < a.n)
+                    cp_async4(dst + NTOK, tile_scale + (size_t)(tile_lrow0 >> 7) * a.kb + kb);
+            }
+            cp_async_commit();  // one group per block, empty past the end
+        };
+#pragma unroll
+        for (int d = 0; d < kD; ++d) issue((uint32_t)d);
+        for (uint32_t it = 0; it < niter; ++it) {
+            const uint32_t b = it % C::kAcc;
+            cp_async_wait<kD - 1>();  // this lane's copies of block it have landed
+            __syncwarp();             // ... and every lane's
+            const float *src = stage + (it % kD) * C::kSStage;
+            const float sw = tile_row0 < a.n ? src[NTOK] : 0.0f;
+            float cur[kPer];
 #pragma unroll
             for (int j = 0; j < kPer; ++j) {
                 const uint32_t tok = 32 * j + lane;
-                v[j] = (it < niter && tok < m_loc) ? ld_dep(a.sa + (size_t)(tok0 + tok) * a.kb + kb) * sw : 0.0f;
+                cur[j] = tok < m_loc ? src[tok] * sw : 0.0f;
             }
-        };
-        float next[kPer];
-        load(0, next);
-        for (uint32_t it = 0; it < niter; ++it) {
-            const uint32_t b = it % C::kAcc;
-            float cur[kPer];
-#pragma unroll
-            for (int j = 0; j < kPer; ++j) cur[j] = next[j];
-            load(it + 1, next);
+            __syncwarp();  // the slot is read before it is refilled
+            issue(it + kD);
             wait(&acce[b], ((it / C::kAcc) & 1) ^ 1, 64);  // the epilogue is done with sbuf[b]
 #pragma unroll
             for (int j = 0; j < kPer; ++j)
@@ -497,6 +526,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
             __syncwarp();
             if (lane == 0) mbar_arrive(&scal[b]);
         }
+        cp_async_wait<0>();  // no copy in flight when the CTA leaves
     } else {
         // ------------------------------------------------------------ epilogue
         const int e = warp - C::kEpiBase;
@@ -556,9 +586,46 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
         }
     };
 
+    // four consecutive outputs (tok, r .. r+3) of this token block, as one
+    // 16-byte store or reduction (8 bytes for bf16) where out is aligned for it
+    const uint32_t elt = a.out_bf16 ? 2u : 4u;
+    const bool vec4 = ((reinterpret_cast<uintptr_t>(a.out) | ((uintptr_t)a.ldc * elt)) & (4 * elt - 1)) == 0;
+    auto put4 = [&](uint32_t tok, uint32_t r, float4 v) {
+        if (vec4 && tok < m_loc && r + 4 <= a.n) {
+            const size_t o = (size_t)(tok0 + tok) * a.ldc + r;
+            float *of = reinterpret_cast<float *>(a.out) + o;
+            if (a.out_bf16) {
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+                uint2 u;
+                u.x = *reinterpret_cast<const uint32_t *>(&lo);
+                u.y = *reinterpret_cast<const uint32_t *>(&hi);
+                *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + o) = u;
+            } else if (add_out) {
+                red_add_v4(of, v);
+            } else if (a.accumulate) {
+                float4 w = *reinterpret_cast<const float4 *>(of);
+                w.x += v.x; w.y += v.y; w.z += v.z; w.w += v.w;
+                *reinterpret_cast<float4 *>(of) = w;
+            } else {
+                *reinterpret_cast<float4 *>(of) = v;
+            }
+            return;
+        }
+        const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (add_out)
+                add(tok, r + i, f[i]);
+            else
+                store(tok, r + i, f[i]);
+        }
+    };
+
     // ---------------------------------------------------------------- output
-    // Each epilogue thread owns one row and a range of token columns; with
-    // split > 1 it writes them to red[token][row] for the cluster reduction.
+    // Block128: every epilogue thread writes its totals to red[token][row] in
+    // the freed stage ring; then the epilogue warps write the block's outputs
+    // in 16-byte pieces, or (split > 1 without f32 reductions) the cluster
+    // reduction below reads them.  PerRow: each thread owns one row.
     if (warp >= C::kEpiBase) {
         const int e = warp - C::kEpiBase;
         const int quad = warp & 3;
@@ -570,13 +637,18 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
             for (int j = 0; j < kCpt; ++j) {
                 const uint32_t tok = cgrp * kCpt + frag_tok<C::kFrag>(j, lane);
                 const uint32_t jrow = 32 * quad + frag_row<C::kFrag>(j, lane);
-                if (split == 1)
-                    store(tok, tile_row0 + jrow, total[j]);
-                else if (add_out)
-                    add(tok, tile_row0 + jrow, total[j]);
-                else
-                    red[tok * kTileRows + jrow] = total[j];
+                red[tok * kRedStride + jrow] = total[j];
             }
+            if (split == 1 || add_out) {
+                // every epilogue warp's totals are in place
+                asm volatile("bar.sync 1, %0;" ::"r"(C::kEpi * 32) : "memory");
+                constexpr uint32_t kR4 = kTileRows / 4;
+                for (uint32_t idx = (uint32_t)e * 32 + lane; idx < m_loc * kR4; idx += C::kEpi * 32) {
+                    const uint32_t tok = idx / kR4, r4 = idx % kR4;
+                    put4(tok, tile_row0 + 4 * r4, *reinterpret_cast<const float4 *>(red + tok * kRedStride + 4 * r4));
+                }
+            }
+            (void)row;
         } else {
             // PerRow: scale the accumulator by sa[token] sw[row], 16 columns at a time
             const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16);
@@ -603,7 +675,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
                     else if (add_out)
                         add(tok, row, v[i] * s);
                     else
-                        red[tok * kTileRows + lrow] = v[i] * s;
+                        red[tok * kRedStride + lrow] = v[i] * s;
                 }
             }
             (void)e;
@@ -626,7 +698,7 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
             const uint32_t tok = idx / span, lr = r_lo + idx % span;
             float v[8];
 #pragma unroll
-            for (int rk = 0; rk < 8; ++rk) v[rk] = rk < (int)split ? peer[rk][tok * kTileRows + lr] : 0.0f;
+            for (int rk = 0; rk < 8; ++rk) v[rk] = rk < (int)split ? peer[rk][tok * kRedStride + lr] : 0.0f;
             float sum = 0.0f;
 #pragma unroll
             for (int rk = 0; rk < 8; ++rk) sum += v[rk];  // rank order; absent ranks add +0
@@ -818,30 +890,43 @@ __global__ void __launch_bounds__(Tc<NTOK, true>::kThreads, 1) __maxnreg__((Tc<N
         }
     } else if (warp == 2) {
         // ------------------------------------------------------------ scale warp
-        constexpr int kPer = (NTOK + 31) / 32;
+        // as in w8a8_gemm_tc_kernel: the raw scales of the next kSAhead units
+        // are in flight in the stage ring
+        constexpr int kPer = (NTOK + 31) / 32, kD = C::kSAhead;
+        float *stage = reinterpret_cast<float *>(smem + C::kStageOff);
         grid_dep_wait();
-        auto load = [&](uint32_t it, float (&v)[kPer]) {
-            const uint32_t u = u0 + it, tile = u / a.kb, kb = u % a.kb;
-            float sw = 0.0f;
+        auto issue = [&](uint32_t it) {  // copies of unit u0 + it into stage slot it % kD
             if (it < niter) {
-                const TileSeg t = tile_seg(tile);
-                sw = __ldg(t.scale + (size_t)(t.lrow0 >> 7) * a.kb + kb);
+                float *dst = stage + (it % kD) * C::kSStage;
+                const uint32_t u = u0 + it, kb = u % a.kb;
+#pragma unroll
+                for (int j = 0; j < kPer; ++j) {
+                    const uint32_t tok = 32 * j + lane;
+                    if (tok < a.m && tok < (uint32_t)NTOK) cp_async4(dst + tok, a.sa + (size_t)tok * a.kb + kb);
+                }
+                if (lane == 0) {
+                    const TileSeg t = tile_seg(u / a.kb);
+                    cp_async4(dst + NTOK, t.scale + (size_t)(t.lrow0 >> 7) * a.kb + kb);
+                }
             }
+            cp_async_commit();
+        };
+#pragma unroll
+        for (int d = 0; d < kD; ++d) issue((uint32_t)d);
+        for (uint32_t it = 0; it < niter; ++it) {
+            const uint32_t b = it % C::kAcc;
+            cp_async_wait<kD - 1>();
+            __syncwarp();
+            const float *src = stage + (it % kD) * C::kSStage;
+            const float sw = src[NTOK];
+            float cur[kPer];
 #pragma unroll
             for (int j = 0; j < kPer; ++j) {
                 const uint32_t tok = 32 * j + lane;
-                v[j] = (it < niter && tok < a.m && tok < (uint32_t)NTOK) ? ld_dep(a.sa + (size_t)tok * a.kb + kb) * sw
-                                                                      : 0.0f;
+                cur[j] = tok < a.m && tok < (uint32_t)NTOK ? src[tok] * sw : 0.0f;
             }
-        };
-        float next[kPer];
-        load(0, next);
-        for (uint32_t it = 0; it < niter; ++it) {
-            const uint32_t b = it % C::kAcc;
-            float cur[kPer];
-#pragma unroll
-            for (int j = 0; j < kPer; ++j) cur[j] = next[j];
-            load(it + 1, next);
+            __syncwarp();
+            issue(it + kD);
             wait(&acce[b], ((it / C::kAcc) & 1) ^ 1, 64);
 #pragma unroll
             for (int j = 0; j < kPer; ++j)
@@ -850,6 +935,7 @@ __global__ void __launch_bounds__(Tc<NTOK, true>::kThreads, 1) __maxnreg__((Tc<N
             __syncwarp();
             if (lane == 0) mbar_arrive(&scal[b]);
         }
+        cp_async_wait<0>();
     } else {
         // ------------------------------------------------------------ epilogue
         const int e = warp - C::kEpiBase;
