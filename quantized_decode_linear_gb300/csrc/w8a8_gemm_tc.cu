@@ -123,6 +123,14 @@ namespace cg = cooperative_groups;
 #ifndef QDL_TC_REGS_256
 #define QDL_TC_REGS_256 104  // one CTA of 19 warps: all the registers it can have
 #endif
+#ifndef QDL_STREAMK_OVERSUB_32
+// The 32-token stream-K grid, in multiples of its estimated resident CTAs
+// (3 per SM; 2 fit at its register count): 2 gives 912 CTAs, three even waves
+// of 304, and measured 47.5 -> 44.6 us per call on the K=8192, N=28672 gate/up
+// projection at M=32 (1.5x: 50.0, 3x: 49.9; the 64- and 128-token variants,
+// one CTA per SM, were slower with any oversubscription)
+#define QDL_STREAMK_OVERSUB_32 2
+#endif
 #ifndef QDL_TC_ACC_128
 #define QDL_TC_ACC_128 4  // accumulator buffers of the 128-token Block128 variants
 #endif
@@ -684,27 +692,32 @@ __global__ void __launch_bounds__(Tc<NTOK, kBlock>::kThreads, 1) __maxnreg__((Tc
     }
 
     if (split > 1 && !add_out) {
-        // rank r adds rows 128r/split .. 128(r+1)/split - 1 of every rank's
-        // partials, in rank order
+        // rank r adds the 4-row chunks 32r/split .. 32(r+1)/split - 1 of every
+        // rank's totals, in rank order, and writes them in 16-byte pieces
         cg::cluster_group cluster = cg::this_cluster();
         cluster.sync();
-        const uint32_t r_lo = (kTileRows * sidx) / split, r_hi = (kTileRows * (sidx + 1)) / split;
-        const uint32_t span = r_hi - r_lo;
-        const uint32_t m_used = m_loc;
+        constexpr uint32_t kR4 = kTileRows / 4;
+        const uint32_t c_lo = (kR4 * sidx) / split, c_hi = (kR4 * (sidx + 1)) / split;
+        const uint32_t span = c_hi - c_lo;
         const float *peer[8];
 #pragma unroll
         for (int rk = 0; rk < 8; ++rk) peer[rk] = cluster.map_shared_rank(red, rk < (int)split ? rk : 0);
-        for (uint32_t idx = threadIdx.x; idx < span * m_used; idx += blockDim.x) {
-            const uint32_t tok = idx / span, lr = r_lo + idx % span;
-            float v[8];
+        for (uint32_t idx = threadIdx.x; idx < span * m_loc; idx += blockDim.x) {
+            const uint32_t tok = idx / span, r4 = c_lo + idx % span;
+            float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-            for (int rk = 0; rk < 8; ++rk) v[rk] = rk < (int)split ? peer[rk][tok * kRedStride + lr] : 0.0f;
-            float sum = 0.0f;
-#pragma unroll
-            for (int rk = 0; rk < 8; ++rk) sum += v[rk];  // rank order; absent ranks add +0
-            store(tok, tile_row0 + lr, sum);
+            for (int rk = 0; rk < 8; ++rk) {  // rank order
+                if (rk < (int)split) {
+                    const float4 v = *reinterpret_cast<const float4 *>(peer[rk] + tok * kRedStride + 4 * r4);
+                    sum.x += v.x;
+                    sum.y += v.y;
+                    sum.z += v.z;
+                    sum.w += v.w;
+                }
+            }
+            put4(tok, tile_row0 + 4 * r4, sum);
         }
-        cluster.sync();  // no rank leaves while others still read its partials
+        cluster.sync();  // no rank leaves while others still read its totals
     }
 
     // ---------------------------------------------------------------- free the tensor memory
@@ -1138,6 +1151,7 @@ cudaError_t launch_streamk_variant(const W8A8Args &a, const CUtensorMap (&maps)[
         }
         p = slots[dev];
     }
+    if (NTOK == 32) p *= QDL_STREAMK_OVERSUB_32;
     const uint64_t units = (uint64_t)((a.n + kTileRows - 1) / kTileRows) * a.kb;
     if (units < p) p = (uint32_t)units;
     cudaLaunchConfig_t cfg = {};
