@@ -36,30 +36,31 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM traffic per launch of the dominant kernel from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and rows;
-# valid only while the kernel source hash matches.  Source: profiles/.
+# valid only while the hash of the kernel's code (comments excluded) matches.
+# Source: profiles/.
 TRAFFIC = {
     "w8a8_block128_gateup_k8192_n14336+14336@1": {"bytes": 235120896 + 147968, "file": "w8a8_gemm_tc.cu",
-                                                  "src": "72f2e8446a02ac0f"},
+                                                  "src": "26e11151993f3829"},
     "w8a8_block128_gateup_k8192_n14336+14336@2": {"bytes": 235229184 + 141824, "file": "w8a8_gemm_tc.cu",
-                                                  "src": "72f2e8446a02ac0f"},
+                                                  "src": "26e11151993f3829"},
     "w8a8_block128_gateup_k8192_n14336+14336@4": {"bytes": 235473408 + 114688, "file": "w8a8_gemm_tc.cu",
-                                                  "src": "72f2e8446a02ac0f"},
+                                                  "src": "26e11151993f3829"},
     "w8a8_block128_gateup_k8192_n14336+14336@8": {"bytes": 235969024 + 29696, "file": "w8a8_gemm_tc.cu",
-                                                  "src": "72f2e8446a02ac0f"},
+                                                  "src": "26e11151993f3829"},
     "w8a8_block128_gateup_k8192_n14336+14336@16": {"bytes": 236966144 + 72192, "file": "w8a8_gemm_tc.cu",
-                                                   "src": "72f2e8446a02ac0f"},
+                                                   "src": "26e11151993f3829"},
     "w8a8_block128_gateup_k8192_n14336+14336@32": {"bytes": 239198464 + 1731584, "file": "w8a8_gemm_tc.cu",
-                                                   "src": "72f2e8446a02ac0f"},
+                                                   "src": "26e11151993f3829"},
     "w8a8_block128_gateup_k8192_n14336+14336@64": {"bytes": 241420544 + 2837504, "file": "w8a8_gemm_tc.cu",
-                                                   "src": "72f2e8446a02ac0f"},
+                                                   "src": "26e11151993f3829"},
     "w8a8_block128_gateup_k8192_n14336+14336@128": {"bytes": 246659840 + 5896704, "file": "w8a8_gemm_tc.cu",
-                                                    "src": "72f2e8446a02ac0f"},
+                                                    "src": "26e11151993f3829"},
     "w8a8_block128_gateup_k8192_n14336+14336@256": {"bytes": 266619136 + 4536576, "file": "w8a8_gemm_tc.cu",
-                                                    "src": "72f2e8446a02ac0f"},
+                                                    "src": "26e11151993f3829"},
     "int4_awq_qkv_k4096_nq4096_nkv1024_g128@1": {"bytes": 14220800 + 0, "file": "int4_qkv_cc.cu",
-                                                 "src": "1918a975bcd9095e"},
+                                                 "src": "9a4ee01b88bafbf2"},
     "int4_awq_qkv_k4096_nq4096_nkv1024_g128@4": {"bytes": 14359296 + 0, "file": "int4_qkv_cc.cu",
-                                                 "src": "1918a975bcd9095e"},
+                                                 "src": "9a4ee01b88bafbf2"},
 }
 
 
@@ -131,11 +132,44 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text):
+    """C/CUDA source with comments removed and whitespace collapsed: what a
+    DRAM-traffic record depends on (string and character literals kept)"""
+    out, i, n, quote = [], 0, len(text), None
+    while i < n:
+        c = text[i]
+        if quote:
+            out.append(c)
+            if c == "\\" and i + 1 < n:
+                out.append(text[i + 1])
+                i += 2
+                continue
+            if c == quote:
+                quote = None
+            i += 1
+        elif c in "\"'":
+            quote = c
+            out.append(c)
+            i += 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def _src_hash(names):
+    """hash of the named csrc files' code, comments and layout excluded"""
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "quantized_decode_linear_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "quantized_decode_linear_gb300", "csrc", n), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

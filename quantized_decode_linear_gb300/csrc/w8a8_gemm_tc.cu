@@ -1,7 +1,7 @@
 // W8A8 decode GEMV / skinny GEMM on the 5th-generation tensor cores
 // (w8a8_decode.rs fn w8a8_gemv and fn w8a8_proj; segment routing from
 // W8a8Weight::boundaries; scale layouts from enum W8a8Scale).  One pass over
-// the weights for any token count up to 256.
+// the weights for any token count (token blocks of 256 beyond 256 rows).
 //
 //   y[m, j] = sum_kb Sa(m, kb) Sw(j, kb) sum_{k in kb} dec(q[m,k]) dec(W[j,k])
 //
@@ -16,15 +16,18 @@
 //                      N = NTOK tokens, K = 32 per instruction, four per
 //                      block) and commits each stage back to its `empty`
 //                      mbarrier.
-//   warp 2 (Block128): stages sa[m, kb] * sw[kb] for each K block in shared
-//                      memory for the epilogue (one buffer per accumulator).
+//   warp 2 (Block128): copies the raw scales of the next K blocks in with
+//                      cp.async and stages sa[m, kb] * sw[kb] for each block
+//                      in shared memory for the epilogue (one buffer per
+//                      accumulator).
 //   other warps      : epilogue, reading the f32 accumulators with tcgen05.ld.
 //
 // Scales.  PerRow: the accumulator sums the CTA's whole K range; the epilogue
 // multiplies by sa[m] sw[j].  Block128: each 128-block accumulates into one of
 // 2-4 TMEM buffers in turn; the epilogue folds a finished buffer into
-// register totals with sa[m, kb] sw[j/128, kb] while the tensor core fills
-// the next ones.
+// register totals with sa[m, kb] sw[j/128, kb] (packed f32x2 FMAs) while the
+// tensor core fills the next ones.  At the end the totals go through the
+// freed stage ring as [token][row] and leave in 16-byte pieces.
 //
 // Launch overlap.  Kernels are launched with programmatic stream
 // serialisation: the weight stream (independent of earlier kernels) starts at
@@ -33,10 +36,11 @@
 //
 // Split-K CTAs of one cluster reduce their partials through distributed shared
 // memory in rank order (deterministic), or, when the caller has zeroed an f32
-// output (the projection entry points), add them into it with f32 atomics
-// (no cluster barrier; the order of the additions varies from run to run).  Every wait is bounded; after a
-// timeout the CTA records a fault word, waits (bounded) for its copies and
-// MMAs in flight, frees its tensor memory and returns.
+// output (the projection entry points), add them into it with f32 reductions
+// (no cluster barrier; the order of the additions varies from run to run).
+// Every wait is bounded; after a timeout the CTA records a fault word, waits
+// (bounded) for its copies and MMAs in flight, frees its tensor memory and
+// returns.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
@@ -76,8 +80,9 @@ namespace cg = cooperative_groups;
 #ifndef QDL_TC_STAGE_BYTES_BIG
 #define QDL_TC_STAGE_BYTES_BIG (72 * 1024)
 #endif
-// token buckets in which the accumulating Block128 GEMV runs stream-K (at 256
-// tokens the f32 atomics of the shared tiles cost more than the balance wins)
+// token buckets in which the accumulating Block128 GEMV runs stream-K (a
+// 256-token stream-K variant spilled at its 96-register budget and measured
+// 2.6x slower than the split-K launch)
 // ... and for the Block128 64- and 128-token variants (the stream-K GEMV of
 // the f32 projection among them), one CTA per SM with a deeper ring: on the
 // K=8192, N=28672 gate/up projection, 7 stages of 24 KB took M=64 from 65.9
@@ -115,7 +120,7 @@ namespace cg = cooperative_groups;
 #define QDL_TC_INFLIGHT_256 16
 #endif
 #ifndef QDL_TC_REGS_32
-#define QDL_TC_REGS_32 96  // 3 CTAs of 7 warps
+#define QDL_TC_REGS_32 96  // (2 CTAs of 7 warps fit an SM at this count)
 #endif
 #ifndef QDL_TC_EPI_256
 #define QDL_TC_EPI_256 16  // epilogue warps of the 256-token Block128 variant

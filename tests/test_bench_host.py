@@ -41,6 +41,17 @@ def test_traffic_records_are_current_and_near_the_algorithmic_bytes():
         assert alg <= rec["bytes"] <= 1.03 * alg, (key, rec["bytes"], alg)
 
 
+def test_source_hash_covers_code_not_comments():
+    """a traffic record stays valid across comment and layout edits, not code edits"""
+    base = "int f(int x) {\n    return x + 1;  // one\n}\n/* block\n comment */\nconst char *s = \"a // b\";\n"
+    same = "int f(int x)\n{\n  return x + 1;  // another comment\n}\nconst char *s = \"a // b\";\n"
+    other = base.replace("x + 1", "x + 2")
+    lit = base.replace("a // b", "a // c")
+    assert bench._code_only(base) == bench._code_only(same)
+    assert bench._code_only(base) != bench._code_only(other)
+    assert bench._code_only(base) != bench._code_only(lit)  # a // inside a string literal is code
+
+
 def test_qkv_algorithmic_bytes():
     # 25,165,824 weight codes + 6,144 scales + 32,768 codes + 1,024 act scales + 196,608 output
     wl = syn.WORKLOADS["w8a8_block128_qkv_m8_k4096_n4096+1024+1024"]
