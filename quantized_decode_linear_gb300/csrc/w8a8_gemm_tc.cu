@@ -69,8 +69,12 @@ namespace cg = cooperative_groups;
 #define QDL_TC_EARLY_MAX_NTOK 16  // token buckets that release their dependents at the start
 #endif
 #ifndef QDL_TC_STAGE_BYTES_16
-// the 16-token variants: 3 stages of 18 KB, so that 4 CTAs share an SM and
-// the next call's early CTAs find free slots while this call streams
+// the 16-token variants: 3 stages of 18 KB.  With the scale staging a CTA
+// needs 57.4 KB (58.4 KB with the driver's reservation), so 3 share an SM; a
+// 256-byte smaller barrier area fits 4, which measured faster for the 25 MB
+// QKV projection at M = 8 (GEMV 5.82 -> 5.01 us) but slower for the 235 MB
+// gate/up projection at M = 1-16 (0.5-1 us per call), and requesting padded
+// shared memory for wide launches to keep those at 3 slowed its 16-row calls
 #define QDL_TC_STAGE_BYTES_16 (54 * 1024)
 #endif
 #ifndef QDL_TC_STAGE_BYTES
