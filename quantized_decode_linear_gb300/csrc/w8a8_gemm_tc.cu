@@ -124,21 +124,16 @@ namespace cg = cooperative_groups;
 #define QDL_TC_INFLIGHT_256 16
 #endif
 #ifndef QDL_TC_REGS_32
-#define QDL_TC_REGS_32 96  // (2 CTAs of 7 warps fit an SM at this count)
+// 80: 3 CTAs of 7 warps fit an SM (6 warps on some sub-partition); at 96 only
+// 2 fit.  Despite a small spill, 3 per SM in one even wave took the gate/up
+// projection at M = 32 from 43.9 to 40.3 us per call (2 per SM in three waves)
+#define QDL_TC_REGS_32 80
 #endif
 #ifndef QDL_TC_EPI_256
 #define QDL_TC_EPI_256 16  // epilogue warps of the 256-token Block128 variant
 #endif
 #ifndef QDL_TC_REGS_256
 #define QDL_TC_REGS_256 104  // one CTA of 19 warps: all the registers it can have
-#endif
-#ifndef QDL_STREAMK_OVERSUB_32
-// The 32-token stream-K grid, in multiples of its estimated resident CTAs
-// (3 per SM; 2 fit at its register count): 2 gives 912 CTAs, three even waves
-// of 304, and measured 47.5 -> 44.6 us per call on the K=8192, N=28672 gate/up
-// projection at M=32 (1.5x: 50.0, 3x: 49.9; the 64- and 128-token variants,
-// one CTA per SM, were slower with any oversubscription)
-#define QDL_STREAMK_OVERSUB_32 2
 #endif
 #ifndef QDL_TC_ACC_128
 #define QDL_TC_ACC_128 4  // accumulator buffers of the 128-token Block128 variants
@@ -1160,7 +1155,6 @@ cudaError_t launch_streamk_variant(const W8A8Args &a, const CUtensorMap (&maps)[
         }
         p = slots[dev];
     }
-    if (NTOK == 32) p *= QDL_STREAMK_OVERSUB_32;
     const uint64_t units = (uint64_t)((a.n + kTileRows - 1) / kTileRows) * a.kb;
     if (units < p) p = (uint32_t)units;
     cudaLaunchConfig_t cfg = {};
