@@ -39,24 +39,24 @@ FALLBACK_HBM_GBS = 6800.0
 # valid only while the hash of the kernel's code (comments excluded) matches.
 # Source: profiles/.
 TRAFFIC = {
-    "w8a8_block128_gateup_k8192_n14336+14336@1": {"bytes": 235105536 + 109824, "file": "w8a8_gemm_tc.cu",
-                                                  "src": "7d5d0b65da9dda09"},
-    "w8a8_block128_gateup_k8192_n14336+14336@2": {"bytes": 235233280 + 120320, "file": "w8a8_gemm_tc.cu",
-                                                  "src": "7d5d0b65da9dda09"},
-    "w8a8_block128_gateup_k8192_n14336+14336@4": {"bytes": 235474176 + 56320, "file": "w8a8_gemm_tc.cu",
-                                                  "src": "7d5d0b65da9dda09"},
-    "w8a8_block128_gateup_k8192_n14336+14336@8": {"bytes": 235967488 + 65280, "file": "w8a8_gemm_tc.cu",
-                                                  "src": "7d5d0b65da9dda09"},
-    "w8a8_block128_gateup_k8192_n14336+14336@16": {"bytes": 236956672 + 59136, "file": "w8a8_gemm_tc.cu",
-                                                   "src": "7d5d0b65da9dda09"},
-    "w8a8_block128_gateup_k8192_n14336+14336@32": {"bytes": 242564608 + 2281728, "file": "w8a8_gemm_tc.cu",
-                                                   "src": "7d5d0b65da9dda09"},
-    "w8a8_block128_gateup_k8192_n14336+14336@64": {"bytes": 241417984 + 2894592, "file": "w8a8_gemm_tc.cu",
-                                                   "src": "7d5d0b65da9dda09"},
-    "w8a8_block128_gateup_k8192_n14336+14336@128": {"bytes": 246654976 + 5884672, "file": "w8a8_gemm_tc.cu",
-                                                    "src": "7d5d0b65da9dda09"},
-    "w8a8_block128_gateup_k8192_n14336+14336@256": {"bytes": 266664192 + 4554752, "file": "w8a8_gemm_tc.cu",
-                                                    "src": "7d5d0b65da9dda09"},
+    "w8a8_block128_gateup_k8192_n14336+14336@1": {"bytes": 235109632 + 170752, "file": "w8a8_gemm_tc.cu",
+                                                  "src": "c94992fe805862c4"},
+    "w8a8_block128_gateup_k8192_n14336+14336@2": {"bytes": 235226368 + 124416, "file": "w8a8_gemm_tc.cu",
+                                                  "src": "c94992fe805862c4"},
+    "w8a8_block128_gateup_k8192_n14336+14336@4": {"bytes": 235474944 + 378880, "file": "w8a8_gemm_tc.cu",
+                                                  "src": "c94992fe805862c4"},
+    "w8a8_block128_gateup_k8192_n14336+14336@8": {"bytes": 235969536 + 74752, "file": "w8a8_gemm_tc.cu",
+                                                  "src": "c94992fe805862c4"},
+    "w8a8_block128_gateup_k8192_n14336+14336@16": {"bytes": 236955904 + 123136, "file": "w8a8_gemm_tc.cu",
+                                                   "src": "c94992fe805862c4"},
+    "w8a8_block128_gateup_k8192_n14336+14336@32": {"bytes": 242545664 + 2216704, "file": "w8a8_gemm_tc.cu",
+                                                   "src": "c94992fe805862c4"},
+    "w8a8_block128_gateup_k8192_n14336+14336@64": {"bytes": 245203200 + 3141120, "file": "w8a8_gemm_tc.cu",
+                                                   "src": "c94992fe805862c4"},
+    "w8a8_block128_gateup_k8192_n14336+14336@128": {"bytes": 246682112 + 5856768, "file": "w8a8_gemm_tc.cu",
+                                                    "src": "c94992fe805862c4"},
+    "w8a8_block128_gateup_k8192_n14336+14336@256": {"bytes": 266647808 + 4793344, "file": "w8a8_gemm_tc.cu",
+                                                    "src": "c94992fe805862c4"},
     "int4_awq_qkv_k4096_nq4096_nkv1024_g128@1": {"bytes": 14220800 + 0, "file": "int4_qkv_cc.cu",
                                                  "src": "9a4ee01b88bafbf2"},
     "int4_awq_qkv_k4096_nq4096_nkv1024_g128@4": {"bytes": 14359296 + 0, "file": "int4_qkv_cc.cu",

@@ -88,17 +88,18 @@ namespace cg = cooperative_groups;
 // 256-token stream-K variant spilled at its 96-register budget and measured
 // 2.6x slower than the split-K launch)
 // ... and for the Block128 64- and 128-token variants (the stream-K GEMV of
-// the f32 projection among them), one CTA per SM with a deeper ring: on the
-// K=8192, N=28672 gate/up projection, 7 stages of 24 KB took M=64 from 65.9
-// to 59.3 us (2 CTAs of 3 stages before; 5 stages 61.8, 8 stages 60.0), and 4
-// stages of 32 KB took M=128 from 77.0 to 72.2 us (6 stages 75.4).  Deeper
-// rings measured no better for the 32-token variant (48.0 vs 48.4 us at
-// M=32) and slower for the per-row and 256-token variants.
+// the f32 projection among them).  128 tokens: one CTA per SM with 4 stages
+// of 32 KB took the K=8192, N=28672 gate/up projection at M=128 from 77.0 to
+// 72.2 us (6 stages 75.4).  64 tokens: 3 stages of 24 KB with the registers
+// capped at 128, so that 2 CTAs share an SM, took M=64 from 52.8 to 47.0 us
+// per call against one CTA of 7 stages at 210 registers (2 CTAs of 4
+// stages: 54.7).  Deeper rings measured no better for the 32-token variant
+// (48.0 vs 48.4 us at M=32) and slower for the per-row and 256-token variants.
 #ifndef QDL_TC_STAGE_BYTES_B128
 #define QDL_TC_STAGE_BYTES_B128 (144 * 1024)
 #endif
 #ifndef QDL_TC_STAGE_BYTES_B64
-#define QDL_TC_STAGE_BYTES_B64 (168 * 1024)
+#define QDL_TC_STAGE_BYTES_B64 (72 * 1024)
 #endif
 #ifndef QDL_TC_ADD_NOCLUSTER
 #define QDL_TC_ADD_NOCLUSTER 1
@@ -131,6 +132,9 @@ namespace cg = cooperative_groups;
 #endif
 #ifndef QDL_TC_EPI_256
 #define QDL_TC_EPI_256 16  // epilogue warps of the 256-token Block128 variant
+#endif
+#ifndef QDL_TC_REGS_64
+#define QDL_TC_REGS_64 128  // 2 CTAs of 7 warps per SM (a small spill in the stream-K variant)
 #endif
 #ifndef QDL_TC_REGS_256
 #define QDL_TC_REGS_256 104  // one CTA of 19 warps: all the registers it can have
@@ -218,11 +222,10 @@ struct Tc {
         kCpt < (NTOK <= 64 ? QDL_TC_INFLIGHT_SMALL : NTOK == 128 ? QDL_TC_INFLIGHT_128 : QDL_TC_INFLIGHT_256)
             ? kCpt
             : (NTOK <= 64 ? QDL_TC_INFLIGHT_SMALL : NTOK == 128 ? QDL_TC_INFLIGHT_128 : QDL_TC_INFLIGHT_256);
-    // register cap per thread, so that several CTAs fit an SM (255: none)
-    // (the 64-token Block128 variants run one CTA per SM with their deep ring,
-    // so they take all the registers they need: a cap of 144 spilled, and
-    // lifting it took the gate/up projection at M = 64 from 59.3 to 54.9 us)
-    static constexpr int kMaxRegs = !kBlock ? 255 : NTOK == 32 ? QDL_TC_REGS_32 : NTOK == 256 ? QDL_TC_REGS_256 : 255;
+    // register cap per thread, so that several CTAs fit an SM (255: none):
+    // 32 tokens 3 per SM, 64 tokens 2 per SM (warps per SM sub-partition x 32
+    // x registers must stay within its 16K registers)
+    static constexpr int kMaxRegs = !kBlock ? 255 : NTOK == 32 ? QDL_TC_REGS_32 : NTOK == 64 ? QDL_TC_REGS_64 : NTOK == 256 ? QDL_TC_REGS_256 : 255;
     static constexpr uint32_t kTmemCols = pow2_at_least(kAcc * NTOK);
     static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
     static_assert(NTOK * kRedStride * 4 <= kBarOff, "the staged totals must fit in the stage ring");
