@@ -140,7 +140,9 @@ namespace cg = cooperative_groups;
 #define QDL_TC_REGS_256 104  // one CTA of 19 warps: all the registers it can have
 #endif
 #ifndef QDL_TC_ACC_128
-#define QDL_TC_ACC_128 4  // accumulator buffers of the 128-token Block128 variants
+// accumulator buffers of the 128-token Block128 variants (4 and 2 measured
+// the same on the gate/up projection at M = 128: 62.2 and 62.3 us per call)
+#define QDL_TC_ACC_128 4
 #endif
 #ifndef QDL_TC_SCALE_AHEAD
 // K blocks whose scales the Block128 scale warp has in flight: its global
@@ -149,8 +151,13 @@ namespace cg = cooperative_groups;
 #define QDL_TC_SCALE_AHEAD 4
 #endif
 #ifndef QDL_TC_FFMA2
+// Block128 folds as packed f32x2 FMAs (0: scalar FMAs, same rounding): M = 128
+// 85.9 -> 75.2 us and M = 256 103.5 -> 93.9 us per call with the 32x32b and
+// 16x256b fragments respectively
 #define QDL_TC_FFMA2 1
 #endif
+// token buckets from which the Block128 fold reads tensor memory in the
+// 16x256b shape (see Tc::kFrag)
 #ifndef QDL_TC_FRAG_MIN_NTOK
 #define QDL_TC_FRAG_MIN_NTOK 128
 #endif
