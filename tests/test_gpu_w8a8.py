@@ -129,6 +129,28 @@ def test_bf16_output(fmt):
     check_close(host(out.float()), yo, bo, extra_rel=BF16_REL, what="bf16 out")
 
 
+@pytest.mark.parametrize("fmt", [qdl.PER_ROW, qdl.BLOCK128])
+@pytest.mark.parametrize("rows", [9, 100])
+def test_bf16_output_unaligned_rows(fmt, rows):
+    """bf16 output with a row stride of N + 3 elements: rows that start off an
+    8-byte boundary take the element-wise stores, ragged N included; columns
+    past N are not written"""
+    k = 512
+    segs = _segments(fmt, k, _aligned_sizes(fmt, [256, 130]), seed=rows + 7)
+    x = syn.bf16_normal((rows, k), seed=rows + 8)
+    qo, so = oracle.act_quant(fmt, x, k)
+    yo, bo = oracle.w8a8_gemv(fmt, qo, so, segs)
+    w, _keep = upload_weight(segs, fmt)
+    ldc = w.n + 3
+    out = torch.full((rows, ldc), -5.0, dtype=torch.bfloat16, device="cuda")
+    q, s = scratch(rows, k, fmt)
+    qdl.w8a8_proj(w, bf16_dev(x), rows, out, q, s, out_dtype=qdl.OUT_BF16, ldc=ldc)
+    torch.cuda.synchronize()
+    o = host(out.float())
+    assert np.all(o[:, w.n:] == -5.0), "columns past N were written"
+    check_close(o[:, :w.n], yo, bo, extra_rel=BF16_REL, what=f"bf16 ldc=N+3 fmt={fmt} rows={rows}")
+
+
 def test_segment_identities_on_gpu():
     """3 segments == 3 single-segment calls concatenated; rows == single-row calls"""
     fmt, k, rows = qdl.BLOCK128, 256, 5
